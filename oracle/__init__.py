@@ -1,0 +1,233 @@
+"""Python access to the C oracle (``ss2_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only callers.  The CUDA library and its
+Python binding never import this package.
+
+``build()`` compiles the oracle with contraction off into ``oracle/_build``;
+``lib()`` loads it.  The wrappers below marshal numpy arrays only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+BUILD_DIR = os.path.join(HERE, "_build")
+SO_PATH = os.path.join(BUILD_DIR, "libss2_oracle.so")
+SOURCES = [os.path.join(HERE, "ss2_oracle.c")]
+HEADERS = [os.path.join(HERE, "ss2_oracle.h")]
+
+NPARAMS = 133
+NVALUES = 108
+EOTF_N = 4096
+P_WEIGHTS, P_POLY, P_POWER, P_OPSIN, P_BIAS, P_AFFINE, P_C2 = 0, 108, 112, 115, 124, 127, 132
+
+CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+          "-Wall", "-Wextra"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _stale() -> bool:
+    if not os.path.exists(SO_PATH):
+        return True
+    t = os.path.getmtime(SO_PATH)
+    return any(os.path.getmtime(p) > t for p in SOURCES + HEADERS)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (gcc, contraction off)."""
+    if force or _stale():
+        os.makedirs(BUILD_DIR, exist_ok=True)
+        tmp = SO_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", *CFLAGS, "-shared", "-o", tmp, *SOURCES, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, SO_PATH)
+    return SO_PATH
+
+
+class Dump(ctypes.Structure):
+    _fields_ = [
+        ("scale", ctypes.c_int),
+        ("lin", ctypes.c_void_p),
+        ("xyb", ctypes.c_void_p),
+        ("hblur", ctypes.c_void_p),
+        ("blur", ctypes.c_void_p),
+        ("terms", ctypes.c_void_p),
+        ("sums", ctypes.c_void_p),
+    ]
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(SO_PATH)
+            vp, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+            L.ss2o_default_params.argtypes = [vp]
+            L.ss2o_score.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, ctypes.POINTER(Dump)]
+            L.ss2o_score.restype = i
+            L.ss2o_score_frames.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp]
+            L.ss2o_score_frames.restype = i
+            L.ss2o_frame_bytes.argtypes = [i, i, i, i]
+            L.ss2o_frame_bytes.restype = ctypes.c_size_t
+            L.ss2o_scale_dims.argtypes = [i, i, vp, vp]
+            L.ss2o_scale_dims.restype = i
+            L.ss2o_cbrtf_cr.argtypes = [ctypes.c_float]
+            L.ss2o_cbrtf_cr.restype = ctypes.c_float
+            L.ss2o_cbrtf_cr_array.argtypes = [vp, vp, ctypes.c_longlong]
+            L.ss2o_eotf_table.argtypes = [vp]
+            L.ss2o_eotf_lookup.argtypes = [vp, ctypes.c_float]
+            L.ss2o_eotf_lookup.restype = ctypes.c_float
+            L.ss2o_yuv_coeffs.argtypes = [vp]
+            L.ss2o_iir_coeffs.argtypes = [vp, vp, vp]
+            L.ss2o_blur_line.argtypes = [vp, i, vp]
+            L.ss2o_downsample.argtypes = [vp, i, i, vp]
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def default_params() -> np.ndarray:
+    p = np.zeros(NPARAMS, np.float64)
+    lib().ss2o_default_params(_ptr(p))
+    return p
+
+
+def frame_bytes(w: int, h: int, depth: int, chroma: int) -> int:
+    return int(lib().ss2o_frame_bytes(w, h, depth, chroma))
+
+
+def scale_dims(w: int, h: int) -> list[tuple[int, int]]:
+    ws = np.zeros(6, np.int32)
+    hs = np.zeros(6, np.int32)
+    n = lib().ss2o_scale_dims(w, h, _ptr(ws), _ptr(hs))
+    return [(int(ws[k]), int(hs[k])) for k in range(n)]
+
+
+def score(ref: np.ndarray, dis: np.ndarray, w: int, h: int, depth: int,
+          chroma: int, params: np.ndarray | None = None, dump_scale: int | None = None):
+    """Scores one frame pair.  Returns (score, values[108], dump dict or None)."""
+    params = default_params() if params is None else np.ascontiguousarray(params, np.float64)
+    ref = np.ascontiguousarray(ref)
+    dis = np.ascontiguousarray(dis)
+    fb = frame_bytes(w, h, depth, chroma)
+    assert ref.nbytes == fb and dis.nbytes == fb, (ref.nbytes, fb)
+    sc = np.zeros(1, np.float64)
+    vals = np.zeros(NVALUES, np.float64)
+    dump = None
+    dptr = None
+    if dump_scale is not None:
+        dims = scale_dims(w, h)
+        if dump_scale < len(dims):
+            sw, sh = dims[dump_scale]
+        else:
+            sw, sh = 1, 1
+        ns = sw * sh
+        dump = {
+            "lin": np.zeros((6, sh, sw), np.float32),
+            "xyb": np.zeros((6, sh, sw), np.float32),
+            "hblur": np.zeros((15, sh, sw), np.float32),
+            "blur": np.zeros((15, sh, sw), np.float32),
+            "terms": np.zeros((18, sh, sw), np.float64),
+            "sums": np.zeros(18, np.float64),
+        }
+        d = Dump(dump_scale, *(dump[k].ctypes.data for k in
+                               ("lin", "xyb", "hblur", "blur", "terms", "sums")))
+        dptr = ctypes.byref(d)
+        _ = ns
+    rc = lib().ss2o_score(_ptr(ref), _ptr(dis), w, h, depth, chroma, _ptr(params),
+                          _ptr(sc), _ptr(vals), dptr)
+    if rc != 0:
+        raise ValueError(f"oracle rejected geometry {w}x{h} depth {depth} chroma {chroma}: rc={rc}")
+    return float(sc[0]), vals, dump
+
+
+def score_frames(ref: np.ndarray, dis: np.ndarray, w: int, h: int, depth: int,
+                 chroma: int, params: np.ndarray | None = None):
+    """Scores n packed frames; ref/dis shaped (n, frame_elems).  Returns (scores, values)."""
+    params = default_params() if params is None else np.ascontiguousarray(params, np.float64)
+    ref = np.ascontiguousarray(ref)
+    dis = np.ascontiguousarray(dis)
+    n = ref.shape[0]
+    sc = np.zeros(n, np.float64)
+    vals = np.zeros((n, NVALUES), np.float64)
+    rc = lib().ss2o_score_frames(_ptr(ref), _ptr(dis), n, w, h, depth, chroma,
+                                 _ptr(params), _ptr(sc), _ptr(vals))
+    if rc != 0:
+        raise ValueError(f"oracle rejected geometry: rc={rc}")
+    return sc, vals
+
+
+def cbrtf_cr(x: float) -> float:
+    return float(lib().ss2o_cbrtf_cr(ctypes.c_float(x)))
+
+
+def cbrtf_cr_array(x: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """The oracle's cube root over a float32 array, split across threads
+    (ctypes releases the GIL during the call)."""
+    import concurrent.futures as cf
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty_like(x)
+    L = lib()
+    nt = max(1, threads or os.cpu_count() or 1)
+    bounds = np.linspace(0, x.size, nt + 1, dtype=np.int64)
+
+    def run(k):
+        a, b = int(bounds[k]), int(bounds[k + 1])
+        if b > a:
+            L.ss2o_cbrtf_cr_array(x.ctypes.data + 4 * a, out.ctypes.data + 4 * a, b - a)
+
+    with cf.ThreadPoolExecutor(max_workers=nt) as ex:
+        list(ex.map(run, range(nt)))
+    return out
+
+
+def eotf_table() -> np.ndarray:
+    t = np.zeros(EOTF_N + 1, np.float32)
+    lib().ss2o_eotf_table(_ptr(t))
+    return t
+
+
+def eotf_lookup(v: float) -> float:
+    t = eotf_table()
+    return float(lib().ss2o_eotf_lookup(_ptr(t), ctypes.c_float(v)))
+
+
+def yuv_coeffs() -> np.ndarray:
+    k = np.zeros(4, np.float32)
+    lib().ss2o_yuv_coeffs(_ptr(k))
+    return k
+
+
+def iir_coeffs():
+    a = np.zeros(3, np.float64)
+    c2 = np.zeros(3, np.float32)
+    g = np.zeros(3, np.float32)
+    lib().ss2o_iir_coeffs(_ptr(a), _ptr(c2), _ptr(g))
+    return a, c2, g
+
+
+def blur_line(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.zeros_like(x)
+    lib().ss2o_blur_line(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def downsample(plane: np.ndarray) -> np.ndarray:
+    plane = np.ascontiguousarray(plane, np.float32)
+    h, w = plane.shape
+    out = np.zeros(((h + 1) // 2, (w + 1) // 2), np.float32)
+    lib().ss2o_downsample(_ptr(plane), w, h, _ptr(out))
+    return out

@@ -1,0 +1,96 @@
+/*
+ * ss2_oracle.h — plain, slow, single-threaded CPU reference of the per-frame
+ * SSIMULACRA2 scoring pipeline.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this code.  The CUDA library never
+ * links, includes or calls it, and it shares no code with the CUDA library.
+ *
+ * Source of the method: "Research-1363: Device-resident ssimulacra2 and a
+ * single-wait MS-SSIM on SYCL" (vmafx documentation), sections "Sources"
+ * (the list of CPU pipeline steps) and "Findings" 2-4 (contraction-off fp32
+ * pipeline, fp64 per-pixel terms summed in sequential order, six sums per
+ * channel).  Where the page is silent the plainest reading is taken; every
+ * such reading is listed in the repository's design notes and restated at
+ * the function that takes it.
+ *
+ * Parity pins: every function here is pinned by a CPU test against something
+ * other than itself (closed forms, exact integer arithmetic, brute force,
+ * invariants); the one exception is the absolute SSIMULACRA2 score scale,
+ * which depends on tuned constants the pages do not give — parity unpinned
+ * for the absolute score values (GPU-vs-oracle parity does not depend on them).
+ *
+ * Build: any C99 compiler with contraction OFF (-ffp-contract=off), no
+ * fast-math.  Products are kept in named temporaries so each rounding is the
+ * one written.
+ */
+#ifndef SS2_ORACLE_H
+#define SS2_ORACLE_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Parameter vector layout (doubles).  Values used in the fp32 pipeline are
+ * rounded to float once, at the start of a call.                            */
+#define SS2O_P_WEIGHTS 0    /* 108 pooling weights, index ((c*6+s)*2+n)*3+k */
+#define SS2O_P_POLY 108     /* p0..p3: score = p0 + p1 P + p2 P^2 + p3 P^3  */
+#define SS2O_P_POWER 112    /* alpha, beta, gamma: s > 0 -> alpha s^beta + gamma */
+#define SS2O_P_OPSIN 115    /* 3x3 opsin mixing matrix, row-major            */
+#define SS2O_P_BIAS 124     /* 3 opsin biases                                */
+#define SS2O_P_AFFINE 127   /* sx, ox, oy, sb, ob                            */
+#define SS2O_P_C2 132       /* SSIM stabiliser C2                            */
+#define SS2O_NPARAMS 133
+
+#define SS2O_NVALUES 108
+#define SS2O_NSCALES 6
+#define SS2O_EOTF_N 4096    /* table has SS2O_EOTF_N + 1 entries            */
+#define SS2O_IIR_R 4        /* kernel support |m| <= R; zeros at +-(R+1)    */
+
+/* Optional stage dump of one scale (any pointer may be NULL).               */
+typedef struct {
+    int scale;      /* scale to dump; a scale that is not computed dumps nothing */
+    float *lin;     /* 6 planes w_s*h_s: ref R,G,B then dis R,G,B (linear)   */
+    float *xyb;     /* 6 planes: ref X,Y,B then dis X,Y,B (after the affine) */
+    float *hblur;   /* 15 planes: per channel c, (mu1, mu2, s11, s22, s12)
+                       after the horizontal pass only                         */
+    float *blur;    /* 15 planes, same order, after both passes              */
+    double *terms;  /* 18 planes: per channel, d, d^4, art, art^4, det, det^4 */
+    double *sums;   /* 18 sequential sums, same order                        */
+} ss2o_dump;
+
+/* Writes the default parameter vector (placeholders for the tuned pooling
+ * weights, map and make-positive affine; see the header of the .c file).   */
+void ss2o_default_params(double *params);
+
+/* Scores one frame pair.  ref/dis: one packed planar frame each
+ * (Y, then U, then V; uint8 for depth 8, little-endian uint16 otherwise).
+ * values (108 doubles) and dump may be NULL.  Returns 0, or -22 (EINVAL)
+ * for a geometry the pipeline rejects.                                       */
+int ss2o_score(const void *ref, const void *dis, int width, int height,
+               int bitdepth, int chroma, const double *params,
+               double *score, double *values, const ss2o_dump *dump);
+
+/* Scores n packed frames (each frame_bytes long) one after another.         */
+int ss2o_score_frames(const void *ref, const void *dis, int n_frames,
+                      int width, int height, int bitdepth, int chroma,
+                      const double *params, double *scores, double *values);
+
+/* Building blocks, exported for the pins. */
+size_t ss2o_frame_bytes(int width, int height, int bitdepth, int chroma);
+int ss2o_scale_dims(int width, int height, int *ws, int *hs); /* -> #scales */
+float ss2o_cbrtf_cr(float x);
+void ss2o_cbrtf_cr_array(const float *x, float *y, long long n);
+void ss2o_eotf_table(float *table);            /* SS2O_EOTF_N + 1 floats */
+float ss2o_eotf_lookup(const float *table, float v);
+void ss2o_yuv_coeffs(float *coeffs);           /* cr_r, cb_g, cr_g, cb_b */
+void ss2o_iir_coeffs(double *a, float *c2, float *g); /* 3 each */
+void ss2o_blur_line(const float *in, int n, float *out);
+void ss2o_downsample(const float *in, int w, int h, float *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
