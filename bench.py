@@ -1,0 +1,383 @@
+"""Benchmark: SSIMULACRA2 frames/s at 3840x2160 8-bit 4:2:0 on one GB300.
+
+A step scores the whole 50-frame 3840x2160 8-bit 4:2:0 workload (the
+synthetic stand-in for the pages' Big Buck Bunny 4K fixture) through the
+C ABI.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+--impl ours (default): frames resident in HBM, W untimed steps, then K steps
+timed with CUDA events on the scoring stream between a barrier and a
+synchronize on both sides (max over ranks).  The inputs (1.24 GB of YUV per
+step) and the workspace traffic (tens of GB per step) are far larger than
+L2.  Per-kernel CUDA events inside the library give the dominant kernel's
+average launch time for the roofline; nvidia-smi samples the clocks during
+the timed region; e2e repeats the measurement through the host-input entry
+point with pinned host buffers (upload and 8-byte-per-frame read-back
+inside the timed region).  The oracle, timed on the host cores over a
+bounded sample, is the CPU baseline.
+
+--impl reference: the oracle (plain single-threaded C, one thread per frame
+across the host cores) on a bounded sample per step; the same metric.
+
+Under torchrun every rank scores its own copy of the workload (frames are
+independent: weak scaling, no data-path collective); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "SSIMULACRA2 frames/sec at 3840x2160 8-bit 4:2:0; HBM GB/s vs GB300 peak"
+DEFAULT_WORKLOAD = "c3_3840x2160_8b_420"
+KERNELS = ("k_pyramid", "k_hblur", "k_vblur", "k_finalize")
+
+
+# ---------------------------------------------------------------------------
+# byte models (stated in the design doc)
+# ---------------------------------------------------------------------------
+
+def scale_dims(w: int, h: int) -> list[tuple[int, int]]:
+    out = []
+    while len(out) < 6 and w >= 8 and h >= 8:
+        out.append((w, h))
+        w, h = (w + 1) // 2, (h + 1) // 2
+    return out
+
+
+def byte_model(spec) -> dict:
+    """Algorithmic bytes per frame: the pipeline minimum B_min and per kernel."""
+    dims = scale_dims(spec.width, spec.height)
+    ns = [w * h for w, h in dims]
+    sum_n = sum(ns)
+    yuv_pair = 2 * synth.frame_elems(spec.width, spec.height, spec.chroma) * (1 if spec.depth == 8 else 2)
+    b_min = yuv_pair + 192 * sum_n + 48 * sum(ns[:-1]) if len(ns) > 1 else yuv_pair + 192 * sum_n
+    return {
+        "sum_n": sum_n,
+        "b_min": b_min,
+        # YUV pair read once, 6 XYB planes written at every scale
+        "k_pyramid": yuv_pair + 24 * sum_n,
+        # 6 XYB planes read, 15 horizontally blurred planes written
+        "k_hblur": (24 + 60) * sum_n,
+        # 15 blurred planes + 6 XYB planes read (the sums stay on chip)
+        "k_vblur": (60 + 24) * sum_n,
+        "k_finalize": 0,
+    }
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle leg
+# ---------------------------------------------------------------------------
+
+def oracle_throughput(wl, n_frames: int, threads: int) -> tuple[float, float]:
+    """Oracle frames/s over n_frames frames, `threads` frames at a time."""
+    import concurrent.futures as cf
+
+    import oracle
+    oracle.build()
+    sp = wl.spec
+    idx = [i % wl.ref.shape[0] for i in range(n_frames)]
+
+    def one(j):
+        return oracle.score(wl.ref[j], wl.dis[j], sp.width, sp.height, sp.depth, sp.chroma)[0]
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, idx))
+    dt = time.perf_counter() - t0
+    return n_frames / dt, dt
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (N > 1: one process per GPU under torchrun)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    spec = synth.SPECS[args.workload]
+    cores = host_cores()
+    per_step = max(1, min(cores, 16))
+    wl = synth.make(args.workload, per_step, workers=min(per_step, cores))
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; the first step pays nothing extra
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_throughput(wl, per_step, per_step)
+    dt = time.perf_counter() - t0
+    fps = per_step * args.steps / dt
+    sample = (f"{per_step} frames of {spec.name} per step, one oracle thread per frame "
+              f"on {per_step} host cores")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32+f64", "data": "synthetic",
+        "config": {"workload": spec.name, "frames_per_step": per_step},
+        "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": per_step,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, ws, rank, local):
+    spec = synth.SPECS[args.workload]
+    # generate before any CUDA work (the pool is spawned)
+    wl = synth.make(args.workload, workers=min(16, host_cores()))
+    import torch
+    import torch.distributed as dist
+
+    from ssimulacra2_image_scoring_gb300 import Scorer
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ref = torch.from_numpy(wl.ref).to(dev)
+    dis = torch.from_numpy(wl.dis).to(dev)
+    n = spec.frames
+    sc = Scorer(spec.width, spec.height, spec.depth, spec.chroma)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        sc.score(ref, dis, stream)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    sc.profile_begin()
+    start.record(stream)
+    for _ in range(args.steps):
+        scores = sc.score(ref, dis, stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    prof = sc.profile_end()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, ws)
+    ms_step = ms_total / args.steps
+    value = n * ws * args.steps / (ms_total / 1000.0)
+
+    # roofline of the dominant kernel
+    bm = byte_model(spec)
+    dom = max(KERNELS, key=lambda k: prof[k][0])
+    dom_ms, dom_launches = prof[dom]
+    frames_per_launch = n * args.steps / max(1, dom_launches)
+    algo_bytes_launch = bm[dom] * frames_per_launch
+    achieved_gbs = algo_bytes_launch / (dom_ms / dom_launches / 1000.0) / 1e9
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        peaks = {}
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured"
+    if not peak:
+        peak, peak_src = 6800.0, "fallback"
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            with open(tfile) as f:
+                tj = json.load(f)
+            if tj.get("kernel") == dom and tj.get("workload") == spec.name:
+                traffic = tj.get("bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+
+    # e2e through the host-input entry point from pinned memory
+    pr = torch.from_numpy(wl.ref).pin_memory()
+    pd = torch.from_numpy(wl.dis).pin_memory()
+    sc.score_host(pr, pd, stream)  # allocates the upload slots once
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(max(1, args.steps)):
+        sc.score_host(pr, pd, stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, ws)
+    e2e_fps = n * ws * max(1, args.steps) / e2e_s
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cores = host_cores()
+        k = max(1, min(cores, 16))
+        fps_cpu, dt_cpu = oracle_throughput(wl, k, k)
+        cpu = {"value": fps_cpu, "unit": "frames/s", "cores": k, "kind": "oracle",
+               "sample": f"{k} frames of {spec.name} (frames 0..{k - 1}), one oracle thread "
+                         f"per frame on {k} host cores, {dt_cpu:.1f} s"}
+
+    gpu_launches = sum(prof[k][1] for k in KERNELS)
+    per_kernel = {k: {"ms_total": prof[k][0], "launches": prof[k][1],
+                      "share": prof[k][0] / max(1e-9, sum(prof[j][0] for j in KERNELS))}
+                  for k in KERNELS}
+    pipe_gbs = bm["b_min"] * value / ws / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": spec.name, "frames_per_step": n, "batch": sc.batch,
+                   "l2": "inputs larger than L2 (YUV 1.24 GB per step, workspace "
+                         f"{sc.workspace_bytes / 1e9:.1f} GB)"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved_gbs, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved_gbs / peak,
+                     "traffic": traffic,
+                     "algo_bytes_per_launch": algo_bytes_launch,
+                     "avg_launch_ms": dom_ms / dom_launches},
+        "pipeline": {"b_min_bytes_per_frame": bm["b_min"], "achieved_gbs": pipe_gbs,
+                     "frac": pipe_gbs / peak, "per_kernel": per_kernel},
+        "clocks": clk,
+        "e2e": {"value": e2e_fps, "unit": "frames/s",
+                "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
+                "d2h_bytes_per_step": 8 * n},
+        "gpu_launches": gpu_launches,
+        "cpu_baseline": cpu,
+        "scores_head": [float(x) for x in scores[:3]],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    sc.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.SPECS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    import __graft_entry__
+    __graft_entry__.build()
+    return run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,646 @@
+// api.cu — the C ABI of libss2 (include/ss2.h): argument checks, the
+// context and its device workspace, the constant tables the kernels read,
+// and the order of launches for a batch of frames.
+//
+// Control crosses to the device once per batch of frames (the launches) and
+// back once per call (the 8-byte-per-frame score read-back and one stream
+// synchronisation), as "Research-1363: Device-resident ssimulacra2 and a
+// single-wait MS-SSIM on SYCL" asks in its Question and Finding 6.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cerrno>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <utility>
+#include <vector>
+
+#include "../../include/ss2.h"
+#include "ss2_impl.h"
+#include "ss2_kernels.h"
+
+#define SS2_API extern "C" __attribute__((visibility("default")))
+
+using namespace ss2;
+
+// ---------------------------------------------------------------------------
+// Errors
+// ---------------------------------------------------------------------------
+
+static thread_local int t_err = 0;
+static thread_local char t_msg[512] = "";
+
+static int fail(int code, const char *fmt, ...) {
+  t_err = code;
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+static int cuda_fail(cudaError_t e, const char *what) {
+  return fail(SS2_EIO, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define CU(call, what)                     \
+  do {                                     \
+    cudaError_t e_ = (call);               \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+SS2_API int ss2_last_error(void) { return t_err; }
+SS2_API const char *ss2_last_error_string(void) { return t_msg; }
+
+// ---------------------------------------------------------------------------
+// Host-built constant tables (the library's own; nothing is shared with any
+// other implementation).
+// ---------------------------------------------------------------------------
+
+// sRGB decoding (IEC 61966-2-1) in fp64.
+static double srgb_to_linear(double v) {
+  return v <= 0.04045 ? v / 12.92 : std::pow((v + 0.055) / 1.055, 2.4);
+}
+
+static void build_eotf(float *T) {
+  for (int i = 0; i <= kEotfN; ++i) T[i] = (float)srgb_to_linear((double)i / kEotfN);
+}
+
+// Recursive Gaussian (sigma = 1.5) as three odd cosine harmonics on |m| <= R:
+// h[m] = sum_k a_k cos(w_k m), w_k = (2k+1) pi / (2 (R+1)).  The a_k solve
+// the least-squares fit to the sampled Gaussian density under sum_m h[m] = 1
+// (Lagrange system, Gauss-Jordan with partial pivoting).  The resonator of
+// harmonic k runs Y[n+1] = 2 cos(w_k) Y[n] - Y[n-1] + a_k cos(w_k R)
+// (x[n+R+1] + x[n-R-1]).
+static void build_iir(float *c2, float *gk) {
+  const double kPi = 3.14159265358979323846, sigma = 1.5;
+  const int R = kIirR;
+  double w[3];
+  for (int k = 0; k < 3; ++k) w[k] = (2 * k + 1) * kPi / (2.0 * (R + 1));
+  double A[4][5] = {};
+  for (int m = -R; m <= R; ++m) {
+    const double gm = std::exp(-(double)m * m / (2.0 * sigma * sigma)) / (sigma * std::sqrt(2.0 * kPi));
+    double cs[3];
+    for (int k = 0; k < 3; ++k) cs[k] = std::cos(w[k] * m);
+    for (int r = 0; r < 3; ++r) {
+      for (int k = 0; k < 3; ++k) A[r][k] += cs[r] * cs[k];
+      A[r][3] += cs[r];
+      A[r][4] += cs[r] * gm;
+    }
+  }
+  for (int k = 0; k < 3; ++k) A[3][k] = A[k][3];
+  A[3][4] = 1.0;
+  for (int col = 0; col < 4; ++col) {
+    int best = col;
+    for (int r = col + 1; r < 4; ++r)
+      if (std::fabs(A[r][col]) > std::fabs(A[best][col])) best = r;
+    for (int j = 0; j < 5; ++j) std::swap(A[col][j], A[best][j]);
+    for (int r = col + 1; r < 4; ++r) {
+      const double f = A[r][col] / A[col][col];
+      for (int j = col; j < 5; ++j) A[r][j] -= f * A[col][j];
+    }
+  }
+  double a[4];
+  for (int r = 3; r >= 0; --r) {
+    double acc = A[r][4];
+    for (int j = r + 1; j < 4; ++j) acc -= A[r][j] * a[j];
+    a[r] = acc / A[r][r];
+  }
+  for (int k = 0; k < 3; ++k) {
+    c2[k] = (float)(2.0 * std::cos(w[k]));
+    gk[k] = (float)(a[k] * std::cos(w[k] * R));
+  }
+}
+
+// BT.709 (Kr = 0.2126, Kb = 0.0722) limited-range decoding coefficients.
+static void build_yuv(float *k) {
+  const double kr = 0.2126, kb = 0.0722, kg = 1.0 - kr - kb;
+  k[0] = (float)(2.0 * (1.0 - kr));           // Cr -> R'
+  k[1] = (float)(2.0 * kb * (1.0 - kb) / kg); // Cb -> G' (subtracted)
+  k[2] = (float)(2.0 * kr * (1.0 - kr) / kg); // Cr -> G' (subtracted)
+  k[3] = (float)(2.0 * (1.0 - kb));           // Cb -> B'
+}
+
+static void default_params(double *p) {
+  std::memset(p, 0, sizeof(double) * kNParams);
+  for (int i = 0; i < kNValues; ++i) p[kPWeights + i] = 1.0 / 108.0;  // placeholder
+  p[kPPoly + 0] = 100.0;   // placeholder map: score = 100 - 100 P
+  p[kPPoly + 1] = -100.0;
+  p[kPPower + 0] = 1.0;
+  p[kPPower + 1] = 1.0;
+  // XYB opsin mixing (JPEG XL, ISO/IEC 18181-1)
+  const double m[9] = {0.30, 0.622, 0.078, 0.23, 0.692, 0.078,
+                       0.24342268924547819, 0.20476744424496821, 0.55180986650955360};
+  for (int i = 0; i < 9; ++i) p[kPOpsin + i] = m[i];
+  for (int i = 0; i < 3; ++i) p[kPBias + i] = 0.0037930732552754493;
+  p[kPAffine + 0] = 1.0;  // identity make-positive affine (placeholder)
+  p[kPAffine + 3] = 1.0;
+  p[kPC2] = 0.0009;
+}
+
+// ---------------------------------------------------------------------------
+// Context
+// ---------------------------------------------------------------------------
+
+struct ss2_ctx {
+  Geom g;
+  Pix px;
+  int batch;
+  int device;
+  double params[kNParams];
+  // device workspace
+  float *d_X = nullptr, *d_H = nullptr;
+  float2 *d_part = nullptr;
+  double *d_values = nullptr, *d_scores = nullptr, *d_params = nullptr;
+  float *d_eotf = nullptr;
+  size_t ws_bytes = 0;
+  // pinned read-back staging
+  double *h_scores = nullptr;
+  double *h_values = nullptr;
+  size_t h_cap = 0;  // frames
+  // per-kernel event timing (ss2_profile_begin / ss2_profile_end)
+  bool prof = false;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<std::pair<int, int>> ev_used;  // (kernel class, index of start event)
+  // host-input path (allocated on first use)
+  uint8_t *d_in[2] = {nullptr, nullptr};
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_copied[2] = {nullptr, nullptr}, ev_consumed[2] = {nullptr, nullptr};
+};
+
+static int chroma_shift(int chroma, int *sx, int *sy) {
+  switch (chroma) {
+    case SS2_CHROMA_420: *sx = 1; *sy = 1; return 0;
+    case SS2_CHROMA_422: *sx = 1; *sy = 0; return 0;
+    case SS2_CHROMA_444: *sx = 0; *sy = 0; return 0;
+    default: return -1;
+  }
+}
+
+static int check_geometry(int w, int h, int depth, int chroma) {
+  int sx = 0, sy = 0;
+  if (w < 8 || h < 8) return fail(SS2_EINVAL, "frame %dx%d is below the 8x8 minimum", w, h);
+  if (w > SS2_MAX_DIM || h > SS2_MAX_DIM)
+    return fail(SS2_EINVAL, "frame %dx%d is above the %d limit", w, h, SS2_MAX_DIM);
+  if (depth < 8 || depth > 16) return fail(SS2_EINVAL, "bit depth %d is outside 8..16", depth);
+  if (chroma_shift(chroma, &sx, &sy))
+    return fail(SS2_EINVAL, "chroma %d is not one of 420, 422, 444", chroma);
+  if (sx && (w & 1)) return fail(SS2_EINVAL, "odd width %d with subsampled chroma %d", w, chroma);
+  return 0;
+}
+
+static void make_geom(int w, int h, int depth, int chroma, Geom &g) {
+  std::memset(&g, 0, sizeof(g));
+  g.w = w; g.h = h; g.depth = depth; g.chroma = chroma;
+  chroma_shift(chroma, &g.sx, &g.sy);
+  g.cw = (w + g.sx) >> g.sx;
+  g.ch = (h + g.sy) >> g.sy;
+  g.bps = depth > 8 ? 2 : 1;
+  g.frame_bytes = ((long long)w * h + 2LL * g.cw * g.ch) * g.bps;
+  int sw = w, sh = h, n = 0;
+  while (n < kMaxScales && sw >= 8 && sh >= 8) {
+    g.ws[n] = sw; g.hs[n] = sh;
+    g.pitch[n] = (sw + 31) & ~31;
+    g.nw[n] = (sw + 31) / 32;
+    g.plane[n] = (long long)g.pitch[n] * sh;
+    ++n;
+    sw = (sw + 1) / 2; sh = (sh + 1) / 2;
+  }
+  g.nscales = n;
+  long long xo = 0, ho = 0;
+  int po = 0;
+  g.hline_off[0] = 0;
+  g.vwarp_off[0] = 0;
+  for (int s = 0; s < n; ++s) {
+    g.xoff[s] = xo; xo += 6 * g.plane[s];
+    g.hoff[s] = ho; ho += (long long)3 * kNq * g.plane[s];
+    g.poff[s] = po; po += 3 * kNSum * g.nw[s];
+    g.hline_off[s + 1] = g.hline_off[s] + 3 * g.hs[s];
+    g.vwarp_off[s + 1] = g.vwarp_off[s] + 3 * g.nw[s];
+  }
+  for (int s = n; s < kMaxScales; ++s) {
+    g.hline_off[s + 1] = g.hline_off[s];
+    g.vwarp_off[s + 1] = g.vwarp_off[s];
+  }
+  g.x_fs = xo; g.h_fs = ho; g.p_fs = po;
+}
+
+static size_t per_frame_bytes(const Geom &g) {
+  return (size_t)(g.x_fs + g.h_fs) * sizeof(float) + (size_t)g.p_fs * sizeof(float2) +
+         (kNValues + 1) * sizeof(double);
+}
+
+// Frames in flight per pass: enough column walkers at scale 0 to fill the
+// GPU (about 160k threads, 3 per column), within a 24 GB workspace.
+static int default_batch(const Geom &g) {
+  long long b = (160000LL + 3LL * g.w - 1) / (3LL * g.w);
+  b = std::max(4LL, std::min(64LL, b));
+  const long long cap = (24LL << 30) / (long long)per_frame_bytes(g);
+  b = std::max(1LL, std::min(b, cap));
+  return (int)b;
+}
+
+static void set_pix(ss2_ctx *c) {
+  Pix &p = c->px;
+  build_yuv(p.yuv);
+  for (int i = 0; i < 9; ++i) p.opsin[i] = (float)c->params[kPOpsin + i];
+  for (int i = 0; i < 3; ++i) p.bias[i] = (float)c->params[kPBias + i];
+  p.sx = (float)c->params[kPAffine + 0];
+  p.ox = (float)c->params[kPAffine + 1];
+  p.oy = (float)c->params[kPAffine + 2];
+  p.sb = (float)c->params[kPAffine + 3];
+  p.ob = (float)c->params[kPAffine + 4];
+  p.c2 = (float)c->params[kPC2];
+  build_iir(p.iir_c2, p.iir_g);
+}
+
+static void free_ctx(ss2_ctx *c) {
+  if (!c) return;
+  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+  cudaFree(c->d_X); cudaFree(c->d_H); cudaFree(c->d_part); cudaFree(c->d_values);
+  cudaFree(c->d_scores); cudaFree(c->d_params); cudaFree(c->d_eotf);
+  cudaFree(c->d_in[0]); cudaFree(c->d_in[1]);
+  if (c->h_scores) cudaFreeHost(c->h_scores);
+  if (c->h_values) cudaFreeHost(c->h_values);
+  for (int i = 0; i < 2; ++i) {
+    if (c->ev_copied[i]) cudaEventDestroy(c->ev_copied[i]);
+    if (c->ev_consumed[i]) cudaEventDestroy(c->ev_consumed[i]);
+  }
+  if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+  delete c;
+}
+
+static int check_device(int *dev) {
+  int n = 0;
+  cudaError_t e = cudaGetDeviceCount(&n);
+  if (e != cudaSuccess || n == 0) {
+    cudaGetLastError();
+    return fail(SS2_ENOTSUP, "no CUDA device (%s)", cudaGetErrorString(e));
+  }
+  CU(cudaGetDevice(dev), "cudaGetDevice");
+  cudaDeviceProp prop;
+  CU(cudaGetDeviceProperties(&prop, *dev), "cudaGetDeviceProperties");
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(SS2_ENOTSUP, "device %s is sm_%d%d; libss2 is built for sm_103a", prop.name,
+                prop.major, prop.minor);
+  return 0;
+}
+
+static int dev_alloc(void **p, size_t bytes, size_t *total) {
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return fail(SS2_ENOMEM, "cudaMalloc of %zu bytes failed (%s)", bytes, cudaGetErrorString(e));
+  }
+  *total += bytes;
+  return 0;
+}
+
+static int ensure_host_cap(ss2_ctx *c, size_t frames) {
+  if (frames <= c->h_cap) return 0;
+  if (c->h_scores) cudaFreeHost(c->h_scores);
+  if (c->h_values) cudaFreeHost(c->h_values);
+  c->h_scores = nullptr;
+  c->h_values = nullptr;
+  c->h_cap = 0;
+  size_t cap = std::max(frames, (size_t)c->batch);
+  if (cudaMallocHost((void **)&c->h_scores, cap * sizeof(double)) != cudaSuccess ||
+      cudaMallocHost((void **)&c->h_values, cap * kNValues * sizeof(double)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SS2_ENOMEM, "pinned allocation for %zu frames failed", cap);
+  }
+  c->h_cap = cap;
+  return 0;
+}
+
+static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
+  if (check_geometry(w, h, depth, chroma)) return nullptr;
+  if (batch != 0 && (batch < 1 || batch > 1024)) {
+    fail(SS2_EINVAL, "batch %d is outside 1..1024", batch);
+    return nullptr;
+  }
+  int dev = 0;
+  if (check_device(&dev)) return nullptr;
+  ss2_ctx *c = new (std::nothrow) ss2_ctx();
+  if (!c) {
+    fail(SS2_ENOMEM, "host allocation failed");
+    return nullptr;
+  }
+  c->device = dev;
+  make_geom(w, h, depth, chroma, c->g);
+  c->batch = batch ? batch : default_batch(c->g);
+  default_params(c->params);
+  set_pix(c);
+  const Geom &g = c->g;
+  const size_t B = (size_t)c->batch;
+  size_t tot = 0;
+  if (dev_alloc((void **)&c->d_X, B * g.x_fs * sizeof(float), &tot) ||
+      dev_alloc((void **)&c->d_H, B * g.h_fs * sizeof(float), &tot) ||
+      dev_alloc((void **)&c->d_part, B * g.p_fs * sizeof(float2), &tot) ||
+      dev_alloc((void **)&c->d_values, B * kNValues * sizeof(double), &tot) ||
+      dev_alloc((void **)&c->d_scores, B * sizeof(double), &tot) ||
+      dev_alloc((void **)&c->d_params, kNParams * sizeof(double), &tot) ||
+      dev_alloc((void **)&c->d_eotf, (kEotfN + 1) * sizeof(float), &tot)) {
+    free_ctx(c);
+    return nullptr;
+  }
+  c->ws_bytes = tot;
+  float T[kEotfN + 1];
+  build_eotf(T);
+  cudaError_t e = cudaMemcpy(c->d_eotf, T, sizeof(T), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(c->d_params, c->params, sizeof(c->params), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "uploading constant tables");
+    free_ctx(c);
+    return nullptr;
+  }
+  if (ensure_host_cap(c, (size_t)c->batch)) {
+    free_ctx(c);
+    return nullptr;
+  }
+  return c;
+}
+
+SS2_API ss2_ctx *ss2_create(int width, int height, int bitdepth, int chroma) {
+  return create(width, height, bitdepth, chroma, 0);
+}
+
+SS2_API ss2_ctx *ss2_create_batch(int width, int height, int bitdepth, int chroma,
+                                  int max_batch) {
+  if (max_batch == 0) {
+    fail(SS2_EINVAL, "batch 0 is outside 1..1024");
+    return nullptr;
+  }
+  return create(width, height, bitdepth, chroma, max_batch);
+}
+
+SS2_API void ss2_destroy(ss2_ctx *ctx) { free_ctx(ctx); }
+
+SS2_API size_t ss2_frame_bytes(const ss2_ctx *ctx) {
+  return ctx ? (size_t)ctx->g.frame_bytes : 0;
+}
+
+SS2_API int ss2_batch(const ss2_ctx *ctx) { return ctx ? ctx->batch : 0; }
+
+SS2_API size_t ss2_workspace_bytes(const ss2_ctx *ctx) { return ctx ? ctx->ws_bytes : 0; }
+
+SS2_API int ss2_default_params(double *params, int n_params) {
+  if (!params || n_params != kNParams)
+    return fail(SS2_EINVAL, "parameter vector must hold %d doubles", kNParams);
+  default_params(params);
+  return 0;
+}
+
+SS2_API int ss2_set_params(ss2_ctx *ctx, const double *params, int n_params) {
+  if (!ctx || !params || n_params != kNParams)
+    return fail(SS2_EINVAL, "ss2_set_params needs a context and %d doubles", kNParams);
+  for (int i = 0; i < kNParams; ++i)
+    if (!std::isfinite(params[i])) return fail(SS2_EINVAL, "parameter %d is not finite", i);
+  for (int i = 0; i < 3; ++i)
+    if (!((float)params[kPBias + i] > 0.0f))
+      return fail(SS2_EINVAL, "opsin bias %d must be positive", i);
+  std::memcpy(ctx->params, params, sizeof(ctx->params));
+  set_pix(ctx);
+  CU(cudaMemcpy(ctx->d_params, ctx->params, sizeof(ctx->params), cudaMemcpyHostToDevice),
+     "uploading parameters");
+  return 0;
+}
+
+SS2_API int ss2_host_tables(float *eotf, float *iir) {
+  if (eotf) build_eotf(eotf);
+  if (iir) build_iir(iir, iir + 3);
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Per-kernel timing: when enabled, every launch is bracketed by a pair of
+// events on the launching stream.
+// ---------------------------------------------------------------------------
+
+enum { kKPyramid = 0, kKHblur = 1, kKVblur = 2, kKFinalize = 3, kKClasses = 4 };
+
+static cudaError_t prof_mark(ss2_ctx *c, int cls, bool start, cudaStream_t st) {
+  if (!c->prof) return cudaSuccess;
+  size_t idx;
+  if (start) {
+    idx = c->ev_used.empty() ? 0 : (size_t)c->ev_used.back().second + 2;
+    while (c->ev_pool.size() < idx + 2) {
+      cudaEvent_t e;
+      cudaError_t r = cudaEventCreate(&e);
+      if (r != cudaSuccess) return r;
+      c->ev_pool.push_back(e);
+    }
+    c->ev_used.push_back({cls, (int)idx});
+  } else {
+    idx = (size_t)c->ev_used.back().second + 1;
+  }
+  return cudaEventRecord(c->ev_pool[idx], st);
+}
+
+#define TIMED(c, cls, st, launch, what)          \
+  do {                                            \
+    CU(prof_mark(c, cls, true, st), "event");     \
+    CU(launch, what);                             \
+    CU(prof_mark(c, cls, false, st), "event");    \
+  } while (0)
+
+SS2_API int ss2_profile_begin(ss2_ctx *ctx) {
+  if (!ctx) return fail(SS2_EINVAL, "NULL context");
+  ctx->prof = true;
+  ctx->ev_used.clear();
+  return 0;
+}
+
+SS2_API int ss2_profile_end(ss2_ctx *ctx, double *ms, int *launches) {
+  if (!ctx) return fail(SS2_EINVAL, "NULL context");
+  double t[kKClasses] = {0, 0, 0, 0};
+  int n[kKClasses] = {0, 0, 0, 0};
+  for (const auto &u : ctx->ev_used) {
+    CU(cudaEventSynchronize(ctx->ev_pool[u.second + 1]), "event sync");
+    float e = 0.0f;
+    CU(cudaEventElapsedTime(&e, ctx->ev_pool[u.second], ctx->ev_pool[u.second + 1]),
+       "event elapsed");
+    t[u.first] += e;
+    n[u.first] += 1;
+  }
+  ctx->prof = false;
+  ctx->ev_used.clear();
+  for (int i = 0; i < kKClasses; ++i) {
+    if (ms) ms[i] = t[i];
+    if (launches) launches[i] = n[i];
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// One pass of the pipeline over nb frames already on the device.
+// ---------------------------------------------------------------------------
+
+static int run_batch(ss2_ctx *c, const uint8_t *ref, const uint8_t *dis, int nb,
+                     cudaStream_t st) {
+  const Geom &g = c->g;
+  TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->d_eotf, ref, dis, c->d_X, nb, st),
+        "k_pyramid launch");
+  TIMED(c, kKHblur, st, launch_hblur(g, c->px, c->d_X, c->d_H, nb, st), "k_hblur launch");
+  TIMED(c, kKVblur, st, launch_vblur(g, c->px, c->d_X, c->d_H, c->d_part, nb, st),
+        "k_vblur launch");
+  TIMED(c, kKFinalize, st,
+        launch_finalize(g, c->d_part, c->d_params, c->d_values, c->d_scores, nb, st),
+        "k_finalize launch");
+  return 0;
+}
+
+static int check_call(ss2_ctx *ctx, const void *ref, const void *dis, int n) {
+  if (!ctx) return fail(SS2_EINVAL, "NULL context");
+  if (n < 0) return fail(SS2_EINVAL, "negative frame count %d", n);
+  if (n > 0 && (!ref || !dis)) return fail(SS2_EINVAL, "NULL frame pointer");
+  return 0;
+}
+
+static int score_device(ss2_ctx *ctx, const void *ref, const void *dis, int n, double *scores,
+                        double *values, void *stream) {
+  if (check_call(ctx, ref, dis, n)) return t_err;
+  if (n == 0) return 0;
+  if (!scores && !values) return fail(SS2_EINVAL, "no output array");
+  if (ensure_host_cap(ctx, (size_t)n)) return t_err;
+  CU(cudaSetDevice(ctx->device), "cudaSetDevice");
+  cudaStream_t st = (cudaStream_t)stream;
+  const uint8_t *r8 = (const uint8_t *)ref, *d8 = (const uint8_t *)dis;
+  const long long fb = ctx->g.frame_bytes;
+  for (int f0 = 0; f0 < n; f0 += ctx->batch) {
+    const int nb = std::min(ctx->batch, n - f0);
+    if (run_batch(ctx, r8 + f0 * fb, d8 + f0 * fb, nb, st)) return t_err;
+    CU(cudaMemcpyAsync(ctx->h_scores + f0, ctx->d_scores, nb * sizeof(double),
+                       cudaMemcpyDeviceToHost, st),
+       "score read-back");
+    if (values)
+      CU(cudaMemcpyAsync(ctx->h_values + (size_t)f0 * kNValues, ctx->d_values,
+                         (size_t)nb * kNValues * sizeof(double), cudaMemcpyDeviceToHost, st),
+         "value read-back");
+  }
+  CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  if (scores) std::memcpy(scores, ctx->h_scores, (size_t)n * sizeof(double));
+  if (values) std::memcpy(values, ctx->h_values, (size_t)n * kNValues * sizeof(double));
+  return 0;
+}
+
+SS2_API int ss2_score_frames(ss2_ctx *ctx, const void *ref, const void *dis, int n_frames,
+                             double *scores, void *stream) {
+  if (n_frames > 0 && !scores) return fail(SS2_EINVAL, "NULL scores array");
+  return score_device(ctx, ref, dis, n_frames, scores, nullptr, stream);
+}
+
+SS2_API int ss2_values(ss2_ctx *ctx, const void *ref, const void *dis, int n_frames,
+                       double *values, double *scores, void *stream) {
+  if (n_frames > 0 && !values) return fail(SS2_EINVAL, "NULL values array");
+  return score_device(ctx, ref, dis, n_frames, scores, values, stream);
+}
+
+static int ensure_upload_slots(ss2_ctx *c) {
+  if (c->d_in[0]) return 0;
+  const size_t bytes = 2 * (size_t)c->batch * (size_t)c->g.frame_bytes;  // ref + dis
+  size_t tot = 0;
+  for (int i = 0; i < 2; ++i)
+    if (dev_alloc((void **)&c->d_in[i], bytes, &tot)) return t_err;
+  c->ws_bytes += tot;
+  CU(cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking), "copy stream");
+  for (int i = 0; i < 2; ++i) {
+    CU(cudaEventCreateWithFlags(&c->ev_copied[i], cudaEventDisableTiming), "event");
+    CU(cudaEventCreateWithFlags(&c->ev_consumed[i], cudaEventDisableTiming), "event");
+  }
+  return 0;
+}
+
+SS2_API int ss2_score_frames_host(ss2_ctx *ctx, const void *ref_host, const void *dis_host,
+                                  int n_frames, double *scores, void *stream) {
+  if (check_call(ctx, ref_host, dis_host, n_frames)) return t_err;
+  if (n_frames == 0) return 0;
+  if (!scores) return fail(SS2_EINVAL, "NULL scores array");
+  if (ensure_host_cap(ctx, (size_t)n_frames)) return t_err;
+  CU(cudaSetDevice(ctx->device), "cudaSetDevice");
+  if (ensure_upload_slots(ctx)) return t_err;
+  cudaStream_t st = (cudaStream_t)stream;
+  const long long fb = ctx->g.frame_bytes;
+  const size_t half = (size_t)ctx->batch * (size_t)fb;
+  const uint8_t *r8 = (const uint8_t *)ref_host, *d8 = (const uint8_t *)dis_host;
+  int k = 0;
+  for (int f0 = 0; f0 < n_frames; f0 += ctx->batch, ++k) {
+    const int nb = std::min(ctx->batch, n_frames - f0);
+    const int slot = k & 1;
+    uint8_t *dref = ctx->d_in[slot], *ddis = ctx->d_in[slot] + half;
+    // slot fence: the upload waits for the kernel that last read this slot
+    CU(cudaStreamWaitEvent(ctx->copy_stream, ctx->ev_consumed[slot], 0), "slot fence");
+    CU(cudaMemcpyAsync(dref, r8 + f0 * fb, (size_t)nb * fb, cudaMemcpyHostToDevice,
+                       ctx->copy_stream),
+       "ref upload");
+    CU(cudaMemcpyAsync(ddis, d8 + f0 * fb, (size_t)nb * fb, cudaMemcpyHostToDevice,
+                       ctx->copy_stream),
+       "dis upload");
+    CU(cudaEventRecord(ctx->ev_copied[slot], ctx->copy_stream), "event record");
+    CU(cudaStreamWaitEvent(st, ctx->ev_copied[slot], 0), "upload wait");
+    const Geom &g = ctx->g;
+    TIMED(ctx, kKPyramid, st,
+          launch_pyramid(g, ctx->px, ctx->d_eotf, dref, ddis, ctx->d_X, nb, st),
+          "k_pyramid launch");
+    CU(cudaEventRecord(ctx->ev_consumed[slot], st), "event record");
+    TIMED(ctx, kKHblur, st, launch_hblur(g, ctx->px, ctx->d_X, ctx->d_H, nb, st),
+          "k_hblur launch");
+    TIMED(ctx, kKVblur, st, launch_vblur(g, ctx->px, ctx->d_X, ctx->d_H, ctx->d_part, nb, st),
+          "k_vblur launch");
+    TIMED(ctx, kKFinalize, st,
+          launch_finalize(g, ctx->d_part, ctx->d_params, ctx->d_values, ctx->d_scores, nb, st),
+          "k_finalize launch");
+    CU(cudaMemcpyAsync(ctx->h_scores + f0, ctx->d_scores, nb * sizeof(double),
+                       cudaMemcpyDeviceToHost, st),
+       "score read-back");
+  }
+  CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  std::memcpy(scores, ctx->h_scores, (size_t)n_frames * sizeof(double));
+  return 0;
+}
+
+SS2_API int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis, int scale,
+                             float *xyb, float *hblur, void *stream) {
+  if (check_call(ctx, ref, dis, 1)) return t_err;
+  if (scale < 0 || scale >= ctx->g.nscales)
+    return fail(SS2_EINVAL, "scale %d is not computed for this geometry", scale);
+  CU(cudaSetDevice(ctx->device), "cudaSetDevice");
+  cudaStream_t st = (cudaStream_t)stream;
+  const Geom &g = ctx->g;
+  CU(launch_pyramid(g, ctx->px, ctx->d_eotf, (const uint8_t *)ref, (const uint8_t *)dis,
+                    ctx->d_X, 1, st),
+     "k_pyramid launch");
+  CU(launch_hblur(g, ctx->px, ctx->d_X, ctx->d_H, 1, st), "k_hblur launch");
+  const size_t ws = g.ws[scale], hs = g.hs[scale];
+  const size_t pitch_b = (size_t)g.pitch[scale] * sizeof(float);
+  if (xyb)
+    for (int p = 0; p < 6; ++p)
+      CU(cudaMemcpy2DAsync(xyb + p * ws * hs, ws * sizeof(float),
+                           ctx->d_X + g.xoff[scale] + p * g.plane[scale], pitch_b,
+                           ws * sizeof(float), hs, cudaMemcpyDeviceToHost, st),
+         "plane read-back");
+  if (hblur)
+    for (int p = 0; p < 3 * kNq; ++p)
+      CU(cudaMemcpy2DAsync(hblur + p * ws * hs, ws * sizeof(float),
+                           ctx->d_H + g.hoff[scale] + p * g.plane[scale], pitch_b,
+                           ws * sizeof(float), hs, cudaMemcpyDeviceToHost, st),
+         "plane read-back");
+  CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  return 0;
+}
+
+SS2_API int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return fail(SS2_EINVAL, "bad cbrt arguments");
+  int dev = 0;
+  if (check_device(&dev)) return t_err;
+  cudaStream_t st = (cudaStream_t)stream;
+  CU(launch_cbrt(x, y, n, st), "k_cbrt launch");
+  CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  return 0;
+}

@@ -1,0 +1,432 @@
+// kernels.cu — the ssimulacra2 hot path on sm_103a.
+//
+//   k_pyramid   YUV -> linear RGB -> XYB at scale 0, then the 2x2 downsample
+//               of linear RGB and XYB at scales 1..5, one 32x32 scale-0 tile
+//               per block (the tile's pyramid stays in shared memory, so the
+//               YUV planes are read once and only XYB reaches HBM).
+//   k_hblur     horizontal recursive Gaussian of the five quantities
+//               (x1, x2, x1^2, x2^2, x1 x2) of one row and channel; the
+//               products are formed in registers (multiply_3plane fused).
+//   k_vblur     vertical recursive Gaussian of the same five quantities down
+//               one column, fused with ssim_map and edge_diff_map and the six
+//               double-float sums; one partial per warp and (channel, sum).
+//   k_finalize  partials -> 108 values -> pool_score, one block per frame.
+//
+// Source: "Research-1363: Device-resident ssimulacra2 and a single-wait
+// MS-SSIM on SYCL" (vmafx documentation), "Sources" (the steps) and
+// Findings 2, 4, 7 (numerics, float pairs and the fixed reduction tree, the
+// sequential IIR along each line).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "ss2_device.cuh"
+#include "ss2_impl.h"
+#include "ss2_kernels.h"
+
+namespace ss2 {
+
+// ---------------------------------------------------------------------------
+// k_pyramid
+// ---------------------------------------------------------------------------
+
+constexpr int kTile = 32;  // scale-0 tile edge; 32 = 2^5 keeps 5 halvings inside the tile
+constexpr int kPyrThreads = 256;
+// shared-memory offset of the level-s tile inside each plane's region:
+// sum_{k<s} (32 >> k)^2 = (4096 - (4096 >> 2s)) / 3
+__host__ __device__ constexpr int lvl_off(int s) { return (4096 - (4096 >> (2 * s))) / 3; }
+constexpr int kLvlTotal = lvl_off(kMaxScales);
+
+__device__ __forceinline__ int read_sample(const uint8_t *__restrict__ p, long long i,
+                                           int bps) {
+  if (bps == 1) return p[i];
+  const uint16_t *q = reinterpret_cast<const uint16_t *>(p);
+  return q[i];
+}
+
+__global__ void __launch_bounds__(kPyrThreads)
+    k_pyramid(Geom g, Pix px, const float *__restrict__ eotf, const uint8_t *__restrict__ ref,
+              const uint8_t *__restrict__ dis, float *__restrict__ X) {
+  __shared__ float L[6][kLvlTotal];
+  const int frame = blockIdx.z;
+  const int tx0 = blockIdx.x * kTile, ty0 = blockIdx.y * kTile;
+  float *Xf = X + (long long)frame * g.x_fs;
+
+  float cb[3];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) cb[i] = cbrt_cr(px.bias[i]);
+
+  // ---- scale 0: unpack, matrix, EOTF, XYB ----
+  {
+    const uint8_t *frames[2] = {ref + (long long)frame * g.frame_bytes,
+                                dis + (long long)frame * g.frame_bytes};
+    const int k = 1 << (g.depth - 8);
+    const float dy = (float)(219 * k), dc = (float)(224 * k);
+    const long long ysz = (long long)g.w * g.h, csz = (long long)g.cw * g.ch;
+    for (int p = threadIdx.x; p < kTile * kTile; p += kPyrThreads) {
+      const int lx = p & (kTile - 1), ly = p / kTile;
+      const int x = tx0 + lx, y = ty0 + ly;
+      if (x >= g.w || y >= g.h) {
+#pragma unroll
+        for (int c = 0; c < 6; ++c) L[c][p] = 0.0f;
+        continue;
+      }
+      const long long ci = (long long)(y >> g.sy) * g.cw + (x >> g.sx);
+#pragma unroll
+      for (int img = 0; img < 2; ++img) {
+        const uint8_t *f = frames[img];
+        const int Ys = read_sample(f, (long long)y * g.w + x, g.bps);
+        const int Us = read_sample(f + ysz * g.bps, ci, g.bps);
+        const int Vs = read_sample(f + (ysz + csz) * g.bps, ci, g.bps);
+        const float yn = __fdiv_rn((float)(Ys - 16 * k), dy);
+        const float cbv = __fdiv_rn((float)(Us - 128 * k), dc);
+        const float crv = __fdiv_rn((float)(Vs - 128 * k), dc);
+        const float r = __fmaf_rn(px.yuv[0], crv, yn);
+        const float gg = __fmaf_rn(-px.yuv[2], crv, __fmaf_rn(-px.yuv[1], cbv, yn));
+        const float b = __fmaf_rn(px.yuv[3], cbv, yn);
+        const float R = eotf_lookup(eotf, clamp01(r));
+        const float G = eotf_lookup(eotf, clamp01(gg));
+        const float B = eotf_lookup(eotf, clamp01(b));
+        L[3 * img + 0][p] = R;
+        L[3 * img + 1][p] = G;
+        L[3 * img + 2][p] = B;
+        float xo, yo, bo;
+        pixel_xyb(px, cb, R, G, B, xo, yo, bo);
+        float *P = Xf + g.xoff[0] + (long long)y * g.pitch[0] + x;
+        P[(3 * img + 0) * g.plane[0]] = xo;
+        P[(3 * img + 1) * g.plane[0]] = yo;
+        P[(3 * img + 2) * g.plane[0]] = bo;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- scales 1..: downsample linear RGB inside the tile, then XYB ----
+  for (int s = 1; s < g.nscales; ++s) {
+    const int tw = kTile >> s;
+    const int ox = tx0 >> s, oy = ty0 >> s;            // tile origin at scale s
+    const int pox = tx0 >> (s - 1), poy = ty0 >> (s - 1);  // at scale s-1
+    const int pw = kTile >> (s - 1);
+    const int ww = g.ws[s - 1], hh = g.hs[s - 1];
+    for (int p = threadIdx.x; p < tw * tw; p += kPyrThreads) {
+      const int lx = p % tw, ly = p / tw;
+      const int x = ox + lx, y = oy + ly;
+      if (x >= g.ws[s] || y >= g.hs[s]) continue;
+      const int x0 = 2 * x, x1 = min(2 * x + 1, ww - 1);
+      const int y0 = 2 * y, y1 = min(2 * y + 1, hh - 1);
+      const int i00 = (y0 - poy) * pw + (x0 - pox), i01 = (y0 - poy) * pw + (x1 - pox);
+      const int i10 = (y1 - poy) * pw + (x0 - pox), i11 = (y1 - poy) * pw + (x1 - pox);
+      float v[6];
+#pragma unroll
+      for (int c = 0; c < 6; ++c) {
+        const float *Lp = &L[c][lvl_off(s - 1)];
+        float t = __fadd_rn(Lp[i00], Lp[i01]);
+        t = __fadd_rn(t, Lp[i10]);
+        t = __fadd_rn(t, Lp[i11]);
+        v[c] = __fmul_rn(t, 0.25f);
+        L[c][lvl_off(s) + p] = v[c];
+      }
+#pragma unroll
+      for (int img = 0; img < 2; ++img) {
+        float xo, yo, bo;
+        pixel_xyb(px, cb, v[3 * img], v[3 * img + 1], v[3 * img + 2], xo, yo, bo);
+        float *P = Xf + g.xoff[s] + (long long)y * g.pitch[s] + x;
+        P[(3 * img + 0) * g.plane[s]] = xo;
+        P[(3 * img + 1) * g.plane[s]] = yo;
+        P[(3 * img + 2) * g.plane[s]] = bo;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Recursive Gaussian step (shared by both passes): three resonators of one
+// quantity.  prev = Y[i-1], cur = Y[i]; in = x[i+N] + x[i-N].
+// ---------------------------------------------------------------------------
+
+struct Res3 {
+  float prev[3], cur[3];
+};
+
+__device__ __forceinline__ float res_step(Res3 &r, const Pix &px, float in) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    float u = __fmaf_rn(px.iir_g[k], in, -r.prev[k]);
+    float n = __fmaf_rn(px.iir_c2[k], r.cur[k], u);
+    r.prev[k] = r.cur[k];
+    r.cur[k] = n;
+  }
+  return __fadd_rn(__fadd_rn(r.cur[0], r.cur[1]), r.cur[2]);
+}
+
+__device__ __forceinline__ void res_zero(Res3 &r) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) r.prev[k] = r.cur[k] = 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+// k_hblur: one thread per (scale, row, channel) of a frame.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(128)
+    k_hblur(Geom g, Pix px, const float *__restrict__ X, float *__restrict__ H) {
+  const int frame = blockIdx.y;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= g.hline_off[g.nscales]) return;
+  int s = 0;
+  while (t >= g.hline_off[s + 1]) ++s;
+  const int local = t - g.hline_off[s];
+  const int c = local % 3, row = local / 3;
+  const int w = g.ws[s];
+  const float *x1 = X + (long long)frame * g.x_fs + g.xoff[s] + c * g.plane[s] +
+                    (long long)row * g.pitch[s];
+  const float *x2 = x1 + 3 * g.plane[s];
+  float *out = H + (long long)frame * g.h_fs + g.hoff[s] + (long long)(c * kNq) * g.plane[s] +
+               (long long)row * g.pitch[s];
+  const long long ps = g.plane[s];
+
+  Res3 r[kNq];
+#pragma unroll
+  for (int q = 0; q < kNq; ++q) res_zero(r[q]);
+
+  for (int i = -kReach; i <= w - 2; ++i) {
+    const int ia = i + kReach, ib = i - kReach;
+    const float a1 = ia < w ? __ldg(x1 + ia) : 0.0f;
+    const float a2 = ia < w ? __ldg(x2 + ia) : 0.0f;
+    const float b1 = ib >= 0 ? __ldg(x1 + ib) : 0.0f;
+    const float b2 = ib >= 0 ? __ldg(x2 + ib) : 0.0f;
+    float in[kNq];
+    in[0] = __fadd_rn(a1, b1);
+    in[1] = __fadd_rn(a2, b2);
+    in[2] = __fadd_rn(__fmul_rn(a1, a1), __fmul_rn(b1, b1));
+    in[3] = __fadd_rn(__fmul_rn(a2, a2), __fmul_rn(b2, b2));
+    in[4] = __fadd_rn(__fmul_rn(a1, a2), __fmul_rn(b1, b2));
+    float o[kNq];
+#pragma unroll
+    for (int q = 0; q < kNq; ++q) o[q] = res_step(r[q], px, in[q]);
+    if (i + 1 >= 0) {
+#pragma unroll
+      for (int q = 0; q < kNq; ++q) out[q * ps + i + 1] = o[q];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_vblur: one warp per 32 columns of one (scale, channel) of a frame; each
+// lane walks its column, forms the map terms at every output row and keeps
+// six float-pair sums, then a fixed shuffle tree gives one pair per warp.
+// ---------------------------------------------------------------------------
+
+struct Acc6 {
+  ff v[kNSum];
+};
+
+__device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float mu2, float s11,
+                                                float s22, float s12, float x1, float x2,
+                                                Acc6 &acc) {
+  // ssim_map (fp32 part as the CPU computes it)
+  const float dm = __fsub_rn(mu1, mu2);
+  const float num_m = __fsub_rn(1.0f, __fmul_rn(dm, dm));
+  const float cov = __fsub_rn(s12, __fmul_rn(mu1, mu2));
+  const float num_s = __fadd_rn(__fmul_rn(2.0f, cov), px.c2);
+  const float v1 = __fsub_rn(s11, __fmul_rn(mu1, mu1));
+  const float v2 = __fsub_rn(s22, __fmul_rn(mu2, mu2));
+  const float den_s = __fadd_rn(__fadd_rn(v1, v2), px.c2);
+  // float-pair part: q = num_m num_s / den_s, d = max(1 - q, 0)
+  const ff q = ff_div_f(two_prod(num_m, num_s), den_s);
+  ff d = ff_add(ff{1.0f, 0.0f}, ff{-q.hi, -q.lo});
+  if (!(d.hi > 0.0f)) d = {0.0f, 0.0f};
+  const ff d2 = ff_mul(d, d);
+  const ff d4 = ff_mul(d2, d2);
+  acc.v[0] = ff_add(acc.v[0], d);
+  acc.v[1] = ff_add(acc.v[1], d4);
+  // edge_diff_map: r = (1 + |x2 - mu2|) / (1 + |x1 - mu1|) - 1
+  const float a2 = fabsf(__fsub_rn(x2, mu2));
+  const float a1 = fabsf(__fsub_rn(x1, mu1));
+  const ff ratio = ff_div(two_sum(1.0f, a2), two_sum(1.0f, a1));
+  const ff rr = ff_add(ratio, ff{-1.0f, 0.0f});
+  const ff r2 = ff_mul(rr, rr);
+  const ff r4 = ff_mul(r2, r2);
+  const bool pos = rr.hi > 0.0f, neg = rr.hi < 0.0f;
+  const ff zero = {0.0f, 0.0f};
+  const ff art = pos ? rr : zero;
+  const ff art4 = pos ? r4 : zero;
+  const ff det = neg ? ff{-rr.hi, -rr.lo} : zero;
+  const ff det4 = neg ? r4 : zero;
+  acc.v[2] = ff_add(acc.v[2], art);
+  acc.v[3] = ff_add(acc.v[3], art4);
+  acc.v[4] = ff_add(acc.v[4], det);
+  acc.v[5] = ff_add(acc.v[5], det4);
+}
+
+__global__ void __launch_bounds__(128)
+    k_vblur(Geom g, Pix px, const float *__restrict__ X, const float *__restrict__ H,
+            float2 *__restrict__ part) {
+  const int frame = blockIdx.y;
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= g.vwarp_off[g.nscales]) return;  // whole warp exits together
+  int s = 0;
+  while (wid >= g.vwarp_off[s + 1]) ++s;
+  const int local = wid - g.vwarp_off[s];
+  const int c = local % 3, cb = local / 3;
+  const int col = cb * 32 + lane;
+  const bool active = col < g.ws[s];
+  const int h = g.hs[s];
+  const long long ps = g.plane[s], pitch = g.pitch[s];
+  const float *hp = H + (long long)frame * g.h_fs + g.hoff[s] + (long long)(c * kNq) * ps + col;
+  const float *x1p = X + (long long)frame * g.x_fs + g.xoff[s] + c * ps + col;
+  const float *x2p = x1p + 3 * ps;
+
+  Acc6 acc;
+#pragma unroll
+  for (int k = 0; k < kNSum; ++k) acc.v[k] = {0.0f, 0.0f};
+  Res3 r[kNq];
+#pragma unroll
+  for (int q = 0; q < kNq; ++q) res_zero(r[q]);
+
+  if (active) {
+    for (int i = -kReach; i <= h - 2; ++i) {
+      const int ia = i + kReach, ib = i - kReach;
+      float o[kNq];
+#pragma unroll
+      for (int q = 0; q < kNq; ++q) {
+        const float a = ia < h ? __ldg(hp + q * ps + ia * pitch) : 0.0f;
+        const float b = ib >= 0 ? __ldg(hp + q * ps + ib * pitch) : 0.0f;
+        o[q] = res_step(r[q], px, __fadd_rn(a, b));
+      }
+      const int row = i + 1;
+      if (row >= 0) {
+        const float x1 = __ldg(x1p + row * pitch);
+        const float x2 = __ldg(x2p + row * pitch);
+        ssim_edge_terms(px, o[0], o[1], o[2], o[3], o[4], x1, x2, acc);
+      }
+    }
+  }
+  // fixed butterfly-free tree: lane l adds lane l + 2^k for k = 4..0
+#pragma unroll
+  for (int k = 0; k < kNSum; ++k) {
+    ff v = acc.v[k];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      ff o;
+      o.hi = __shfl_down_sync(0xffffffffu, v.hi, off);
+      o.lo = __shfl_down_sync(0xffffffffu, v.lo, off);
+      v = ff_add(v, o);
+    }
+    if (lane == 0) {
+      part[(long long)frame * g.p_fs + g.poff[s] + (c * kNSum + k) * g.nw[s] + cb] =
+          make_float2(v.hi, v.lo);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_finalize: one block per frame.  Thread j < 108 owns value j: it adds the
+// warp partials of its (scale, channel, sum) in index order, then forms the
+// 1-norm (mean) or 4-norm (fourth root of the mean fourth power) in fp64.
+// Thread 0 pools: P = sum_i w_i |v_i| in index order, then the map.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(128)
+    k_finalize(Geom g, const float2 *__restrict__ part, const double *__restrict__ params,
+               double *__restrict__ values, double *__restrict__ scores) {
+  __shared__ double v[kNValues];
+  const int frame = blockIdx.x;
+  const int j = threadIdx.x;
+  if (j < kNValues) {
+    const int kind = j % 3, n = (j / 3) % 2, s = (j / 6) % 6, c = j / 36;
+    double out = 0.0;
+    if (s < g.nscales) {
+      const int k = 2 * kind + n;
+      const float2 *p = part + (long long)frame * g.p_fs + g.poff[s] + (c * kNSum + k) * g.nw[s];
+      ff acc = {0.0f, 0.0f};
+      for (int i = 0; i < g.nw[s]; ++i) {
+        const float2 t = p[i];
+        acc = ff_add(acc, ff{t.x, t.y});
+      }
+      const double S = (double)acc.hi + (double)acc.lo;
+      const double N = (double)g.ws[s] * (double)g.hs[s];
+      out = n == 0 ? S / N : sqrt(sqrt(S / N));
+    }
+    v[j] = out;
+    values[(long long)frame * kNValues + j] = out;
+  }
+  __syncthreads();
+  if (j == 0) {
+    double P = 0.0;
+    for (int i = 0; i < kNValues; ++i) {
+      const double t = params[kPWeights + i] * fabs(v[i]);
+      P = P + t;
+    }
+    const double *pc = params + kPPoly;
+    double sc = pc[3] * P;
+    sc = sc + pc[2];
+    sc = sc * P;
+    sc = sc + pc[1];
+    sc = sc * P;
+    sc = sc + pc[0];
+    const double *pw = params + kPPower;
+    if (sc > 0.0) {
+      double t = pw[1] == 1.0 ? sc : pow(sc, pw[1]);
+      t = pw[0] * t;
+      sc = t + pw[2];
+    }
+    scores[frame] = sc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_cbrt: the pipeline's cube root on an array (checks against the oracle).
+// ---------------------------------------------------------------------------
+
+__global__ void k_cbrt(const float *__restrict__ x, float *__restrict__ y, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    y[i] = v >= 0.0f && v < __int_as_float(0x7f800000) ? cbrt_cr(v) : v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const long long blocks = std::min<long long>((n + 255) / 256, 152LL * 16);
+  k_cbrt<<<(unsigned)blocks, 256, 0, st>>>(x, y, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pyramid(const Geom &g, const Pix &px, const float *eotf, const uint8_t *ref,
+                           const uint8_t *dis, float *X, int nframes, cudaStream_t st) {
+  dim3 grid((g.w + kTile - 1) / kTile, (g.h + kTile - 1) / kTile, nframes);
+  k_pyramid<<<grid, kPyrThreads, 0, st>>>(g, px, eotf, ref, dis, X);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hblur(const Geom &g, const Pix &px, const float *X, float *H, int nframes,
+                         cudaStream_t st) {
+  const int lines = g.hline_off[g.nscales];
+  dim3 grid((lines + 127) / 128, nframes);
+  k_hblur<<<grid, 128, 0, st>>>(g, px, X, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vblur(const Geom &g, const Pix &px, const float *X, const float *H,
+                         float2 *part, int nframes, cudaStream_t st) {
+  const int warps = g.vwarp_off[g.nscales];
+  dim3 grid((warps + 3) / 4, nframes);
+  k_vblur<<<grid, 128, 0, st>>>(g, px, X, H, part);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const Geom &g, const float2 *part, const double *params,
+                            double *values, double *scores, int nframes, cudaStream_t st) {
+  k_finalize<<<nframes, 128, 0, st>>>(g, part, params, values, scores);
+  return cudaGetLastError();
+}
+
+}  // namespace ss2

@@ -1,0 +1,186 @@
+// ss2_device.cuh — device arithmetic for the ssimulacra2 kernels.
+//
+// Every fp32 operation of the pixel pipeline is written with an explicit
+// round-to-nearest intrinsic (__fadd_rn, __fmul_rn, __fmaf_rn, __fdiv_rn) so
+// that nothing is contracted or reassociated: "Research-1363: Device-resident
+// ssimulacra2 and a single-wait MS-SSIM on SYCL", Finding 2 (contraction off,
+// products in named temporaries, fma only in the YUV matrix) makes the
+// pipeline up to the sums reproducible bit for bit.  The library is also
+// compiled with -fmad=false.
+//
+// Double-float ("float pair") arithmetic follows Finding 4: the product of
+// two floats is exact as a pair (two_prod, via fma), the quotient is two
+// partial quotients, and sums of pairs renormalise after every addition.
+// These are the classic error-free transformations of Dekker (1971) and
+// Knuth (TAOCP vol. 2, 4.2.2): two_sum, quick_two_sum, two_prod.
+#pragma once
+
+#include <cstdint>
+
+#include "ss2_impl.h"
+
+namespace ss2 {
+
+struct ff {
+  float hi, lo;
+};
+
+// a + b = s + e exactly (Knuth two_sum).
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  float s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+// a + b = s + e exactly when |a| >= |b| (Dekker quick_two_sum).
+__device__ __forceinline__ ff quick_two_sum(float a, float b) {
+  float s = __fadd_rn(a, b);
+  float e = __fsub_rn(b, __fsub_rn(s, a));
+  return {s, e};
+}
+
+// a * b = p + e exactly (fma-based two_prod).
+__device__ __forceinline__ ff two_prod(float a, float b) {
+  float p = __fmul_rn(a, b);
+  float e = __fmaf_rn(a, b, -p);
+  return {p, e};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  ff s = two_sum(a.hi, b.hi);
+  float e = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  return quick_two_sum(s.hi, e);
+}
+
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  ff p = two_prod(a.hi, b.hi);
+  float c = __fmaf_rn(a.hi, b.lo, __fmul_rn(a.lo, b.hi));
+  return quick_two_sum(p.hi, __fadd_rn(p.lo, c));
+}
+
+// a / b for a pair numerator and a float denominator: q1 = RN(a.hi / b);
+// the residual a.hi - q1 b is exact in one fma (q1 is correctly rounded),
+// the low word is folded in and the second quotient needs only ~24 bits.
+__device__ __forceinline__ ff ff_div_f(ff a, float b) {
+  float q1 = __fdiv_rn(a.hi, b);
+  float r = __fmaf_rn(-q1, b, a.hi);
+  r = __fadd_rn(r, a.lo);
+  float q2 = __fdividef(r, b);
+  return quick_two_sum(q1, q2);
+}
+
+// a / b for pairs (same scheme, the denominator's low word enters the
+// residual).
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+  float q1 = __fdiv_rn(a.hi, b.hi);
+  float r = __fmaf_rn(-q1, b.hi, a.hi);
+  r = __fadd_rn(r, a.lo);
+  r = __fmaf_rn(-q1, b.lo, r);
+  float q2 = __fdividef(r, b.hi);
+  return quick_two_sum(q1, q2);
+}
+
+// ---------------------------------------------------------------------------
+// Correctly rounded cube root (Finding 2 asks for the CPU's cube root exactly;
+// the plain reading is cbrt rounded to nearest).  First guess: CUDA's cbrtf.
+// Then an exact decision between the guess and its neighbours: the rounded
+// result y satisfies (y - u/2)^3 < x < (y + u/2)^3 for the float spacing u
+// around y, and each midpoint cube is compared with x in 128-bit integers.
+// ---------------------------------------------------------------------------
+
+// A positive finite float as X * 2^e, X an integer < 2^24.
+__device__ __forceinline__ void float_parts(float v, uint32_t &X, int &e) {
+  uint32_t b = __float_as_uint(v);
+  uint32_t be = (b >> 23) & 0xffu;
+  uint32_t m = b & 0x7fffffu;
+  X = be ? (m | 0x800000u) : m;
+  e = be ? (int)be - 150 : -149;
+}
+
+// Sign of (M 2^f)^3 - X 2^g, exact; M < 2^27, X < 2^24.
+__device__ __forceinline__ int cube_cmp(uint32_t M, int f, uint32_t X, int g) {
+  unsigned long long m2 = (unsigned long long)M * M;
+  unsigned __int128 c = (unsigned __int128)m2 * M;   // < 2^81
+  int d = 3 * f - g;
+  if (d >= 0) {
+    if (d >= 24) return 1;
+    unsigned __int128 lhs = c << d;
+    return lhs > X ? 1 : (lhs < X ? -1 : 0);
+  }
+  if (-d >= 104) return X ? -1 : 1;
+  unsigned __int128 rhs = (unsigned __int128)X << (-d);
+  return c > rhs ? 1 : (c < rhs ? -1 : 0);
+}
+
+// Correctly rounded cbrt for x >= 0 finite.
+__device__ __forceinline__ float cbrt_cr(float x) {
+  if (x == 0.0f) return 0.0f;
+  float y = cbrtf(x);
+  uint32_t X;
+  int g;
+  float_parts(x, X, g);
+#pragma unroll 1
+  for (int it = 0; it < 4; ++it) {
+    uint32_t Y;
+    int e;
+    float_parts(y, Y, e);
+    if (cube_cmp(2u * Y + 1u, e - 1, X, g) < 0) {          // above upper midpoint
+      y = __uint_as_float(__float_as_uint(y) + 1u);
+      continue;
+    }
+    const bool floor_binade = (Y == 0x800000u) && (e > -149);
+    const uint32_t Ml = floor_binade ? 4u * Y - 1u : 2u * Y - 1u;
+    const int fl = floor_binade ? e - 2 : e - 1;
+    if (cube_cmp(Ml, fl, X, g) > 0) {                       // below lower midpoint
+      y = __uint_as_float(__float_as_uint(y) - 1u);
+      continue;
+    }
+    break;
+  }
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// Pixel pipeline pieces (one rounding per written operation).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float clamp01(float v) {
+  if (v < 0.0f) return 0.0f;
+  if (v > 1.0f) return 1.0f;
+  return v;
+}
+
+// Linear interpolation in the sRGB EOTF table (uniform grid, 4096 intervals).
+__device__ __forceinline__ float eotf_lookup(const float *__restrict__ T, float v) {
+  float t = __fmul_rn(v, (float)kEotfN);
+  int i = (int)t;
+  i = i > kEotfN - 1 ? kEotfN - 1 : i;
+  float f = __fsub_rn(t, (float)i);
+  float t0 = __ldg(T + i), t1 = __ldg(T + i + 1);
+  return __fmaf_rn(f, __fsub_rn(t1, t0), t0);
+}
+
+// Linear RGB -> XYB with the make-positive affine.
+__device__ __forceinline__ void pixel_xyb(const Pix &p, const float cb[3], float r,
+                                          float g, float b, float &X, float &Y,
+                                          float &B) {
+  float c[3];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    float t0 = __fmul_rn(p.opsin[3 * i + 0], r);
+    float t1 = __fmul_rn(p.opsin[3 * i + 1], g);
+    float t2 = __fmul_rn(p.opsin[3 * i + 2], b);
+    float s = __fadd_rn(__fadd_rn(t0, t1), t2);
+    s = __fadd_rn(s, p.bias[i]);
+    s = s < 0.0f ? 0.0f : s;
+    c[i] = __fsub_rn(cbrt_cr(s), cb[i]);
+  }
+  float x = __fmul_rn(0.5f, __fsub_rn(c[0], c[1]));
+  float y = __fmul_rn(0.5f, __fadd_rn(c[0], c[1]));
+  X = __fadd_rn(__fmul_rn(x, p.sx), p.ox);
+  Y = __fadd_rn(y, p.oy);
+  B = __fadd_rn(__fmul_rn(__fsub_rn(c[2], y), p.sb), p.ob);
+}
+
+}  // namespace ss2

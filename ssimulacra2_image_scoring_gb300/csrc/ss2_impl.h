@@ -1,0 +1,56 @@
+// ss2_impl.h — internal types shared by the host side of libss2 and its
+// kernels: the geometry of a context's workspace and the per-pixel
+// constants passed to every launch by value.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace ss2 {
+
+constexpr int kMaxScales = 6;
+constexpr int kNValues = 108;
+constexpr int kNParams = 133;
+constexpr int kEotfN = 4096;   // table intervals; the table has kEotfN + 1 entries
+constexpr int kIirR = 4;       // recursive Gaussian support |m| <= R
+constexpr int kReach = kIirR + 1;  // taps at n +- (R + 1)
+constexpr int kNq = 5;         // blurred quantities per channel: mu1 mu2 s11 s22 s12
+constexpr int kNSum = 6;       // d, d^4, art, art^4, det, det^4
+
+// Parameter vector offsets (doubles), see include/ss2.h.
+constexpr int kPWeights = 0, kPPoly = 108, kPPower = 112, kPOpsin = 115, kPBias = 124,
+              kPAffine = 127, kPC2 = 132;
+
+// Workspace geometry of one context.  Planes at scale s are fp32, row-major,
+// pitch[s] floats per row (a multiple of 32), plane[s] = pitch[s] * hs[s].
+//   X block of a frame:  6 planes per scale (ref X Y B, dis X Y B) at xoff[s]
+//   H block of a frame: 15 planes per scale (channel-major, 5 quantities)
+//   partials of a frame: float2 pairs, (channel * 6 + sum) * nw[s] + warp,
+//                         at poff[s]
+struct Geom {
+  int w, h, depth, chroma, sx, sy, cw, ch, bps;
+  int nscales;
+  int ws[kMaxScales], hs[kMaxScales], pitch[kMaxScales], nw[kMaxScales];
+  long long plane[kMaxScales];
+  long long xoff[kMaxScales], hoff[kMaxScales];
+  long long x_fs, h_fs;            // floats per frame
+  int poff[kMaxScales];
+  int p_fs;                        // float2 per frame
+  long long frame_bytes;
+  // flat work decomposition over the scales
+  int hline_off[kMaxScales + 1];   // prefix of 3 * hs[s]     (horizontal lines)
+  int vwarp_off[kMaxScales + 1];   // prefix of 3 * nw[s]     (vertical warps)
+};
+
+// Per-pixel constants (fp32 pipeline), rounded from the parameter vector.
+struct Pix {
+  float yuv[4];        // cr->R', cb->G' (magnitude), cr->G' (magnitude), cb->B'
+  float opsin[9];
+  float bias[3];
+  float sx, ox, oy, sb, ob;
+  float c2;
+  float iir_c2[3];     // 2 cos(w_k)
+  float iir_g[3];      // a_k cos(w_k R)
+};
+
+}  // namespace ss2

@@ -1,0 +1,263 @@
+"""ctypes binding of libss2 (include/ss2.h).
+
+Argument marshalling only: every step of the scoring path runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the current
+stream.  If the shared library is missing the binding raises; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from . import _build
+
+NVALUES = 108
+NPARAMS = 133
+EOTF_N = 4096
+
+EINVAL, ENOMEM, ENOTSUP, EIO = -22, -12, -95, -5
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SS2Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libss2 error {code}: {msg}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libss2.so (built by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.SO_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is not built; call __graft_entry__.build() first")
+            L = ctypes.CDLL(path)
+            vp, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+            L.ss2_create.argtypes = [i, i, i, i]
+            L.ss2_create.restype = vp
+            L.ss2_create_batch.argtypes = [i, i, i, i, i]
+            L.ss2_create_batch.restype = vp
+            L.ss2_destroy.argtypes = [vp]
+            L.ss2_destroy.restype = None
+            L.ss2_score_frames.argtypes = [vp, vp, vp, i, vp, vp]
+            L.ss2_score_frames.restype = i
+            L.ss2_score_frames_host.argtypes = [vp, vp, vp, i, vp, vp]
+            L.ss2_score_frames_host.restype = i
+            L.ss2_values.argtypes = [vp, vp, vp, i, vp, vp, vp]
+            L.ss2_values.restype = i
+            L.ss2_debug_planes.argtypes = [vp, vp, vp, i, vp, vp, vp]
+            L.ss2_debug_planes.restype = i
+            L.ss2_debug_cbrt.argtypes = [vp, vp, ctypes.c_longlong, vp]
+            L.ss2_debug_cbrt.restype = i
+            L.ss2_profile_begin.argtypes = [vp]
+            L.ss2_profile_begin.restype = i
+            L.ss2_profile_end.argtypes = [vp, vp, vp]
+            L.ss2_profile_end.restype = i
+            L.ss2_frame_bytes.argtypes = [vp]
+            L.ss2_frame_bytes.restype = ctypes.c_size_t
+            L.ss2_batch.argtypes = [vp]
+            L.ss2_batch.restype = i
+            L.ss2_workspace_bytes.argtypes = [vp]
+            L.ss2_workspace_bytes.restype = ctypes.c_size_t
+            L.ss2_default_params.argtypes = [vp, i]
+            L.ss2_default_params.restype = i
+            L.ss2_set_params.argtypes = [vp, vp, i]
+            L.ss2_set_params.restype = i
+            L.ss2_host_tables.argtypes = [vp, vp]
+            L.ss2_host_tables.restype = i
+            L.ss2_last_error.argtypes = []
+            L.ss2_last_error.restype = i
+            L.ss2_last_error_string.argtypes = []
+            L.ss2_last_error_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def last_error() -> tuple[int, str]:
+    L = lib()
+    return int(L.ss2_last_error()), L.ss2_last_error_string().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        code, msg = last_error()
+        raise SS2Error(rc, msg)
+
+
+def default_params() -> np.ndarray:
+    p = np.zeros(NPARAMS, np.float64)
+    _check(lib().ss2_default_params(p.ctypes.data, NPARAMS))
+    return p
+
+
+def host_tables() -> tuple[np.ndarray, np.ndarray]:
+    """The library's host-built EOTF table (4097) and IIR coefficients (6)."""
+    eotf = np.zeros(EOTF_N + 1, np.float32)
+    iir = np.zeros(6, np.float32)
+    _check(lib().ss2_host_tables(eotf.ctypes.data, iir.ctypes.data))
+    return eotf, iir
+
+
+def debug_cbrt(x, out=None, stream=None):
+    """The pipeline's cube root applied to a float32 CUDA tensor."""
+    import torch
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32
+            and x.is_contiguous()):
+        raise TypeError("x must be a contiguous float32 CUDA tensor")
+    out = torch.empty_like(x) if out is None else out
+    _check(lib().ss2_debug_cbrt(x.data_ptr(), out.data_ptr(), x.numel(), _stream_handle(stream)))
+    return out
+
+
+def _stream_handle(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+class Scorer:
+    """A scoring context for one frame geometry (ss2_create)."""
+
+    def __init__(self, width: int, height: int, bitdepth: int, chroma: int,
+                 batch: int | None = None, params: np.ndarray | None = None):
+        L = lib()
+        if batch is None:
+            h = L.ss2_create(width, height, bitdepth, chroma)
+        else:
+            h = L.ss2_create_batch(width, height, bitdepth, chroma, batch)
+        if not h:
+            code, msg = last_error()
+            raise SS2Error(code, msg)
+        self._h = h
+        self.width, self.height, self.bitdepth, self.chroma = width, height, bitdepth, chroma
+        if params is not None:
+            self.set_params(params)
+
+    # -- properties --------------------------------------------------------
+    @property
+    def handle(self) -> int:
+        if not self._h:
+            raise SS2Error(EINVAL, "context is closed")
+        return self._h
+
+    @property
+    def frame_bytes(self) -> int:
+        return int(lib().ss2_frame_bytes(self.handle))
+
+    @property
+    def batch(self) -> int:
+        return int(lib().ss2_batch(self.handle))
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(lib().ss2_workspace_bytes(self.handle))
+
+    def set_params(self, params: np.ndarray) -> None:
+        p = np.ascontiguousarray(params, np.float64)
+        _check(lib().ss2_set_params(self.handle, p.ctypes.data, p.size))
+
+    # -- scoring -----------------------------------------------------------
+    def _frames(self, t) -> int:
+        import torch
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError("frames must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError("frames must be contiguous")
+        nbytes = t.numel() * t.element_size()
+        fb = self.frame_bytes
+        if nbytes % fb:
+            raise ValueError(f"{nbytes} bytes is not a whole number of {fb}-byte frames")
+        return nbytes // fb
+
+    def score(self, ref, dis, stream=None) -> np.ndarray:
+        """Scores device-resident frames; returns float64 scores on the host."""
+        n = self._frames(ref)
+        if self._frames(dis) != n:
+            raise ValueError("ref and dis hold different frame counts")
+        out = np.zeros(n, np.float64)
+        _check(lib().ss2_score_frames(self.handle, ref.data_ptr(), dis.data_ptr(), n,
+                                      out.ctypes.data, _stream_handle(stream)))
+        return out
+
+    def values(self, ref, dis, stream=None) -> tuple[np.ndarray, np.ndarray]:
+        """Scores and the 108 pooled values per frame."""
+        n = self._frames(ref)
+        if self._frames(dis) != n:
+            raise ValueError("ref and dis hold different frame counts")
+        vals = np.zeros((n, NVALUES), np.float64)
+        sc = np.zeros(n, np.float64)
+        _check(lib().ss2_values(self.handle, ref.data_ptr(), dis.data_ptr(), n,
+                                vals.ctypes.data, sc.ctypes.data, _stream_handle(stream)))
+        return vals, sc
+
+    def score_host(self, ref: np.ndarray, dis: np.ndarray, stream=None) -> np.ndarray:
+        """Scores frames held in host memory (pinned memory overlaps the upload)."""
+        import torch
+        def _ptr_bytes(a):
+            if isinstance(a, torch.Tensor):
+                if a.is_cuda or not a.is_contiguous():
+                    raise ValueError("host frames must be a contiguous CPU tensor or array")
+                return a.data_ptr(), a.numel() * a.element_size()
+            a = np.ascontiguousarray(a)
+            return a.ctypes.data, a.nbytes
+        pr, nr = _ptr_bytes(ref)
+        pd, nd = _ptr_bytes(dis)
+        fb = self.frame_bytes
+        if nr != nd or nr % fb:
+            raise ValueError("ref/dis must hold the same whole number of frames")
+        n = nr // fb
+        out = np.zeros(n, np.float64)
+        _check(lib().ss2_score_frames_host(self.handle, pr, pd, n, out.ctypes.data,
+                                           _stream_handle(stream)))
+        return out
+
+    def debug_planes(self, ref, dis, scale: int, stream=None):
+        """XYB planes (6, hs, ws) and horizontally blurred planes (15, hs, ws)
+        of one scale for the first frame pair."""
+        ws, hs = self.width, self.height
+        for _ in range(scale):
+            ws, hs = (ws + 1) // 2, (hs + 1) // 2
+        xyb = np.zeros((6, hs, ws), np.float32)
+        hb = np.zeros((15, hs, ws), np.float32)
+        _check(lib().ss2_debug_planes(self.handle, ref.data_ptr(), dis.data_ptr(), scale,
+                                      xyb.ctypes.data, hb.ctypes.data, _stream_handle(stream)))
+        return xyb, hb
+
+    KERNELS = ("k_pyramid", "k_hblur", "k_vblur", "k_finalize")
+
+    def profile_begin(self) -> None:
+        """Starts per-kernel CUDA-event timing of this context's launches."""
+        _check(lib().ss2_profile_begin(self.handle))
+
+    def profile_end(self) -> dict:
+        """Stops timing; returns {kernel: (total ms, launches)}."""
+        ms = np.zeros(4, np.float64)
+        n = np.zeros(4, np.int32)
+        _check(lib().ss2_profile_end(self.handle, ms.ctypes.data, n.ctypes.data))
+        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
+
+    def close(self) -> None:
+        if self._h:
+            lib().ss2_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
