@@ -186,6 +186,32 @@ int ss2_set_params(ss2_ctx *ctx, const double *params, int n_params);
  * pointer may be NULL.                                                     */
 int ss2_host_tables(float *eotf, float *iir);
 
+/*
+ * ss2_score_frames_noalloc — scores n_frames frame pairs without allocating
+ * anything, for callers that cannot call cudaMalloc at scoring time (code
+ * inside a custom allocator or memory-pool callback, processes with a device
+ * memory budget fixed up front, plug-ins handed buffers by a host that
+ * forbids allocation).  It has no counterpart on the source pages: it is the
+ * ss2_score_frames path with its workspace in one fixed 64 MiB device array
+ * that the library holds on every GPU that loads it, until exit.
+ *   width, height, bitdepth, chroma: as ss2_create; the frame's workspace
+ *             must fit the 64 MiB array (about 600k pixels, e.g. 853x481 or
+ *             960x540), else -EINVAL before any GPU work.
+ *   ref, dis: DEVICE pointers to n_frames packed frames each (caller-owned).
+ *   scores:   DEVICE array of n_frames doubles (caller-owned), written by the
+ *             last kernel; the call does not synchronise or read back.
+ *   stream:   cudaStream_t for all work (NULL = legacy default stream).
+ * Uses the default parameters.  The first call on a device does a one-time
+ * set-up (looks up the array's address, copies the constant tables with
+ * synchronous copies); make it before any stream capture.  All calls on a
+ * device share the array and keep the last call's contents; calls that
+ * overlap on the GPU race and corrupt each other's results.  Returns 0 or a
+ * negative code as the other entry points.
+ */
+int ss2_score_frames_noalloc(int width, int height, int bitdepth, int chroma,
+                             const void *ref, const void *dis, int n_frames,
+                             double *scores, void *stream);
+
 /* Last failure on the calling thread (0 if none yet).                      */
 int ss2_last_error(void);
 const char *ss2_last_error_string(void);

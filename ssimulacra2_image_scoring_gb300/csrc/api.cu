@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "../../include/ss2.h"
+#include "ss2_host.h"
 #include "ss2_impl.h"
 #include "ss2_kernels.h"
 
@@ -34,7 +35,7 @@ using namespace ss2;
 static thread_local int t_err = 0;
 static thread_local char t_msg[512] = "";
 
-static int fail(int code, const char *fmt, ...) {
+int ss2::fail(int code, const char *fmt, ...) {
   t_err = code;
   va_list ap;
   va_start(ap, fmt);
@@ -43,7 +44,7 @@ static int fail(int code, const char *fmt, ...) {
   return code;
 }
 
-static int cuda_fail(cudaError_t e, const char *what) {
+int ss2::cuda_fail(cudaError_t e, const char *what) {
   return fail(SS2_EIO, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
@@ -66,7 +67,7 @@ static double srgb_to_linear(double v) {
   return v <= 0.04045 ? v / 12.92 : std::pow((v + 0.055) / 1.055, 2.4);
 }
 
-static void build_eotf(float *T) {
+void ss2::build_eotf(float *T) {
   for (int i = 0; i <= kEotfN; ++i) T[i] = (float)srgb_to_linear((double)i / kEotfN);
 }
 
@@ -125,7 +126,7 @@ static void build_yuv(float *k) {
   k[3] = (float)(2.0 * (1.0 - kb));           // Cb -> B'
 }
 
-static void default_params(double *p) {
+void ss2::default_params(double *p) {
   std::memset(p, 0, sizeof(double) * kNParams);
   for (int i = 0; i < kNValues; ++i) p[kPWeights + i] = 1.0 / 108.0;  // placeholder
   p[kPPoly + 0] = 100.0;   // placeholder map: score = 100 - 100 P
@@ -181,7 +182,7 @@ static int chroma_shift(int chroma, int *sx, int *sy) {
   }
 }
 
-static int check_geometry(int w, int h, int depth, int chroma) {
+int ss2::check_geometry(int w, int h, int depth, int chroma) {
   int sx = 0, sy = 0;
   if (w < 8 || h < 8) return fail(SS2_EINVAL, "frame %dx%d is below the 8x8 minimum", w, h);
   if (w > SS2_MAX_DIM || h > SS2_MAX_DIM)
@@ -193,7 +194,7 @@ static int check_geometry(int w, int h, int depth, int chroma) {
   return 0;
 }
 
-static void make_geom(int w, int h, int depth, int chroma, Geom &g) {
+void ss2::make_geom(int w, int h, int depth, int chroma, Geom &g) {
   std::memset(&g, 0, sizeof(g));
   g.w = w; g.h = h; g.depth = depth; g.chroma = chroma;
   chroma_shift(chroma, &g.sx, &g.sy);
@@ -229,7 +230,7 @@ static void make_geom(int w, int h, int depth, int chroma, Geom &g) {
   g.x_fs = xo; g.h_fs = ho; g.p_fs = po;
 }
 
-static size_t per_frame_bytes(const Geom &g) {
+size_t ss2::per_frame_bytes(const Geom &g) {
   return (size_t)(g.x_fs + g.h_fs) * sizeof(float) + (size_t)g.p_fs * sizeof(float2) +
          (kNValues + 1) * sizeof(double);
 }
@@ -244,19 +245,20 @@ static int default_batch(const Geom &g) {
   return (int)b;
 }
 
-static void set_pix(ss2_ctx *c) {
-  Pix &p = c->px;
+void ss2::build_pix(const double *params, Pix &p) {
   build_yuv(p.yuv);
-  for (int i = 0; i < 9; ++i) p.opsin[i] = (float)c->params[kPOpsin + i];
-  for (int i = 0; i < 3; ++i) p.bias[i] = (float)c->params[kPBias + i];
-  p.sx = (float)c->params[kPAffine + 0];
-  p.ox = (float)c->params[kPAffine + 1];
-  p.oy = (float)c->params[kPAffine + 2];
-  p.sb = (float)c->params[kPAffine + 3];
-  p.ob = (float)c->params[kPAffine + 4];
-  p.c2 = (float)c->params[kPC2];
+  for (int i = 0; i < 9; ++i) p.opsin[i] = (float)params[kPOpsin + i];
+  for (int i = 0; i < 3; ++i) p.bias[i] = (float)params[kPBias + i];
+  p.sx = (float)params[kPAffine + 0];
+  p.ox = (float)params[kPAffine + 1];
+  p.oy = (float)params[kPAffine + 2];
+  p.sb = (float)params[kPAffine + 3];
+  p.ob = (float)params[kPAffine + 4];
+  p.c2 = (float)params[kPC2];
   build_iir(p.iir_c2, p.iir_g);
 }
+
+static void set_pix(ss2_ctx *c) { build_pix(c->params, c->px); }
 
 static void free_ctx(ss2_ctx *c) {
   if (!c) return;
@@ -274,7 +276,7 @@ static void free_ctx(ss2_ctx *c) {
   delete c;
 }
 
-static int check_device(int *dev) {
+int ss2::check_device(int *dev) {
   int n = 0;
   cudaError_t e = cudaGetDeviceCount(&n);
   if (e != cudaSuccess || n == 0) {

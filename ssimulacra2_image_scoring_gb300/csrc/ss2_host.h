@@ -1,0 +1,27 @@
+// ss2_host.h — host-side helpers of libss2 shared by its entry points:
+// error reporting, argument checks, workspace geometry and the constant
+// tables the kernels read.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+
+#include "ss2_impl.h"
+
+namespace ss2 {
+
+// Records code and message as the calling thread's last failure; returns code.
+int fail(int code, const char *fmt, ...);
+int cuda_fail(cudaError_t e, const char *what);
+
+int check_geometry(int w, int h, int depth, int chroma);  // 0 or -EINVAL
+int check_device(int *dev);                               // 0 or -ENOTSUP / -EIO
+void make_geom(int w, int h, int depth, int chroma, Geom &g);
+size_t per_frame_bytes(const Geom &g);                    // workspace bytes per frame
+
+void default_params(double *params);                      // kNParams doubles
+void build_pix(const double *params, Pix &p);
+void build_eotf(float *table);                            // kEotfN + 1 floats
+
+}  // namespace ss2

@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.ss2_profile_begin.restype = i
             L.ss2_profile_end.argtypes = [vp, vp, vp]
             L.ss2_profile_end.restype = i
+            L.ss2_score_frames_noalloc.argtypes = [i, i, i, i, vp, vp, i, vp, vp]
+            L.ss2_score_frames_noalloc.restype = i
             L.ss2_frame_bytes.argtypes = [vp]
             L.ss2_frame_bytes.restype = ctypes.c_size_t
             L.ss2_batch.argtypes = [vp]
@@ -115,6 +117,30 @@ def debug_cbrt(x, out=None, stream=None):
     out = torch.empty_like(x) if out is None else out
     _check(lib().ss2_debug_cbrt(x.data_ptr(), out.data_ptr(), x.numel(), _stream_handle(stream)))
     return out
+
+
+def score_noalloc(width: int, height: int, bitdepth: int, chroma: int, ref, dis,
+                  scores=None, stream=None):
+    """Scores device frames through ss2_score_frames_noalloc, which allocates
+    nothing (for callers that cannot call cudaMalloc while scoring).  Returns
+    the float64 CUDA tensor of scores; the caller synchronises."""
+    import torch
+    for t in (ref, dis):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+            raise TypeError("frames must be contiguous CUDA tensors")
+    fe = (width * height + 2 * ((width + (chroma != 444)) >> (chroma != 444)) *
+          ((height + (chroma == 420)) >> (chroma == 420)))
+    fb = fe * (1 if bitdepth <= 8 else 2)
+    nbytes = ref.numel() * ref.element_size()
+    if nbytes % fb or dis.numel() * dis.element_size() != nbytes:
+        raise ValueError("ref/dis must hold the same whole number of frames")
+    n = nbytes // fb
+    if scores is None:
+        scores = torch.empty(n, dtype=torch.float64, device=ref.device)
+    _check(lib().ss2_score_frames_noalloc(width, height, bitdepth, chroma, ref.data_ptr(),
+                                          dis.data_ptr(), n, scores.data_ptr(),
+                                          _stream_handle(stream)))
+    return scores
 
 
 def _stream_handle(stream) -> int | None:
