@@ -236,7 +236,7 @@ def run_reference(args, ws, rank):
 def run_ours(args, ws, rank, local):
     spec = synth.SPECS[args.workload]
     # generate before any CUDA work (the pool is spawned)
-    wl = synth.make(args.workload, workers=min(16, host_cores()))
+    wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
     import torch
     import torch.distributed as dist
 
@@ -249,8 +249,9 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     ref = torch.from_numpy(wl.ref).to(dev)
     dis = torch.from_numpy(wl.dis).to(dev)
-    n = spec.frames
-    sc = Scorer(spec.width, spec.height, spec.depth, spec.chroma)
+    n = wl.ref.shape[0]
+    sc = Scorer(spec.width, spec.height, spec.depth, spec.chroma,
+                batch=min(n, 1024) if args.frames else None)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -370,6 +371,8 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--frames", type=int, default=0,
+                    help="score only the first N frames of the workload (small profiling cases)")
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
     if args.impl == "reference":

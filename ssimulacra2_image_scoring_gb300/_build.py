@@ -68,8 +68,8 @@ def build(force: bool = False, extra_flags: list[str] | None = None) -> str:
         objs = list(ex.map(lambda s: _compile(s, extra), srcs))
     if force or _stale(SO_PATH, objs):
         tmp = SO_PATH + f".tmp{os.getpid()}"
-        subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs],
-                       check=True)
+        subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-Xlinker",
+                        "--no-undefined", "-o", tmp, *objs], check=True)
         os.replace(tmp, SO_PATH)
     return SO_PATH
 

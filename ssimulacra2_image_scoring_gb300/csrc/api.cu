@@ -7,6 +7,7 @@
 // synchronisation), as "Research-1363: Device-resident ssimulacra2 and a
 // single-wait MS-SSIM on SYCL" asks in its Question and Finding 6.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cerrno>
@@ -15,6 +16,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <utility>
 #include <vector>
@@ -158,10 +160,13 @@ struct ss2_ctx {
   float2 *d_part = nullptr;
   double *d_values = nullptr, *d_scores = nullptr, *d_params = nullptr;
   float *d_eotf = nullptr;
+  int *d_err = nullptr;            // error bits raised by kernels (bounded waits)
+  PlaneMaps maps;
   size_t ws_bytes = 0;
   // pinned read-back staging
   double *h_scores = nullptr;
   double *h_values = nullptr;
+  int *h_err = nullptr;
   size_t h_cap = 0;  // frames
   // per-kernel event timing (ss2_profile_begin / ss2_profile_end)
   bool prof = false;
@@ -214,20 +219,67 @@ void ss2::make_geom(int w, int h, int depth, int chroma, Geom &g) {
   g.nscales = n;
   long long xo = 0, ho = 0;
   int po = 0;
-  g.hline_off[0] = 0;
+  g.hunit_off[0] = 0;
   g.vwarp_off[0] = 0;
   for (int s = 0; s < n; ++s) {
     g.xoff[s] = xo; xo += 6 * g.plane[s];
     g.hoff[s] = ho; ho += (long long)3 * kNq * g.plane[s];
     g.poff[s] = po; po += 3 * kNSum * g.nw[s];
-    g.hline_off[s + 1] = g.hline_off[s] + 3 * g.hs[s];
+    g.hunit_off[s + 1] = g.hunit_off[s] + 3 * ((g.hs[s] + kBoxRows - 1) / kBoxRows);
     g.vwarp_off[s + 1] = g.vwarp_off[s] + 3 * g.nw[s];
   }
   for (int s = n; s < kMaxScales; ++s) {
-    g.hline_off[s + 1] = g.hline_off[s];
+    g.hunit_off[s + 1] = g.hunit_off[s];
     g.vwarp_off[s + 1] = g.vwarp_off[s];
   }
   g.x_fs = xo; g.h_fs = ho; g.p_fs = po;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// One 4-D map over a stack of fp32 planes: (column, row, plane, frame), boxes
+// of kBoxCols x kBoxRows, zero fill outside the tensor.
+static int encode_stack(CUtensorMap *m, float *base, int ws, int hs, int nplanes, int batch,
+                        long long pitch, long long plane, long long frame_stride) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SS2_EIO, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[4] = {(cuuint64_t)ws, (cuuint64_t)hs, (cuuint64_t)nplanes,
+                              (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)pitch * 4, (cuuint64_t)plane * 4,
+                                 (cuuint64_t)frame_stride * 4};
+  const cuuint32_t box[4] = {kBoxCols, kBoxRows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SS2_EIO, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return 0;
+}
+
+int ss2::encode_maps(const Geom &g, float *X, float *H, int batch, PlaneMaps &m) {
+  std::memset(&m, 0, sizeof(m));
+  for (int s = 0; s < g.nscales; ++s) {
+    if (encode_stack(&m.x[s], X + g.xoff[s], g.ws[s], g.hs[s], 6, batch, g.pitch[s], g.plane[s],
+                     g.x_fs) ||
+        encode_stack(&m.h[s], H + g.hoff[s], g.ws[s], g.hs[s], 3 * kNq, batch, g.pitch[s],
+                     g.plane[s], g.h_fs))
+      return t_err;
+  }
+  return 0;
 }
 
 size_t ss2::per_frame_bytes(const Geom &g) {
@@ -264,7 +316,8 @@ static void free_ctx(ss2_ctx *c) {
   if (!c) return;
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   cudaFree(c->d_X); cudaFree(c->d_H); cudaFree(c->d_part); cudaFree(c->d_values);
-  cudaFree(c->d_scores); cudaFree(c->d_params); cudaFree(c->d_eotf);
+  cudaFree(c->d_scores); cudaFree(c->d_params); cudaFree(c->d_eotf); cudaFree(c->d_err);
+  if (c->h_err) cudaFreeHost(c->h_err);
   cudaFree(c->d_in[0]); cudaFree(c->d_in[1]);
   if (c->h_scores) cudaFreeHost(c->h_scores);
   if (c->h_values) cudaFreeHost(c->h_values);
@@ -347,7 +400,8 @@ static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
       dev_alloc((void **)&c->d_values, B * kNValues * sizeof(double), &tot) ||
       dev_alloc((void **)&c->d_scores, B * sizeof(double), &tot) ||
       dev_alloc((void **)&c->d_params, kNParams * sizeof(double), &tot) ||
-      dev_alloc((void **)&c->d_eotf, (kEotfN + 1) * sizeof(float), &tot)) {
+      dev_alloc((void **)&c->d_eotf, (kEotfN + 1) * sizeof(float), &tot) ||
+      dev_alloc((void **)&c->d_err, sizeof(int), &tot)) {
     free_ctx(c);
     return nullptr;
   }
@@ -357,12 +411,14 @@ static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
   cudaError_t e = cudaMemcpy(c->d_eotf, T, sizeof(T), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(c->d_params, c->params, sizeof(c->params), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMallocHost((void **)&c->h_err, sizeof(int));
   if (e != cudaSuccess) {
     cuda_fail(e, "uploading constant tables");
     free_ctx(c);
     return nullptr;
   }
-  if (ensure_host_cap(c, (size_t)c->batch)) {
+  if (ensure_host_cap(c, (size_t)c->batch) || encode_maps(g, c->d_X, c->d_H, c->batch, c->maps)) {
     free_ctx(c);
     return nullptr;
   }
@@ -489,13 +545,30 @@ static int run_batch(ss2_ctx *c, const uint8_t *ref, const uint8_t *dis, int nb,
   const Geom &g = c->g;
   TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->d_eotf, ref, dis, c->d_X, nb, st),
         "k_pyramid launch");
-  TIMED(c, kKHblur, st, launch_hblur(g, c->px, c->d_X, c->d_H, nb, st), "k_hblur launch");
+  TIMED(c, kKHblur, st, launch_hblur(g, c->px, c->maps, c->d_err, nb, st), "k_hblur launch");
   TIMED(c, kKVblur, st, launch_vblur(g, c->px, c->d_X, c->d_H, c->d_part, nb, st),
         "k_vblur launch");
   TIMED(c, kKFinalize, st,
         launch_finalize(g, c->d_part, c->d_params, c->d_values, c->d_scores, nb, st),
         "k_finalize launch");
   return 0;
+}
+
+// Reads the kernels' error word after the stream's work (enqueue before the
+// stream synchronisation, check after it).
+static int enqueue_err_readback(ss2_ctx *c, cudaStream_t st) {
+  CU(cudaMemcpyAsync(c->h_err, c->d_err, sizeof(int), cudaMemcpyDeviceToHost, st),
+     "error word read-back");
+  return 0;
+}
+
+static int check_err_word(ss2_ctx *c, cudaStream_t st) {
+  if (*c->h_err == 0) return 0;
+  const int bits = *c->h_err;
+  *c->h_err = 0;
+  cudaMemsetAsync(c->d_err, 0, sizeof(int), st);
+  cudaStreamSynchronize(st);
+  return fail(SS2_EIO, "a kernel gave up waiting for a TMA transfer (error bits 0x%x)", bits);
 }
 
 static int check_call(ss2_ctx *ctx, const void *ref, const void *dis, int n) {
@@ -526,7 +599,9 @@ static int score_device(ss2_ctx *ctx, const void *ref, const void *dis, int n, d
                          (size_t)nb * kNValues * sizeof(double), cudaMemcpyDeviceToHost, st),
          "value read-back");
   }
+  if (enqueue_err_readback(ctx, st)) return t_err;
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  if (check_err_word(ctx, st)) return t_err;
   if (scores) std::memcpy(scores, ctx->h_scores, (size_t)n * sizeof(double));
   if (values) std::memcpy(values, ctx->h_values, (size_t)n * kNValues * sizeof(double));
   return 0;
@@ -591,7 +666,7 @@ SS2_API int ss2_score_frames_host(ss2_ctx *ctx, const void *ref_host, const void
           launch_pyramid(g, ctx->px, ctx->d_eotf, dref, ddis, ctx->d_X, nb, st),
           "k_pyramid launch");
     CU(cudaEventRecord(ctx->ev_consumed[slot], st), "event record");
-    TIMED(ctx, kKHblur, st, launch_hblur(g, ctx->px, ctx->d_X, ctx->d_H, nb, st),
+    TIMED(ctx, kKHblur, st, launch_hblur(g, ctx->px, ctx->maps, ctx->d_err, nb, st),
           "k_hblur launch");
     TIMED(ctx, kKVblur, st, launch_vblur(g, ctx->px, ctx->d_X, ctx->d_H, ctx->d_part, nb, st),
           "k_vblur launch");
@@ -602,7 +677,9 @@ SS2_API int ss2_score_frames_host(ss2_ctx *ctx, const void *ref_host, const void
                        cudaMemcpyDeviceToHost, st),
        "score read-back");
   }
+  if (enqueue_err_readback(ctx, st)) return t_err;
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  if (check_err_word(ctx, st)) return t_err;
   std::memcpy(scores, ctx->h_scores, (size_t)n_frames * sizeof(double));
   return 0;
 }
@@ -618,7 +695,7 @@ SS2_API int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis, int
   CU(launch_pyramid(g, ctx->px, ctx->d_eotf, (const uint8_t *)ref, (const uint8_t *)dis,
                     ctx->d_X, 1, st),
      "k_pyramid launch");
-  CU(launch_hblur(g, ctx->px, ctx->d_X, ctx->d_H, 1, st), "k_hblur launch");
+  CU(launch_hblur(g, ctx->px, ctx->maps, ctx->d_err, 1, st), "k_hblur launch");
   const size_t ws = g.ws[scale], hs = g.hs[scale];
   const size_t pitch_b = (size_t)g.pitch[scale] * sizeof(float);
   if (xyb)
@@ -633,8 +710,9 @@ SS2_API int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis, int
                            ctx->d_H + g.hoff[scale] + p * g.plane[scale], pitch_b,
                            ws * sizeof(float), hs, cudaMemcpyDeviceToHost, st),
          "plane read-back");
+  if (enqueue_err_readback(ctx, st)) return t_err;
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
-  return 0;
+  return check_err_word(ctx, st);
 }
 
 SS2_API int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream) {

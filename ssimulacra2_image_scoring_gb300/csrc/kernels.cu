@@ -21,6 +21,7 @@
 #include <algorithm>
 
 #include "ss2_device.cuh"
+#include "ss2_tma.cuh"
 #include "ss2_impl.h"
 #include "ss2_kernels.h"
 
@@ -166,50 +167,165 @@ __device__ __forceinline__ void res_zero(Res3 &r) {
 }
 
 // ---------------------------------------------------------------------------
-// k_hblur: one thread per (scale, row, channel) of a frame.
+// k_hblur: one warp per 32 rows of one (frame, scale, channel); lane = row.
+//
+// The rows are walked left to right in chunks of 8 columns.  TMA brings each
+// chunk of the two XYB planes (x1, x2) into a 4-slot shared-memory ring
+// (8 x 32 floats per plane, zero-filled outside the image, which is exactly
+// the recursion's zero extension), up to three chunks ahead of the walk.
+// Each lane reads its row with 16-byte loads; the recursion needs the
+// samples 5 ahead and 5 behind the step (the window of radius R = 4 has
+// taps at +-(R+1)), kept in rolling registers.  The five quantities
+// (x1, x2, x1^2, x2^2, x1 x2) are formed in registers.  The chunk's 5 x 8
+// outputs per lane go to a double-buffered shared tile and leave with TMA
+// stores (clipped to the image), so global traffic is whole boxes both ways.
+// Every mbarrier wait is bounded; a timeout raises kErrTmaTimeout.
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(128)
-    k_hblur(Geom g, Pix px, const float *__restrict__ X, float *__restrict__ H) {
+constexpr int kHWarps = 4;
+constexpr int kHSlots = 4;
+constexpr int kHBox = kBoxRows * kBoxCols;  // floats in one plane box (1 KB)
+
+struct HWarpSmem {
+  float in[kHSlots][2][kHBox];   // [slot][x1 | x2][row * 8 + col]
+  float out[2][kNq][kHBox];      // [buffer][quantity][row * 8 + col]
+};
+static_assert(sizeof(HWarpSmem) == 18432, "per-warp tile");
+// warp tiles, then the mbarriers; +1024 to align the base to 1 KB
+constexpr int kHSmemBytes = kHWarps * (int)sizeof(HWarpSmem) + kHWarps * kHSlots * 8 + 1024;
+
+__global__ void __launch_bounds__(kHWarps * 32)
+    k_hblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, int *__restrict__ err) {
+  extern __shared__ __align__(16) unsigned char hsm_raw[];
+  unsigned char *hsm = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(hsm_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int frame = blockIdx.y;
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= g.hline_off[g.nscales]) return;
+  const int unit = blockIdx.x * kHWarps + warp;
+  if (unit >= g.hunit_off[g.nscales]) return;  // whole warp
   int s = 0;
-  while (t >= g.hline_off[s + 1]) ++s;
-  const int local = t - g.hline_off[s];
-  const int c = local % 3, row = local / 3;
-  const int w = g.ws[s];
-  const float *x1 = X + (long long)frame * g.x_fs + g.xoff[s] + c * g.plane[s] +
-                    (long long)row * g.pitch[s];
-  const float *x2 = x1 + 3 * g.plane[s];
-  float *out = H + (long long)frame * g.h_fs + g.hoff[s] + (long long)(c * kNq) * g.plane[s] +
-               (long long)row * g.pitch[s];
-  const long long ps = g.plane[s];
+  while (unit >= g.hunit_off[s + 1]) ++s;
+  const int local = unit - g.hunit_off[s];
+  const int nrb = (g.hs[s] + kBoxRows - 1) / kBoxRows;
+  const int c = local / nrb, row0 = (local % nrb) * kBoxRows;
+  const int nchunk = (g.ws[s] + kBoxCols - 1) / kBoxCols;
+  HWarpSmem &sm = reinterpret_cast<HWarpSmem *>(hsm)[warp];
+  uint64_t *bar = reinterpret_cast<uint64_t *>(hsm + kHWarps * sizeof(HWarpSmem)) + warp * kHSlots;
+  const CUtensorMap *mx = &maps.x[s];
+  const CUtensorMap *mh = &maps.h[s];
+
+  if (lane == 0) {
+    for (int i = 0; i < kHSlots; ++i) mbar_init(&bar[i], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // chunk m (columns 8m .. 8m+7) of both planes -> slot m % 4
+  auto issue = [&](int m) {
+    const int slot = m & (kHSlots - 1);
+    mbar_arrive_expect_tx(&bar[slot], 2 * kHBox * (int)sizeof(float));
+    tma_load_4d(sm.in[slot][0], mx, &bar[slot], m * kBoxCols, row0, c, frame);
+    tma_load_4d(sm.in[slot][1], mx, &bar[slot], m * kBoxCols, row0, 3 + c, frame);
+  };
+  if (lane == 0)
+    for (int m = 0; m < kHSlots && m <= nchunk; ++m) issue(m);
+  auto wait_chunk = [&](int m) -> bool {
+    const bool ok = mbar_wait(&bar[m & (kHSlots - 1)], (uint32_t)(m >> 2) & 1u);
+    return __all_sync(0xffffffffu, ok);
+  };
+  auto bail = [&]() {
+    if (lane == 0) {
+      atomicOr(err, kErrTmaTimeout);
+      bulk_wait<0>();
+    }
+  };
 
   Res3 r[kNq];
 #pragma unroll
   for (int q = 0; q < kNq; ++q) res_zero(r[q]);
 
-  for (int i = -kReach; i <= w - 2; ++i) {
-    const int ia = i + kReach, ib = i - kReach;
-    const float a1 = ia < w ? __ldg(x1 + ia) : 0.0f;
-    const float a2 = ia < w ? __ldg(x2 + ia) : 0.0f;
-    const float b1 = ib >= 0 ? __ldg(x1 + ib) : 0.0f;
-    const float b2 = ib >= 0 ? __ldg(x2 + ib) : 0.0f;
-    float in[kNq];
-    in[0] = __fadd_rn(a1, b1);
-    in[1] = __fadd_rn(a2, b2);
-    in[2] = __fadd_rn(__fmul_rn(a1, a1), __fmul_rn(b1, b1));
-    in[3] = __fadd_rn(__fmul_rn(a2, a2), __fmul_rn(b2, b2));
-    in[4] = __fadd_rn(__fmul_rn(a1, a2), __fmul_rn(b1, b2));
-    float o[kNq];
+  // rolling 4-column groups of both planes: gm0 = cols 8k-8..8k-5,
+  // gm1 = 8k-4..8k-1, g0 = 8k..8k+3 (all zero before column 0)
+  float4 gm0[2], gm1[2], g0[2];
+  if (!wait_chunk(0)) { bail(); return; }
 #pragma unroll
-    for (int q = 0; q < kNq; ++q) o[q] = res_step(r[q], px, in[q]);
-    if (i + 1 >= 0) {
+  for (int p = 0; p < 2; ++p) {
+    gm0[p] = make_float4(0.f, 0.f, 0.f, 0.f);
+    gm1[p] = gm0[p];
+    g0[p] = *reinterpret_cast<const float4 *>(&sm.in[0][p][lane * kBoxCols]);
+  }
+  // warm-up steps producing Y[-4] .. Y[-1]: inputs x[0..3] ahead, zeros behind
+  {
+    const float a1[4] = {g0[0].x, g0[0].y, g0[0].z, g0[0].w};
+    const float a2[4] = {g0[1].x, g0[1].y, g0[1].z, g0[1].w};
 #pragma unroll
-      for (int q = 0; q < kNq; ++q) out[q * ps + i + 1] = o[q];
+    for (int j = 0; j < 4; ++j) {
+      float in[kNq];
+      in[0] = __fadd_rn(a1[j], 0.0f);
+      in[1] = __fadd_rn(a2[j], 0.0f);
+      in[2] = __fadd_rn(__fmul_rn(a1[j], a1[j]), 0.0f);
+      in[3] = __fadd_rn(__fmul_rn(a2[j], a2[j]), 0.0f);
+      in[4] = __fadd_rn(__fmul_rn(a1[j], a2[j]), 0.0f);
+#pragma unroll
+      for (int q = 0; q < kNq; ++q) res_step(r[q], px, in[q]);
     }
   }
+
+  for (int k = 0; k < nchunk; ++k) {
+    if (!wait_chunk(k + 1)) { bail(); return; }
+    const int sk = k & (kHSlots - 1), sk1 = (k + 1) & (kHSlots - 1);
+    float4 g1[2], gn[2];  // cols 8k+4..8k+7 and 8k+8..8k+11
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      g1[p] = *reinterpret_cast<const float4 *>(&sm.in[sk][p][lane * kBoxCols + 4]);
+      gn[p] = *reinterpret_cast<const float4 *>(&sm.in[sk1][p][lane * kBoxCols]);
+    }
+    __syncwarp();
+    if (lane == 0 && k + kHSlots <= nchunk) issue(k + kHSlots);  // slot k is free
+    float o[kNq][kBoxCols];
+    {
+      // step producing Y[8k + j] takes x[8k + j + 4] + x[8k + j - 6]
+      const float ah1[8] = {g1[0].x, g1[0].y, g1[0].z, g1[0].w, gn[0].x, gn[0].y, gn[0].z, gn[0].w};
+      const float ah2[8] = {g1[1].x, g1[1].y, g1[1].z, g1[1].w, gn[1].x, gn[1].y, gn[1].z, gn[1].w};
+      const float bh1[8] = {gm0[0].z, gm0[0].w, gm1[0].x, gm1[0].y, gm1[0].z, gm1[0].w, g0[0].x, g0[0].y};
+      const float bh2[8] = {gm0[1].z, gm0[1].w, gm1[1].x, gm1[1].y, gm1[1].z, gm1[1].w, g0[1].x, g0[1].y};
+#pragma unroll
+      for (int j = 0; j < kBoxCols; ++j) {
+        float in[kNq];
+        in[0] = __fadd_rn(ah1[j], bh1[j]);
+        in[1] = __fadd_rn(ah2[j], bh2[j]);
+        in[2] = __fadd_rn(__fmul_rn(ah1[j], ah1[j]), __fmul_rn(bh1[j], bh1[j]));
+        in[3] = __fadd_rn(__fmul_rn(ah2[j], ah2[j]), __fmul_rn(bh2[j], bh2[j]));
+        in[4] = __fadd_rn(__fmul_rn(ah1[j], ah2[j]), __fmul_rn(bh1[j], bh2[j]));
+#pragma unroll
+        for (int q = 0; q < kNq; ++q) o[q][j] = res_step(r[q], px, in[q]);
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      gm0[p] = g0[p];
+      gm1[p] = g1[p];
+      g0[p] = gn[p];
+    }
+    // the store issued from this buffer two chunks ago must have read it
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    const int ob = k & 1;
+#pragma unroll
+    for (int q = 0; q < kNq; ++q) {
+      float4 *d = reinterpret_cast<float4 *>(&sm.out[ob][q][lane * kBoxCols]);
+      d[0] = make_float4(o[q][0], o[q][1], o[q][2], o[q][3]);
+      d[1] = make_float4(o[q][4], o[q][5], o[q][6], o[q][7]);
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < kNq; ++q)
+        tma_store_4d(mh, sm.out[ob][q], k * kBoxCols, row0, c * kNq + q, frame);
+      bulk_commit();
+    }
+  }
+  if (lane == 0) bulk_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -407,11 +523,20 @@ cudaError_t launch_pyramid(const Geom &g, const Pix &px, const float *eotf, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_hblur(const Geom &g, const Pix &px, const float *X, float *H, int nframes,
-                         cudaStream_t st) {
-  const int lines = g.hline_off[g.nscales];
-  dim3 grid((lines + 127) / 128, nframes);
-  k_hblur<<<grid, 128, 0, st>>>(g, px, X, H);
+cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, int *err,
+                         int nframes, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[64] = {};
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(k_hblur, cudaFuncAttributeMaxDynamicSharedMemorySize, kHSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int units = g.hunit_off[g.nscales];
+  dim3 grid((units + kHWarps - 1) / kHWarps, nframes);
+  k_hblur<<<grid, kHWarps * 32, kHSmemBytes, st>>>(g, px, maps, err);
   return cudaGetLastError();
 }
 

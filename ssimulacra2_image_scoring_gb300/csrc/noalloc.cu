@@ -51,7 +51,8 @@ constexpr size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign;
 // head of the array: constant tables written once at set-up
 constexpr size_t kEotfOff = 0;
 constexpr size_t kParamsOff = align_up(kEotfOff + sizeof(float) * (ss2::kEotfN + 1));
-constexpr size_t kHeadBytes = align_up(kParamsOff + sizeof(double) * ss2::kNParams);
+constexpr size_t kErrOff = align_up(kParamsOff + sizeof(double) * ss2::kNParams);
+constexpr size_t kHeadBytes = align_up(kErrOff + sizeof(int));
 
 constexpr int kMaxDevices = 64;
 
@@ -81,6 +82,7 @@ static int scratch_for_device(int dev, unsigned char **out) {
     e = cudaMemcpy(base + kEotfOff, table, sizeof(table), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(base + kParamsOff, params, sizeof(params), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(base + kErrOff, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "scratch set-up copy");
     g_dev_ptr[dev] = base;
   }
@@ -132,13 +134,16 @@ SS2_API int ss2_score_frames_noalloc(int width, int height, int bitdepth, int ch
   default_params(pdef);
   Pix px;
   build_pix(pdef, px);
+  PlaneMaps maps;
+  if (encode_maps(g, X, H, nb_max, maps)) return ss2_last_error();
+  int *err = reinterpret_cast<int *>(base + kErrOff);
   cudaStream_t st = (cudaStream_t)stream;
   const uint8_t *r8 = static_cast<const uint8_t *>(ref), *d8 = static_cast<const uint8_t *>(dis);
   for (int f0 = 0; f0 < n_frames; f0 += nb_max) {
     const int nb = std::min(nb_max, n_frames - f0);
     const long long off = (long long)f0 * g.frame_bytes;
     cudaError_t e = launch_pyramid(g, px, eotf, r8 + off, d8 + off, X, nb, st);
-    if (e == cudaSuccess) e = launch_hblur(g, px, X, H, nb, st);
+    if (e == cudaSuccess) e = launch_hblur(g, px, maps, err, nb, st);
     if (e == cudaSuccess) e = launch_vblur(g, px, X, H, part, nb, st);
     if (e == cudaSuccess) e = launch_finalize(g, part, params, values, scores + f0, nb, st);
     if (e != cudaSuccess) return cuda_fail(e, "allocation-free scoring launch");

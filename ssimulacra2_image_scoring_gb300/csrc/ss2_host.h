@@ -20,6 +20,10 @@ int check_device(int *dev);                               // 0 or -ENOTSUP / -EI
 void make_geom(int w, int h, int depth, int chroma, Geom &g);
 size_t per_frame_bytes(const Geom &g);                    // workspace bytes per frame
 
+// TMA descriptors of the XYB and blurred-plane stacks of a workspace holding
+// `batch` frames (X, H: device bases of the frame blocks).
+int encode_maps(const Geom &g, float *X, float *H, int batch, PlaneMaps &maps);
+
 void default_params(double *params);                      // kNParams doubles
 void build_pix(const double *params, Pix &p);
 void build_eotf(float *table);                            // kEotfN + 1 floats

@@ -3,6 +3,8 @@
 // constants passed to every launch by value.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -38,9 +40,19 @@ struct Geom {
   int p_fs;                        // float2 per frame
   long long frame_bytes;
   // flat work decomposition over the scales
-  int hline_off[kMaxScales + 1];   // prefix of 3 * hs[s]     (horizontal lines)
-  int vwarp_off[kMaxScales + 1];   // prefix of 3 * nw[s]     (vertical warps)
+  int hunit_off[kMaxScales + 1];   // prefix of 3 * ceil(hs[s] / 32) (horizontal warps)
+  int vwarp_off[kMaxScales + 1];   // prefix of 3 * nw[s]            (vertical warps)
 };
+
+// TMA descriptors of the plane stacks, one per scale: x[s] views the XYB
+// block as a 4-D tensor (column, row, plane 0..5, frame) and h[s] the
+// horizontally blurred block (column, row, plane 0..14, frame); both use
+// 8-column x 32-row boxes.
+struct PlaneMaps {
+  CUtensorMap x[kMaxScales];
+  CUtensorMap h[kMaxScales];
+};
+constexpr int kBoxCols = 8, kBoxRows = 32;
 
 // Per-pixel constants (fp32 pipeline), rounded from the parameter vector.
 struct Pix {

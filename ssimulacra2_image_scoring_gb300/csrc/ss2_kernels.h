@@ -11,8 +11,8 @@ namespace ss2 {
 
 cudaError_t launch_pyramid(const Geom &g, const Pix &px, const float *eotf, const uint8_t *ref,
                            const uint8_t *dis, float *X, int nframes, cudaStream_t st);
-cudaError_t launch_hblur(const Geom &g, const Pix &px, const float *X, float *H, int nframes,
-                         cudaStream_t st);
+cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, int *err,
+                         int nframes, cudaStream_t st);
 cudaError_t launch_vblur(const Geom &g, const Pix &px, const float *X, const float *H,
                          float2 *part, int nframes, cudaStream_t st);
 cudaError_t launch_finalize(const Geom &g, const float2 *part, const double *params,
