@@ -252,16 +252,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // One 4-D map over a stack of fp32 planes: (column, row, plane, frame), boxes
-// of kBoxCols x kBoxRows, zero fill outside the tensor.
+// of bc x br x bp x 1, zero fill outside the tensor.
 static int encode_stack(CUtensorMap *m, float *base, int ws, int hs, int nplanes, int batch,
-                        long long pitch, long long plane, long long frame_stride) {
+                        long long pitch, long long plane, long long frame_stride, int bc, int br,
+                        int bp) {
   auto fn = encode_fn();
   if (!fn) return fail(SS2_EIO, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[4] = {(cuuint64_t)ws, (cuuint64_t)hs, (cuuint64_t)nplanes,
                               (cuuint64_t)batch};
   const cuuint64_t strides[3] = {(cuuint64_t)pitch * 4, (cuuint64_t)plane * 4,
                                  (cuuint64_t)frame_stride * 4};
-  const cuuint32_t box[4] = {kBoxCols, kBoxRows, 1, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)bc, (cuuint32_t)br, (cuuint32_t)bp, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -273,10 +274,16 @@ static int encode_stack(CUtensorMap *m, float *base, int ws, int hs, int nplanes
 int ss2::encode_maps(const Geom &g, float *X, float *H, int batch, PlaneMaps &m) {
   std::memset(&m, 0, sizeof(m));
   for (int s = 0; s < g.nscales; ++s) {
-    if (encode_stack(&m.x[s], X + g.xoff[s], g.ws[s], g.hs[s], 6, batch, g.pitch[s], g.plane[s],
-                     g.x_fs) ||
-        encode_stack(&m.h[s], H + g.hoff[s], g.ws[s], g.hs[s], 3 * kNq, batch, g.pitch[s],
-                     g.plane[s], g.h_fs))
+    float *xb = X + g.xoff[s], *hb = H + g.hoff[s];
+    const int ws = g.ws[s], hs = g.hs[s];
+    if (encode_stack(&m.x[s], xb, ws, hs, 6, batch, g.pitch[s], g.plane[s], g.x_fs, kBoxCols,
+                     kBoxRows, 1) ||
+        encode_stack(&m.h[s], hb, ws, hs, 3 * kNq, batch, g.pitch[s], g.plane[s], g.h_fs,
+                     kBoxCols, kBoxRows, 1) ||
+        encode_stack(&m.hv[s], hb, ws, hs, 3 * kNq, batch, g.pitch[s], g.plane[s], g.h_fs,
+                     kVCols, kVRows, kNq) ||
+        encode_stack(&m.xv[s], xb, ws, hs, 6, batch, g.pitch[s], g.plane[s], g.x_fs, kVCols,
+                     kVRows, 1))
       return t_err;
   }
   return 0;
@@ -546,7 +553,7 @@ static int run_batch(ss2_ctx *c, const uint8_t *ref, const uint8_t *dis, int nb,
   TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->d_eotf, ref, dis, c->d_X, nb, st),
         "k_pyramid launch");
   TIMED(c, kKHblur, st, launch_hblur(g, c->px, c->maps, c->d_err, nb, st), "k_hblur launch");
-  TIMED(c, kKVblur, st, launch_vblur(g, c->px, c->d_X, c->d_H, c->d_part, nb, st),
+  TIMED(c, kKVblur, st, launch_vblur(g, c->px, c->maps, c->d_part, c->d_err, nb, st),
         "k_vblur launch");
   TIMED(c, kKFinalize, st,
         launch_finalize(g, c->d_part, c->d_params, c->d_values, c->d_scores, nb, st),
@@ -668,7 +675,7 @@ SS2_API int ss2_score_frames_host(ss2_ctx *ctx, const void *ref_host, const void
     CU(cudaEventRecord(ctx->ev_consumed[slot], st), "event record");
     TIMED(ctx, kKHblur, st, launch_hblur(g, ctx->px, ctx->maps, ctx->d_err, nb, st),
           "k_hblur launch");
-    TIMED(ctx, kKVblur, st, launch_vblur(g, ctx->px, ctx->d_X, ctx->d_H, ctx->d_part, nb, st),
+    TIMED(ctx, kKVblur, st, launch_vblur(g, ctx->px, ctx->maps, ctx->d_part, ctx->d_err, nb, st),
           "k_vblur launch");
     TIMED(ctx, kKFinalize, st,
           launch_finalize(g, ctx->d_part, ctx->d_params, ctx->d_values, ctx->d_scores, nb, st),

@@ -376,24 +376,81 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
   acc.v[5] = ff_add(acc.v[5], det4);
 }
 
-__global__ void __launch_bounds__(128)
-    k_vblur(Geom g, Pix px, const float *__restrict__ X, const float *__restrict__ H,
-            float2 *__restrict__ part) {
+// Column walkers.  One warp per 32 columns of one (frame, scale, channel);
+// lane = column.  TMA brings 8-row chunks of the channel's five blurred
+// planes (one 32 x 8 x 5 box) into a 4-slot ring, up to two chunks ahead,
+// and 8-row chunks of the two XYB planes into a 2-slot ring.  Step n of the
+// recursion takes rows n+4 and n-6 of the blurred planes (taps at +-(R+1));
+// its outputs mu1, mu2, s11, s22, s12 feed the SSIM and edge terms of row n
+// at once, so the vertically blurred planes never exist in memory.
+constexpr int kVWarps = 4;
+constexpr int kVSlots = 4;
+constexpr int kVBox = kVRows * kVCols;          // floats per plane box (1 KB)
+
+struct VWarpSmem {
+  float h[kVSlots][kNq][kVBox];   // [slot][quantity][row * 32 + col]
+  float x[2][2][kVBox];           // [slot][x1 | x2][row * 32 + col]
+};
+static_assert(sizeof(VWarpSmem) == 24576, "per-warp tile");
+constexpr int kVSmemBytes = kVWarps * (int)sizeof(VWarpSmem) + kVWarps * 8 * 8 + 1024;
+
+__global__ void __launch_bounds__(kVWarps * 32)
+    k_vblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, float2 *__restrict__ part,
+            int *__restrict__ err) {
+  extern __shared__ __align__(16) unsigned char vsm_raw[];
+  unsigned char *vsm = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(vsm_raw) + 1023) & ~uintptr_t(1023));
   const int frame = blockIdx.y;
-  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wid = blockIdx.x * kVWarps + warp;
   if (wid >= g.vwarp_off[g.nscales]) return;  // whole warp exits together
   int s = 0;
   while (wid >= g.vwarp_off[s + 1]) ++s;
   const int local = wid - g.vwarp_off[s];
   const int c = local % 3, cb = local / 3;
-  const int col = cb * 32 + lane;
-  const bool active = col < g.ws[s];
+  const int col0 = cb * kVCols;
+  const bool active = col0 + lane < g.ws[s];
   const int h = g.hs[s];
-  const long long ps = g.plane[s], pitch = g.pitch[s];
-  const float *hp = H + (long long)frame * g.h_fs + g.hoff[s] + (long long)(c * kNq) * ps + col;
-  const float *x1p = X + (long long)frame * g.x_fs + g.xoff[s] + c * ps + col;
-  const float *x2p = x1p + 3 * ps;
+  const int nchunk = (h + kVRows - 1) / kVRows;
+  VWarpSmem &sm = reinterpret_cast<VWarpSmem *>(vsm)[warp];
+  uint64_t *hbar = reinterpret_cast<uint64_t *>(vsm + kVWarps * sizeof(VWarpSmem)) + warp * 8;
+  uint64_t *xbar = hbar + kVSlots;
+  const CUtensorMap *mh = &maps.hv[s];
+  const CUtensorMap *mx = &maps.xv[s];
+
+  if (lane == 0) {
+    for (int i = 0; i < kVSlots; ++i) mbar_init(&hbar[i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&xbar[i], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // blurred-plane chunk m (rows 8m .. 8m+7), m >= -1, lives in slot m % 4
+  auto issue_h = [&](int m) {
+    const int slot = m & (kVSlots - 1);
+    mbar_arrive_expect_tx(&hbar[slot], kNq * kVBox * (int)sizeof(float));
+    tma_load_4d(sm.h[slot][0], mh, &hbar[slot], col0, m * kVRows, c * kNq, frame);
+  };
+  auto issue_x = [&](int m) {
+    const int slot = m & 1;
+    mbar_arrive_expect_tx(&xbar[slot], 2 * kVBox * (int)sizeof(float));
+    tma_load_4d(sm.x[slot][0], mx, &xbar[slot], col0, m * kVRows, c, frame);
+    tma_load_4d(sm.x[slot][1], mx, &xbar[slot], col0, m * kVRows, 3 + c, frame);
+  };
+  if (lane == 0) {
+    for (int m = -1; m <= 2 && m <= nchunk; ++m) issue_h(m);
+    for (int m = 0; m <= 1 && m < nchunk; ++m) issue_x(m);
+  }
+  auto wait_h = [&](int m) -> bool {
+    const bool ok = mbar_wait(&hbar[m & (kVSlots - 1)], (uint32_t)((m + 1) >> 2) & 1u);
+    return __all_sync(0xffffffffu, ok);
+  };
+  auto wait_x = [&](int m) -> bool {
+    const bool ok = mbar_wait(&xbar[m & 1], (uint32_t)(m >> 1) & 1u);
+    return __all_sync(0xffffffffu, ok);
+  };
+  auto bail = [&]() {
+    if (lane == 0) atomicOr(err, kErrTmaTimeout);
+  };
 
   Acc6 acc;
 #pragma unroll
@@ -402,25 +459,44 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
   for (int q = 0; q < kNq; ++q) res_zero(r[q]);
 
-  if (active) {
-    for (int i = -kReach; i <= h - 2; ++i) {
-      const int ia = i + kReach, ib = i - kReach;
+  if (!wait_h(-1) || !wait_h(0)) { bail(); return; }
+  // warm-up steps producing Y[-4] .. Y[-1]: rows 0..3 ahead, zeros behind
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int q = 0; q < kNq; ++q)
+      res_step(r[q], px, __fadd_rn(sm.h[0][q][j * kVCols + lane], 0.0f));
+  }
+
+  for (int k = 0; k < nchunk; ++k) {
+    if (!wait_h(k + 1) || !wait_x(k)) { bail(); return; }
+    const int sp = (k - 1) & (kVSlots - 1), sk = k & (kVSlots - 1), sn = (k + 1) & (kVSlots - 1);
+    const int xs = k & 1;
+#pragma unroll
+    for (int j = 0; j < kVRows; ++j) {
+      // ahead row 8k + j + 4, behind row 8k + j - 6
+      const float *ha = j < 4 ? &sm.h[sk][0][(j + 4) * kVCols + lane]
+                              : &sm.h[sn][0][(j - 4) * kVCols + lane];
+      const float *hb = j < 6 ? &sm.h[sp][0][(j + 2) * kVCols + lane]
+                              : &sm.h[sk][0][(j - 6) * kVCols + lane];
       float o[kNq];
 #pragma unroll
-      for (int q = 0; q < kNq; ++q) {
-        const float a = ia < h ? __ldg(hp + q * ps + ia * pitch) : 0.0f;
-        const float b = ib >= 0 ? __ldg(hp + q * ps + ib * pitch) : 0.0f;
-        o[q] = res_step(r[q], px, __fadd_rn(a, b));
-      }
-      const int row = i + 1;
-      if (row >= 0) {
-        const float x1 = __ldg(x1p + row * pitch);
-        const float x2 = __ldg(x2p + row * pitch);
+      for (int q = 0; q < kNq; ++q)
+        o[q] = res_step(r[q], px, __fadd_rn(ha[q * kVBox], hb[q * kVBox]));
+      const int row = k * kVRows + j;
+      if (active && row < h) {
+        const float x1 = sm.x[xs][0][j * kVCols + lane];
+        const float x2 = sm.x[xs][1][j * kVCols + lane];
         ssim_edge_terms(px, o[0], o[1], o[2], o[3], o[4], x1, x2, acc);
       }
     }
+    __syncwarp();
+    if (lane == 0) {
+      if (k + 3 <= nchunk) issue_h(k + 3);       // into the slot of chunk k - 1
+      if (k + 2 < nchunk) issue_x(k + 2);        // into the slot of chunk k
+    }
   }
-  // fixed butterfly-free tree: lane l adds lane l + 2^k for k = 4..0
+  // fixed tree: lane l adds lane l + 2^m for m = 4..0
 #pragma unroll
   for (int k = 0; k < kNSum; ++k) {
     ff v = acc.v[k];
@@ -540,11 +616,20 @@ cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_vblur(const Geom &g, const Pix &px, const float *X, const float *H,
-                         float2 *part, int nframes, cudaStream_t st) {
+cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, float2 *part,
+                         int *err, int nframes, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[64] = {};
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(k_vblur, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
   const int warps = g.vwarp_off[g.nscales];
-  dim3 grid((warps + 3) / 4, nframes);
-  k_vblur<<<grid, 128, 0, st>>>(g, px, X, H, part);
+  dim3 grid((warps + kVWarps - 1) / kVWarps, nframes);
+  k_vblur<<<grid, kVWarps * 32, kVSmemBytes, st>>>(g, px, maps, part, err);
   return cudaGetLastError();
 }
 

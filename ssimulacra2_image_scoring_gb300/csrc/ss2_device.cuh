@@ -59,25 +59,45 @@ __device__ __forceinline__ ff ff_mul(ff a, ff b) {
   return quick_two_sum(p.hi, __fadd_rn(p.lo, c));
 }
 
-// a / b for a pair numerator and a float denominator: q1 = RN(a.hi / b);
-// the residual a.hi - q1 b is exact in one fma (q1 is correctly rounded),
-// the low word is folded in and the second quotient needs only ~24 bits.
+// Approximate reciprocal (one MUFU operation, relative error near 2^-23).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// a / b to within an ulp: the product a * (1/b) corrected by one
+// Newton-Raphson step on its residual (Markstein, IBM J. Res. Dev. 34(1),
+// 1990).  The quotient is faithful, so the residual a - q b it leaves is
+// exactly representable and a second partial quotient recovers the rest.
+// When a == b the corrected quotient is exactly 1.
+__device__ __forceinline__ float div_newton(float a, float b, float rb) {
+  const float q0 = __fmul_rn(a, rb);
+  const float e = __fmaf_rn(-q0, b, a);
+  return __fmaf_rn(e, rb, q0);
+}
+
+// a / b for a pair numerator and a float denominator: two partial quotients
+// (Finding 4: "two correctly rounded partial quotients", here the first is
+// faithful and the exact residual makes the pair accurate to about 2^-46).
 __device__ __forceinline__ ff ff_div_f(ff a, float b) {
-  float q1 = __fdiv_rn(a.hi, b);
+  const float rb = rcp_approx(b);
+  const float q1 = div_newton(a.hi, b, rb);
   float r = __fmaf_rn(-q1, b, a.hi);
   r = __fadd_rn(r, a.lo);
-  float q2 = __fdividef(r, b);
+  const float q2 = __fmul_rn(r, rb);
   return quick_two_sum(q1, q2);
 }
 
 // a / b for pairs (same scheme, the denominator's low word enters the
 // residual).
 __device__ __forceinline__ ff ff_div(ff a, ff b) {
-  float q1 = __fdiv_rn(a.hi, b.hi);
+  const float rb = rcp_approx(b.hi);
+  const float q1 = div_newton(a.hi, b.hi, rb);
   float r = __fmaf_rn(-q1, b.hi, a.hi);
   r = __fadd_rn(r, a.lo);
   r = __fmaf_rn(-q1, b.lo, r);
-  float q2 = __fdividef(r, b.hi);
+  const float q2 = __fmul_rn(r, rb);
   return quick_two_sum(q1, q2);
 }
 
@@ -113,10 +133,9 @@ __device__ __forceinline__ int cube_cmp(uint32_t M, int f, uint32_t X, int g) {
   return c > rhs ? 1 : (c < rhs ? -1 : 0);
 }
 
-// Correctly rounded cbrt for x >= 0 finite.
-__device__ __forceinline__ float cbrt_cr(float x) {
-  if (x == 0.0f) return 0.0f;
-  float y = cbrtf(x);
+// Exact rounding decision: moves y until x lies strictly between the cubes
+// of the two midpoints around it.
+__device__ __noinline__ float cbrt_round_exact(float x, float y) {
   uint32_t X;
   int g;
   float_parts(x, X, g);
@@ -139,6 +158,34 @@ __device__ __forceinline__ float cbrt_cr(float x) {
     break;
   }
   return y;
+}
+
+// Correctly rounded cbrt for x >= 0 finite.  y = cbrtf(x) is within an ulp.
+// The residual R = x - y^3 is formed to about 2^-43 x with error-free
+// products (y^2 = p + e exactly, y p = q1 + q2 exactly, x - q1 exact by
+// Sterbenz), and the root's offset from y is R / (3 y^2) to first order, so
+// |R| against T = 1.5 y^2 u (half an ulp u of y, in residual units) decides
+// the rounding.  Within 2^-16 of the boundary, at a power of two (where the
+// spacing below halves) and below x = 2^-100 (where the error terms of the
+// products would underflow), the exact integer test decides.
+__device__ __forceinline__ float cbrt_cr(float x) {
+  if (x == 0.0f) return 0.0f;
+  const float y = cbrtf(x);
+  const uint32_t yb = __float_as_uint(y);
+  if ((yb & 0x7fffffu) == 0u || __float_as_uint(x) < 0x0d800000u) return cbrt_round_exact(x, y);
+  const ff y2 = two_prod(y, y);
+  const ff y3 = two_prod(y, y2.hi);
+  const float y3c = __fmul_rn(y, y2.lo);
+  float r = __fsub_rn(x, y3.hi);
+  r = __fsub_rn(r, y3.lo);
+  r = __fsub_rn(r, y3c);
+  const float u = __uint_as_float((yb & 0x7f800000u) - (23u << 23));  // ulp(y)
+  const float T = __fmul_rn(__fmul_rn(1.5f, y2.hi), u);
+  const float ar = fabsf(r);
+  if (ar < __fmul_rn(T, 0.9999847412109375f)) return y;             // |offset| < u/2
+  if (ar > __fmul_rn(T, 1.0000152587890625f) && ar < __fmul_rn(T, 2.9f))
+    return __uint_as_float(r > 0.0f ? yb + 1u : yb - 1u);           // u/2 < |offset| < 1.45u
+  return cbrt_round_exact(x, y);
 }
 
 // ---------------------------------------------------------------------------
