@@ -63,9 +63,10 @@ typedef struct ss2_ctx ss2_ctx;
  * CUDA device.  width, height >= 8 and <= SS2_MAX_DIM; bitdepth 8..16;
  * chroma one of 420, 422, 444; subsampled chroma needs an even width
  * (Research-1363, "Sources": the CLI rejects odd widths for 4:2:0).
- * The context owns a device workspace for a batch of frames in flight,
- * chosen from the geometry (ss2_create_batch sets it), and holds the
- * default parameter vector (see ss2_default_params).
+ * The context owns two device workspaces, each for a batch of frames
+ * (chosen from the geometry; ss2_create_batch sets it), used in turn on two
+ * internal streams so that consecutive batches overlap on the GPU, and holds
+ * the default parameter vector (see ss2_default_params).
  * Returns NULL on failure: -EINVAL (bad geometry), -ENOTSUP (no sm_103
  * device), -ENOMEM, -EIO.
  */
@@ -85,10 +86,12 @@ void ss2_destroy(ss2_ctx *ctx);
  *   ref, dis: DEVICE pointers, caller-owned, n_frames packed frames each,
  *             read only during the call, not retained.
  *   scores:   HOST array of n_frames doubles, caller-owned.
- *   stream:   cudaStream_t (NULL = legacy default stream); all work is
- *             enqueued on it and the call returns after the scores have
- *             reached host memory (one stream synchronisation per call,
- *             8 bytes read back per frame).
+ *   stream:   cudaStream_t (NULL = legacy default stream); the work starts
+ *             after what is already queued on it (the context's two
+ *             internal streams wait on an event recorded there, and the
+ *             stream waits for them at the end); the call returns after the
+ *             scores have reached host memory (one stream synchronisation
+ *             per call, 8 bytes read back per frame).
  * n_frames == 0 is a no-op returning 0.  Returns 0 or a negative code;
  * on -EINVAL nothing was enqueued.
  */
@@ -153,7 +156,7 @@ int ss2_profile_end(ss2_ctx *ctx, double *ms, int *launches);
 /* ss2_frame_bytes — bytes of one packed frame of the context's geometry. */
 size_t ss2_frame_bytes(const ss2_ctx *ctx);
 
-/* ss2_batch — frames processed per pass (the workspace's batch size).    */
+/* ss2_batch — frames processed per pass (each workspace's batch size).   */
 int ss2_batch(const ss2_ctx *ctx);
 
 /* ss2_workspace_bytes — device bytes the context holds.                  */

@@ -149,19 +149,35 @@ void ss2::default_params(double *p) {
 // Context
 // ---------------------------------------------------------------------------
 
+// A lane is one pass of the pipeline in flight: a workspace for `batch`
+// frames and an internal stream.  Batches alternate between the two lanes,
+// so the memory-bound pass of one batch can run beside the arithmetic-bound
+// passes of the other.
+constexpr int kLanes = 2;
+
+struct Lane {
+  float *X = nullptr, *H = nullptr;
+  float2 *part = nullptr;
+  double *values = nullptr, *scores = nullptr;
+  PlaneMaps maps;
+  cudaStream_t st = nullptr;
+  cudaEvent_t ev_done = nullptr;
+  // host-input path (allocated on first use): ref then dis frames of a batch
+  uint8_t *in = nullptr;
+  cudaEvent_t ev_copied = nullptr, ev_consumed = nullptr;
+};
+
 struct ss2_ctx {
   Geom g;
   Pix px;
   int batch;
   int device;
   double params[kNParams];
-  // device workspace
-  float *d_X = nullptr, *d_H = nullptr;
-  float2 *d_part = nullptr;
-  double *d_values = nullptr, *d_scores = nullptr, *d_params = nullptr;
+  Lane lane[kLanes];
+  double *d_params = nullptr;
   float *d_eotf = nullptr;
   int *d_err = nullptr;            // error bits raised by kernels (bounded waits)
-  PlaneMaps maps;
+  cudaEvent_t ev_fork = nullptr;
   size_t ws_bytes = 0;
   // pinned read-back staging
   double *h_scores = nullptr;
@@ -172,10 +188,7 @@ struct ss2_ctx {
   bool prof = false;
   std::vector<cudaEvent_t> ev_pool;
   std::vector<std::pair<int, int>> ev_used;  // (kernel class, index of start event)
-  // host-input path (allocated on first use)
-  uint8_t *d_in[2] = {nullptr, nullptr};
-  cudaStream_t copy_stream = nullptr;
-  cudaEvent_t ev_copied[2] = {nullptr, nullptr}, ev_consumed[2] = {nullptr, nullptr};
+  cudaStream_t copy_stream = nullptr;   // host-input path uploads
 };
 
 static int chroma_shift(int chroma, int *sx, int *sy) {
@@ -294,12 +307,12 @@ size_t ss2::per_frame_bytes(const Geom &g) {
          (kNValues + 1) * sizeof(double);
 }
 
-// Frames in flight per pass: enough column walkers at scale 0 to fill the
-// GPU (about 160k threads, 3 per column), within a 24 GB workspace.
+// Frames per pass: enough column walkers at scale 0 to fill the GPU (about
+// 160k threads, 3 per column), within 16 GB per lane workspace.
 static int default_batch(const Geom &g) {
   long long b = (160000LL + 3LL * g.w - 1) / (3LL * g.w);
   b = std::max(4LL, std::min(64LL, b));
-  const long long cap = (24LL << 30) / (long long)per_frame_bytes(g);
+  const long long cap = (16LL << 30) / (long long)per_frame_bytes(g);
   b = std::max(1LL, std::min(b, cap));
   return (int)b;
 }
@@ -322,16 +335,19 @@ static void set_pix(ss2_ctx *c) { build_pix(c->params, c->px); }
 static void free_ctx(ss2_ctx *c) {
   if (!c) return;
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
-  cudaFree(c->d_X); cudaFree(c->d_H); cudaFree(c->d_part); cudaFree(c->d_values);
-  cudaFree(c->d_scores); cudaFree(c->d_params); cudaFree(c->d_eotf); cudaFree(c->d_err);
+  for (Lane &L : c->lane) {
+    cudaFree(L.X); cudaFree(L.H); cudaFree(L.part); cudaFree(L.values); cudaFree(L.scores);
+    cudaFree(L.in);
+    if (L.st) cudaStreamDestroy(L.st);
+    if (L.ev_done) cudaEventDestroy(L.ev_done);
+    if (L.ev_copied) cudaEventDestroy(L.ev_copied);
+    if (L.ev_consumed) cudaEventDestroy(L.ev_consumed);
+  }
+  cudaFree(c->d_params); cudaFree(c->d_eotf); cudaFree(c->d_err);
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
   if (c->h_err) cudaFreeHost(c->h_err);
-  cudaFree(c->d_in[0]); cudaFree(c->d_in[1]);
   if (c->h_scores) cudaFreeHost(c->h_scores);
   if (c->h_values) cudaFreeHost(c->h_values);
-  for (int i = 0; i < 2; ++i) {
-    if (c->ev_copied[i]) cudaEventDestroy(c->ev_copied[i]);
-    if (c->ev_consumed[i]) cudaEventDestroy(c->ev_consumed[i]);
-  }
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   delete c;
 }
@@ -401,12 +417,30 @@ static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
   const Geom &g = c->g;
   const size_t B = (size_t)c->batch;
   size_t tot = 0;
-  if (dev_alloc((void **)&c->d_X, B * g.x_fs * sizeof(float), &tot) ||
-      dev_alloc((void **)&c->d_H, B * g.h_fs * sizeof(float), &tot) ||
-      dev_alloc((void **)&c->d_part, B * g.p_fs * sizeof(float2), &tot) ||
-      dev_alloc((void **)&c->d_values, B * kNValues * sizeof(double), &tot) ||
-      dev_alloc((void **)&c->d_scores, B * sizeof(double), &tot) ||
-      dev_alloc((void **)&c->d_params, kNParams * sizeof(double), &tot) ||
+  for (Lane &L : c->lane) {
+    if (dev_alloc((void **)&L.X, B * g.x_fs * sizeof(float), &tot) ||
+        dev_alloc((void **)&L.H, B * g.h_fs * sizeof(float), &tot) ||
+        dev_alloc((void **)&L.part, B * g.p_fs * sizeof(float2), &tot) ||
+        dev_alloc((void **)&L.values, B * kNValues * sizeof(double), &tot) ||
+        dev_alloc((void **)&L.scores, B * sizeof(double), &tot) ||
+        encode_maps(g, L.X, L.H, c->batch, L.maps)) {
+      free_ctx(c);
+      return nullptr;
+    }
+    cudaError_t e = cudaStreamCreateWithFlags(&L.st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L.ev_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "lane stream");
+      free_ctx(c);
+      return nullptr;
+    }
+  }
+  if (cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess) {
+    cuda_fail(cudaGetLastError(), "fork event");
+    free_ctx(c);
+    return nullptr;
+  }
+  if (dev_alloc((void **)&c->d_params, kNParams * sizeof(double), &tot) ||
       dev_alloc((void **)&c->d_eotf, (kEotfN + 1) * sizeof(float), &tot) ||
       dev_alloc((void **)&c->d_err, sizeof(int), &tot)) {
     free_ctx(c);
@@ -425,7 +459,7 @@ static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
     free_ctx(c);
     return nullptr;
   }
-  if (ensure_host_cap(c, (size_t)c->batch) || encode_maps(g, c->d_X, c->d_H, c->batch, c->maps)) {
+  if (ensure_host_cap(c, (size_t)c->batch)) {
     free_ctx(c);
     return nullptr;
   }
@@ -547,17 +581,42 @@ SS2_API int ss2_profile_end(ss2_ctx *ctx, double *ms, int *launches) {
 // One pass of the pipeline over nb frames already on the device.
 // ---------------------------------------------------------------------------
 
-static int run_batch(ss2_ctx *c, const uint8_t *ref, const uint8_t *dis, int nb,
-                     cudaStream_t st) {
+static int run_batch(ss2_ctx *c, Lane &L, const uint8_t *ref, const uint8_t *dis, int nb,
+                     cudaEvent_t after_pyramid) {
   const Geom &g = c->g;
-  TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->d_eotf, ref, dis, c->d_X, nb, st),
+  cudaStream_t st = L.st;
+  TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->d_eotf, ref, dis, L.X, nb, st),
         "k_pyramid launch");
-  TIMED(c, kKHblur, st, launch_hblur(g, c->px, c->maps, c->d_err, nb, st), "k_hblur launch");
-  TIMED(c, kKVblur, st, launch_vblur(g, c->px, c->maps, c->d_part, c->d_err, nb, st),
+  if (after_pyramid) CU(cudaEventRecord(after_pyramid, st), "event record");
+  TIMED(c, kKHblur, st, launch_hblur(g, c->px, L.maps, c->d_err, nb, st), "k_hblur launch");
+  TIMED(c, kKVblur, st, launch_vblur(g, c->px, L.maps, L.part, c->d_err, nb, st),
         "k_vblur launch");
   TIMED(c, kKFinalize, st,
-        launch_finalize(g, c->d_part, c->d_params, c->d_values, c->d_scores, nb, st),
+        launch_finalize(g, L.part, c->d_params, L.values, L.scores, nb, st),
         "k_finalize launch");
+  return 0;
+}
+
+// Batches of a call: as few as the workspace allows, of near-equal size.
+static void batch_plan(int n, int cap, int *nbatches, int *base, int *extra) {
+  *nbatches = (n + cap - 1) / cap;
+  *base = n / *nbatches;
+  *extra = n % *nbatches;   // the first `extra` batches take one more frame
+}
+
+// The lanes' streams start after the work already on the caller's stream...
+static int fork_lanes(ss2_ctx *c, cudaStream_t st) {
+  CU(cudaEventRecord(c->ev_fork, st), "fork event");
+  for (Lane &L : c->lane) CU(cudaStreamWaitEvent(L.st, c->ev_fork, 0), "fork wait");
+  return 0;
+}
+
+// ...and the caller's stream continues after the lanes' work.
+static int join_lanes(ss2_ctx *c, cudaStream_t st) {
+  for (Lane &L : c->lane) {
+    CU(cudaEventRecord(L.ev_done, L.st), "join event");
+    CU(cudaStreamWaitEvent(st, L.ev_done, 0), "join wait");
+  }
   return 0;
 }
 
@@ -595,17 +654,23 @@ static int score_device(ss2_ctx *ctx, const void *ref, const void *dis, int n, d
   cudaStream_t st = (cudaStream_t)stream;
   const uint8_t *r8 = (const uint8_t *)ref, *d8 = (const uint8_t *)dis;
   const long long fb = ctx->g.frame_bytes;
-  for (int f0 = 0; f0 < n; f0 += ctx->batch) {
-    const int nb = std::min(ctx->batch, n - f0);
-    if (run_batch(ctx, r8 + f0 * fb, d8 + f0 * fb, nb, st)) return t_err;
-    CU(cudaMemcpyAsync(ctx->h_scores + f0, ctx->d_scores, nb * sizeof(double),
-                       cudaMemcpyDeviceToHost, st),
+  int nbat, base, extra;
+  batch_plan(n, ctx->batch, &nbat, &base, &extra);
+  if (fork_lanes(ctx, st)) return t_err;
+  for (int b = 0, f0 = 0; b < nbat; ++b) {
+    const int nb = base + (b < extra ? 1 : 0);
+    Lane &L = ctx->lane[b % kLanes];
+    if (run_batch(ctx, L, r8 + f0 * fb, d8 + f0 * fb, nb, nullptr)) return t_err;
+    CU(cudaMemcpyAsync(ctx->h_scores + f0, L.scores, nb * sizeof(double),
+                       cudaMemcpyDeviceToHost, L.st),
        "score read-back");
     if (values)
-      CU(cudaMemcpyAsync(ctx->h_values + (size_t)f0 * kNValues, ctx->d_values,
-                         (size_t)nb * kNValues * sizeof(double), cudaMemcpyDeviceToHost, st),
+      CU(cudaMemcpyAsync(ctx->h_values + (size_t)f0 * kNValues, L.values,
+                         (size_t)nb * kNValues * sizeof(double), cudaMemcpyDeviceToHost, L.st),
          "value read-back");
+    f0 += nb;
   }
+  if (join_lanes(ctx, st)) return t_err;
   if (enqueue_err_readback(ctx, st)) return t_err;
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
   if (check_err_word(ctx, st)) return t_err;
@@ -627,17 +692,16 @@ SS2_API int ss2_values(ss2_ctx *ctx, const void *ref, const void *dis, int n_fra
 }
 
 static int ensure_upload_slots(ss2_ctx *c) {
-  if (c->d_in[0]) return 0;
+  if (c->lane[0].in) return 0;
   const size_t bytes = 2 * (size_t)c->batch * (size_t)c->g.frame_bytes;  // ref + dis
   size_t tot = 0;
-  for (int i = 0; i < 2; ++i)
-    if (dev_alloc((void **)&c->d_in[i], bytes, &tot)) return t_err;
+  for (Lane &L : c->lane) {
+    if (dev_alloc((void **)&L.in, bytes, &tot)) return t_err;
+    CU(cudaEventCreateWithFlags(&L.ev_copied, cudaEventDisableTiming), "event");
+    CU(cudaEventCreateWithFlags(&L.ev_consumed, cudaEventDisableTiming), "event");
+  }
   c->ws_bytes += tot;
   CU(cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking), "copy stream");
-  for (int i = 0; i < 2; ++i) {
-    CU(cudaEventCreateWithFlags(&c->ev_copied[i], cudaEventDisableTiming), "event");
-    CU(cudaEventCreateWithFlags(&c->ev_consumed[i], cudaEventDisableTiming), "event");
-  }
   return 0;
 }
 
@@ -653,37 +717,30 @@ SS2_API int ss2_score_frames_host(ss2_ctx *ctx, const void *ref_host, const void
   const long long fb = ctx->g.frame_bytes;
   const size_t half = (size_t)ctx->batch * (size_t)fb;
   const uint8_t *r8 = (const uint8_t *)ref_host, *d8 = (const uint8_t *)dis_host;
-  int k = 0;
-  for (int f0 = 0; f0 < n_frames; f0 += ctx->batch, ++k) {
-    const int nb = std::min(ctx->batch, n_frames - f0);
-    const int slot = k & 1;
-    uint8_t *dref = ctx->d_in[slot], *ddis = ctx->d_in[slot] + half;
-    // slot fence: the upload waits for the kernel that last read this slot
-    CU(cudaStreamWaitEvent(ctx->copy_stream, ctx->ev_consumed[slot], 0), "slot fence");
+  int nbat, base, extra;
+  batch_plan(n_frames, ctx->batch, &nbat, &base, &extra);
+  if (fork_lanes(ctx, st)) return t_err;
+  for (int b = 0, f0 = 0; b < nbat; ++b) {
+    const int nb = base + (b < extra ? 1 : 0);
+    Lane &L = ctx->lane[b % kLanes];
+    uint8_t *dref = L.in, *ddis = L.in + half;
+    // slot fence: the upload waits for the kernel that last read this lane's slot
+    CU(cudaStreamWaitEvent(ctx->copy_stream, L.ev_consumed, 0), "slot fence");
     CU(cudaMemcpyAsync(dref, r8 + f0 * fb, (size_t)nb * fb, cudaMemcpyHostToDevice,
                        ctx->copy_stream),
        "ref upload");
     CU(cudaMemcpyAsync(ddis, d8 + f0 * fb, (size_t)nb * fb, cudaMemcpyHostToDevice,
                        ctx->copy_stream),
        "dis upload");
-    CU(cudaEventRecord(ctx->ev_copied[slot], ctx->copy_stream), "event record");
-    CU(cudaStreamWaitEvent(st, ctx->ev_copied[slot], 0), "upload wait");
-    const Geom &g = ctx->g;
-    TIMED(ctx, kKPyramid, st,
-          launch_pyramid(g, ctx->px, ctx->d_eotf, dref, ddis, ctx->d_X, nb, st),
-          "k_pyramid launch");
-    CU(cudaEventRecord(ctx->ev_consumed[slot], st), "event record");
-    TIMED(ctx, kKHblur, st, launch_hblur(g, ctx->px, ctx->maps, ctx->d_err, nb, st),
-          "k_hblur launch");
-    TIMED(ctx, kKVblur, st, launch_vblur(g, ctx->px, ctx->maps, ctx->d_part, ctx->d_err, nb, st),
-          "k_vblur launch");
-    TIMED(ctx, kKFinalize, st,
-          launch_finalize(g, ctx->d_part, ctx->d_params, ctx->d_values, ctx->d_scores, nb, st),
-          "k_finalize launch");
-    CU(cudaMemcpyAsync(ctx->h_scores + f0, ctx->d_scores, nb * sizeof(double),
-                       cudaMemcpyDeviceToHost, st),
+    CU(cudaEventRecord(L.ev_copied, ctx->copy_stream), "event record");
+    CU(cudaStreamWaitEvent(L.st, L.ev_copied, 0), "upload wait");
+    if (run_batch(ctx, L, dref, ddis, nb, L.ev_consumed)) return t_err;
+    CU(cudaMemcpyAsync(ctx->h_scores + f0, L.scores, nb * sizeof(double),
+                       cudaMemcpyDeviceToHost, L.st),
        "score read-back");
+    f0 += nb;
   }
+  if (join_lanes(ctx, st)) return t_err;
   if (enqueue_err_readback(ctx, st)) return t_err;
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
   if (check_err_word(ctx, st)) return t_err;
@@ -699,22 +756,23 @@ SS2_API int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis, int
   CU(cudaSetDevice(ctx->device), "cudaSetDevice");
   cudaStream_t st = (cudaStream_t)stream;
   const Geom &g = ctx->g;
-  CU(launch_pyramid(g, ctx->px, ctx->d_eotf, (const uint8_t *)ref, (const uint8_t *)dis,
-                    ctx->d_X, 1, st),
+  Lane &L = ctx->lane[0];
+  CU(launch_pyramid(g, ctx->px, ctx->d_eotf, (const uint8_t *)ref, (const uint8_t *)dis, L.X,
+                    1, st),
      "k_pyramid launch");
-  CU(launch_hblur(g, ctx->px, ctx->maps, ctx->d_err, 1, st), "k_hblur launch");
+  CU(launch_hblur(g, ctx->px, L.maps, ctx->d_err, 1, st), "k_hblur launch");
   const size_t ws = g.ws[scale], hs = g.hs[scale];
   const size_t pitch_b = (size_t)g.pitch[scale] * sizeof(float);
   if (xyb)
     for (int p = 0; p < 6; ++p)
       CU(cudaMemcpy2DAsync(xyb + p * ws * hs, ws * sizeof(float),
-                           ctx->d_X + g.xoff[scale] + p * g.plane[scale], pitch_b,
+                           L.X + g.xoff[scale] + p * g.plane[scale], pitch_b,
                            ws * sizeof(float), hs, cudaMemcpyDeviceToHost, st),
          "plane read-back");
   if (hblur)
     for (int p = 0; p < 3 * kNq; ++p)
       CU(cudaMemcpy2DAsync(hblur + p * ws * hs, ws * sizeof(float),
-                           ctx->d_H + g.hoff[scale] + p * g.plane[scale], pitch_b,
+                           L.H + g.hoff[scale] + p * g.plane[scale], pitch_b,
                            ws * sizeof(float), hs, cudaMemcpyDeviceToHost, st),
          "plane read-back");
   if (enqueue_err_readback(ctx, st)) return t_err;
