@@ -334,9 +334,23 @@ __global__ void __launch_bounds__(kHWarps * 32)
 // six float-pair sums, then a fixed shuffle tree gives one pair per warp.
 // ---------------------------------------------------------------------------
 
+// Six float-pair sums per lane.  An addition keeps the high word exact
+// (two_sum) and folds the rounding error and the term's low word into the
+// low word without renormalising; acc_renorm restores |lo| <= ulp(hi)/2
+// once per chunk of rows, which bounds the low word's own rounding.
 struct Acc6 {
   ff v[kNSum];
 };
+
+__device__ __forceinline__ ff acc_add(ff s, ff t) {
+  const ff h = two_sum(s.hi, t.hi);
+  return {h.hi, __fadd_rn(s.lo, __fadd_rn(h.lo, t.lo))};
+}
+
+__device__ __forceinline__ void acc_renorm(Acc6 &a) {
+#pragma unroll
+  for (int k = 0; k < kNSum; ++k) a.v[k] = quick_two_sum(a.v[k].hi, a.v[k].lo);
+}
 
 __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float mu2, float s11,
                                                 float s22, float s12, float x1, float x2,
@@ -351,29 +365,35 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
   const float den_s = __fadd_rn(__fadd_rn(v1, v2), px.c2);
   // float-pair part: q = num_m num_s / den_s, d = max(1 - q, 0)
   const ff q = ff_div_f(two_prod(num_m, num_s), den_s);
-  ff d = ff_add(ff{1.0f, 0.0f}, ff{-q.hi, -q.lo});
+  const ff one_m = two_sum(1.0f, -q.hi);
+  ff d = quick_two_sum(one_m.hi, __fsub_rn(one_m.lo, q.lo));
   if (!(d.hi > 0.0f)) d = {0.0f, 0.0f};
   const ff d2 = ff_mul(d, d);
   const ff d4 = ff_mul(d2, d2);
-  acc.v[0] = ff_add(acc.v[0], d);
-  acc.v[1] = ff_add(acc.v[1], d4);
-  // edge_diff_map: r = (1 + |x2 - mu2|) / (1 + |x1 - mu1|) - 1
+  acc.v[0] = acc_add(acc.v[0], d);
+  acc.v[1] = acc_add(acc.v[1], d4);
+  // edge_diff_map: r = (1 + a2) / (1 + a1) - 1 = (a2 - a1) / (1 + a1), with
+  // a = |x - mu|; the numerator and denominator are exact pairs
   const float a2 = fabsf(__fsub_rn(x2, mu2));
   const float a1 = fabsf(__fsub_rn(x1, mu1));
-  const ff ratio = ff_div(two_sum(1.0f, a2), two_sum(1.0f, a1));
-  const ff rr = ff_add(ratio, ff{-1.0f, 0.0f});
-  const ff r2 = ff_mul(rr, rr);
+  const ff r = ff_div(two_sum(a2, -a1), two_sum(1.0f, a1));
+  const ff r2 = ff_mul(r, r);
   const ff r4 = ff_mul(r2, r2);
-  const bool pos = rr.hi > 0.0f, neg = rr.hi < 0.0f;
-  const ff zero = {0.0f, 0.0f};
-  const ff art = pos ? rr : zero;
-  const ff art4 = pos ? r4 : zero;
-  const ff det = neg ? ff{-rr.hi, -rr.lo} : zero;
-  const ff det4 = neg ? r4 : zero;
-  acc.v[2] = ff_add(acc.v[2], art);
-  acc.v[3] = ff_add(acc.v[3], art4);
-  acc.v[4] = ff_add(acc.v[4], det);
-  acc.v[5] = ff_add(acc.v[5], det4);
+  // artifact (r > 0) and detail lost (r < 0) are exclusive: one addition each
+  // into the sum that the sign selects (r = 0 adds zero to detail lost)
+  const bool pos = r.hi > 0.0f;
+  const ff ar = pos ? r : ff{-r.hi, -r.lo};
+  ff s1 = pos ? acc.v[2] : acc.v[4];
+  ff s4 = pos ? acc.v[3] : acc.v[5];
+  s1 = acc_add(s1, ar);
+  s4 = acc_add(s4, r4);
+  if (pos) {
+    acc.v[2] = s1;
+    acc.v[3] = s4;
+  } else {
+    acc.v[4] = s1;
+    acc.v[5] = s4;
+  }
 }
 
 // Column walkers.  One warp per 32 columns of one (frame, scale, channel);
@@ -490,6 +510,7 @@ __global__ void __launch_bounds__(kVWarps * 32)
         ssim_edge_terms(px, o[0], o[1], o[2], o[3], o[4], x1, x2, acc);
       }
     }
+    acc_renorm(acc);
     __syncwarp();
     if (lane == 0) {
       if (k + 3 <= nchunk) issue_h(k + 3);       // into the slot of chunk k - 1
