@@ -80,6 +80,42 @@ def byte_model(spec) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# DRAM traffic from the committed ncu summary of a kernel
+# ---------------------------------------------------------------------------
+
+KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h"]
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "ssimulacra2_image_scoring_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel: str, workload: str, frames_per_launch: float):
+    """dram read+write bytes per launch of `kernel`, scaled from the per-frame
+    figure of its ncu summary; None when there is no summary for this
+    workload or the kernels changed since it was captured."""
+    short = workload.split("_")[0]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{short}_4frames.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines()
+                  if line.startswith(("kernel-source hash:", "traffic_bytes_per_frame:")))
+    if fields.get("kernel-source hash", "").strip() != kernel_source_hash():
+        return None
+    try:
+        return float(fields["traffic_bytes_per_frame"]) * frames_per_launch
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
 
@@ -294,16 +330,7 @@ def run_ours(args, ws, rank, local):
     peak_src = "measured"
     if not peak:
         peak, peak_src = 6800.0, "fallback"
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tfile):
-        try:
-            with open(tfile) as f:
-                tj = json.load(f)
-            if tj.get("kernel") == dom and tj.get("workload") == spec.name:
-                traffic = tj.get("bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
+    traffic = profile_traffic(dom, spec.name, frames_per_launch)
 
     # e2e through the host-input entry point from pinned memory
     pr = torch.from_numpy(wl.ref).pin_memory()
