@@ -65,6 +65,30 @@ SS2_API const char *ss2_last_error_string(void) { return t_msg; }
 // ---------------------------------------------------------------------------
 
 // sRGB decoding (IEC 61966-2-1) in fp64.
+static double srgb_to_linear(double v);
+
+void ss2::build_eotf_pairs(float *P) {
+  float T[kEotfN + 1];
+  build_eotf(T);
+  for (int i = 0; i < kEotfN; ++i) {
+    P[2 * i] = T[i];
+    P[2 * i + 1] = T[i + 1] - T[i];
+  }
+}
+
+int ss2::norm_entries(int depth) { return depth == 8 ? 256 : 65536; }
+
+// (v - 16k) / 219k and (v - 128k) / 224k, k = 2^(depth-8), as float
+// quotients of exactly representable operands (correctly rounded).
+void ss2::build_norm(int depth, float *yn, float *cn) {
+  const int k = 1 << (depth - 8), n = norm_entries(depth);
+  const float dy = (float)(219 * k), dc = (float)(224 * k);
+  for (int v = 0; v < n; ++v) {
+    yn[v] = (float)(v - 16 * k) / dy;
+    cn[v] = (float)(v - 128 * k) / dc;
+  }
+}
+
 static double srgb_to_linear(double v) {
   return v <= 0.04045 ? v / 12.92 : std::pow((v + 0.055) / 1.055, 2.4);
 }
@@ -175,7 +199,8 @@ struct ss2_ctx {
   double params[kNParams];
   Lane lane[kLanes];
   double *d_params = nullptr;
-  float *d_eotf = nullptr;
+  float *d_tabs = nullptr;         // EOTF pairs, then the two normalisation tables
+  PyrTabs tabs;
   int *d_err = nullptr;            // error bits raised by kernels (bounded waits)
   cudaEvent_t ev_fork = nullptr;
   size_t ws_bytes = 0;
@@ -343,7 +368,7 @@ static void free_ctx(ss2_ctx *c) {
     if (L.ev_copied) cudaEventDestroy(L.ev_copied);
     if (L.ev_consumed) cudaEventDestroy(L.ev_consumed);
   }
-  cudaFree(c->d_params); cudaFree(c->d_eotf); cudaFree(c->d_err);
+  cudaFree(c->d_params); cudaFree(c->d_tabs); cudaFree(c->d_err);
   if (c->ev_fork) cudaEventDestroy(c->ev_fork);
   if (c->h_err) cudaFreeHost(c->h_err);
   if (c->h_scores) cudaFreeHost(c->h_scores);
@@ -441,15 +466,22 @@ static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
     return nullptr;
   }
   if (dev_alloc((void **)&c->d_params, kNParams * sizeof(double), &tot) ||
-      dev_alloc((void **)&c->d_eotf, (kEotfN + 1) * sizeof(float), &tot) ||
+      dev_alloc((void **)&c->d_tabs,
+                (2 * kEotfN + 2 * norm_entries(depth)) * sizeof(float), &tot) ||
       dev_alloc((void **)&c->d_err, sizeof(int), &tot)) {
     free_ctx(c);
     return nullptr;
   }
   c->ws_bytes = tot;
-  float T[kEotfN + 1];
-  build_eotf(T);
-  cudaError_t e = cudaMemcpy(c->d_eotf, T, sizeof(T), cudaMemcpyHostToDevice);
+  const int nn = norm_entries(depth);
+  std::vector<float> tab((size_t)2 * kEotfN + 2 * (size_t)nn);
+  build_eotf_pairs(tab.data());
+  build_norm(depth, tab.data() + 2 * kEotfN, tab.data() + 2 * kEotfN + nn);
+  c->tabs.eotf = reinterpret_cast<const float2 *>(c->d_tabs);
+  c->tabs.ynorm = c->d_tabs + 2 * kEotfN;
+  c->tabs.cnorm = c->d_tabs + 2 * kEotfN + nn;
+  cudaError_t e = cudaMemcpy(c->d_tabs, tab.data(), tab.size() * sizeof(float),
+                             cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(c->d_params, c->params, sizeof(c->params), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
@@ -585,7 +617,7 @@ static int run_batch(ss2_ctx *c, Lane &L, const uint8_t *ref, const uint8_t *dis
                      cudaEvent_t after_pyramid) {
   const Geom &g = c->g;
   cudaStream_t st = L.st;
-  TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->d_eotf, ref, dis, L.X, nb, st),
+  TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->tabs, ref, dis, L.X, nb, st),
         "k_pyramid launch");
   if (after_pyramid) CU(cudaEventRecord(after_pyramid, st), "event record");
   TIMED(c, kKHblur, st, launch_hblur(g, c->px, L.maps, c->d_err, nb, st), "k_hblur launch");
@@ -757,7 +789,7 @@ SS2_API int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis, int
   cudaStream_t st = (cudaStream_t)stream;
   const Geom &g = ctx->g;
   Lane &L = ctx->lane[0];
-  CU(launch_pyramid(g, ctx->px, ctx->d_eotf, (const uint8_t *)ref, (const uint8_t *)dis, L.X,
+  CU(launch_pyramid(g, ctx->px, ctx->tabs, (const uint8_t *)ref, (const uint8_t *)dis, L.X,
                     1, st),
      "k_pyramid launch");
   CU(launch_hblur(g, ctx->px, L.maps, ctx->d_err, 1, st), "k_hblur launch");

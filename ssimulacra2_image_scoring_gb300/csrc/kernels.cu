@@ -46,7 +46,7 @@ __device__ __forceinline__ int read_sample(const uint8_t *__restrict__ p, long l
 }
 
 __global__ void __launch_bounds__(kPyrThreads)
-    k_pyramid(Geom g, Pix px, const float *__restrict__ eotf, const uint8_t *__restrict__ ref,
+    k_pyramid(Geom g, Pix px, PyrTabs tabs, const uint8_t *__restrict__ ref,
               const uint8_t *__restrict__ dis, float *__restrict__ X) {
   __shared__ float L[6][kLvlTotal];
   const int frame = blockIdx.z;
@@ -79,15 +79,22 @@ __global__ void __launch_bounds__(kPyrThreads)
         const int Ys = read_sample(f, (long long)y * g.w + x, g.bps);
         const int Us = read_sample(f + ysz * g.bps, ci, g.bps);
         const int Vs = read_sample(f + (ysz + csz) * g.bps, ci, g.bps);
-        const float yn = __fdiv_rn((float)(Ys - 16 * k), dy);
-        const float cbv = __fdiv_rn((float)(Us - 128 * k), dc);
-        const float crv = __fdiv_rn((float)(Vs - 128 * k), dc);
+        float yn, cbv, crv;
+        if (tabs.ynorm) {
+          yn = __ldg(tabs.ynorm + Ys);
+          cbv = __ldg(tabs.cnorm + Us);
+          crv = __ldg(tabs.cnorm + Vs);
+        } else {
+          yn = __fdiv_rn((float)(Ys - 16 * k), dy);
+          cbv = __fdiv_rn((float)(Us - 128 * k), dc);
+          crv = __fdiv_rn((float)(Vs - 128 * k), dc);
+        }
         const float r = __fmaf_rn(px.yuv[0], crv, yn);
         const float gg = __fmaf_rn(-px.yuv[2], crv, __fmaf_rn(-px.yuv[1], cbv, yn));
         const float b = __fmaf_rn(px.yuv[3], cbv, yn);
-        const float R = eotf_lookup(eotf, clamp01(r));
-        const float G = eotf_lookup(eotf, clamp01(gg));
-        const float B = eotf_lookup(eotf, clamp01(b));
+        const float R = eotf_lookup(tabs.eotf, clamp01(r));
+        const float G = eotf_lookup(tabs.eotf, clamp01(gg));
+        const float B = eotf_lookup(tabs.eotf, clamp01(b));
         L[3 * img + 0][p] = R;
         L[3 * img + 1][p] = G;
         L[3 * img + 2][p] = B;
@@ -613,10 +620,10 @@ cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st) 
   return cudaGetLastError();
 }
 
-cudaError_t launch_pyramid(const Geom &g, const Pix &px, const float *eotf, const uint8_t *ref,
+cudaError_t launch_pyramid(const Geom &g, const Pix &px, const PyrTabs &tabs, const uint8_t *ref,
                            const uint8_t *dis, float *X, int nframes, cudaStream_t st) {
   dim3 grid((g.w + kTile - 1) / kTile, (g.h + kTile - 1) / kTile, nframes);
-  k_pyramid<<<grid, kPyrThreads, 0, st>>>(g, px, eotf, ref, dis, X);
+  k_pyramid<<<grid, kPyrThreads, 0, st>>>(g, px, tabs, ref, dis, X);
   return cudaGetLastError();
 }
 

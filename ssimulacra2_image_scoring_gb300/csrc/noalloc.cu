@@ -50,7 +50,7 @@ constexpr size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign;
 
 // head of the array: constant tables written once at set-up
 constexpr size_t kEotfOff = 0;
-constexpr size_t kParamsOff = align_up(kEotfOff + sizeof(float) * (ss2::kEotfN + 1));
+constexpr size_t kParamsOff = align_up(kEotfOff + sizeof(float) * 2 * ss2::kEotfN);
 constexpr size_t kErrOff = align_up(kParamsOff + sizeof(double) * ss2::kNParams);
 constexpr size_t kHeadBytes = align_up(kErrOff + sizeof(int));
 
@@ -74,9 +74,9 @@ static int scratch_for_device(int dev, unsigned char **out) {
     void *p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-    float table[kEotfN + 1];
+    float table[2 * kEotfN];
     double params[kNParams];
-    build_eotf(table);
+    build_eotf_pairs(table);
     default_params(params);
     unsigned char *base = static_cast<unsigned char *>(p);
     e = cudaMemcpy(base + kEotfOff, table, sizeof(table), cudaMemcpyHostToDevice);
@@ -123,7 +123,10 @@ SS2_API int ss2_score_frames_noalloc(int width, int height, int bitdepth, int ch
   float *H = reinterpret_cast<float *>(work + nb_max * x_bytes);
   float2 *part = reinterpret_cast<float2 *>(work + nb_max * (x_bytes + h_bytes));
   double *values = reinterpret_cast<double *>(work + nb_max * (x_bytes + h_bytes + p_bytes));
-  const float *eotf = reinterpret_cast<const float *>(base + kEotfOff);
+  PyrTabs tabs;
+  tabs.eotf = reinterpret_cast<const float2 *>(base + kEotfOff);
+  tabs.ynorm = nullptr;   // normalisation by division on the device
+  tabs.cnorm = nullptr;
   const double *params = reinterpret_cast<const double *>(base + kParamsOff);
   // the kernels index frames by g.x_fs / g.h_fs / g.p_fs; use the padded strides
   g.x_fs = (long long)(x_bytes / sizeof(float));
@@ -142,7 +145,7 @@ SS2_API int ss2_score_frames_noalloc(int width, int height, int bitdepth, int ch
   for (int f0 = 0; f0 < n_frames; f0 += nb_max) {
     const int nb = std::min(nb_max, n_frames - f0);
     const long long off = (long long)f0 * g.frame_bytes;
-    cudaError_t e = launch_pyramid(g, px, eotf, r8 + off, d8 + off, X, nb, st);
+    cudaError_t e = launch_pyramid(g, px, tabs, r8 + off, d8 + off, X, nb, st);
     if (e == cudaSuccess) e = launch_hblur(g, px, maps, err, nb, st);
     if (e == cudaSuccess) e = launch_vblur(g, px, maps, part, err, nb, st);
     if (e == cudaSuccess) e = launch_finalize(g, part, params, values, scores + f0, nb, st);

@@ -160,32 +160,45 @@ __device__ __noinline__ float cbrt_round_exact(float x, float y) {
   return y;
 }
 
-// Correctly rounded cbrt for x >= 0 finite.  y = cbrtf(x) is within an ulp.
-// The residual R = x - y^3 is formed to about 2^-43 x with error-free
-// products (y^2 = p + e exactly, y p = q1 + q2 exactly, x - q1 exact by
-// Sterbenz), and the root's offset from y is R / (3 y^2) to first order, so
-// |R| against T = 1.5 y^2 u (half an ulp u of y, in residual units) decides
-// the rounding.  Within 2^-16 of the boundary, at a power of two (where the
-// spacing below halves) and below x = 2^-100 (where the error terms of the
-// products would underflow), the exact integer test decides.
+__device__ __forceinline__ float lg2_approx(float x) {
+  float r;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Correctly rounded cbrt for x >= 0 finite.
+//   1. y0 = 2^(log2(x) / 3) from the hardware approximations (a few ulps).
+//   2. The residual R = x - y0^3 to about 2^-43 x: y0^2 = p + e and
+//      y0 p = q + f exactly (fma), x - q exact by Sterbenz.
+//   3. One Newton step y0 + R / (3 y0^2), whose error is about 2^-41 y0,
+//      with the rounding error of the final addition kept exactly
+//      (two_sum): the root lies at that error (plus 2^-41 y0) from the
+//      float y, so y is the nearest float unless the error is within
+//      2^-14 ulp of half an ulp.
+//   4. Those near-ties, powers of two (where the spacing below halves) and
+//      x < 2^-100 (where the products' error terms underflow) take the exact
+//      128-bit integer decision.
 __device__ __forceinline__ float cbrt_cr(float x) {
   if (x == 0.0f) return 0.0f;
-  const float y = cbrtf(x);
-  const uint32_t yb = __float_as_uint(y);
-  if ((yb & 0x7fffffu) == 0u || __float_as_uint(x) < 0x0d800000u) return cbrt_round_exact(x, y);
-  const ff y2 = two_prod(y, y);
-  const ff y3 = two_prod(y, y2.hi);
-  const float y3c = __fmul_rn(y, y2.lo);
-  float r = __fsub_rn(x, y3.hi);
-  r = __fsub_rn(r, y3.lo);
-  r = __fsub_rn(r, y3c);
-  const float u = __uint_as_float((yb & 0x7f800000u) - (23u << 23));  // ulp(y)
-  const float T = __fmul_rn(__fmul_rn(1.5f, y2.hi), u);
-  const float ar = fabsf(r);
-  if (ar < __fmul_rn(T, 0.9999847412109375f)) return y;             // |offset| < u/2
-  if (ar > __fmul_rn(T, 1.0000152587890625f) && ar < __fmul_rn(T, 2.9f))
-    return __uint_as_float(r > 0.0f ? yb + 1u : yb - 1u);           // u/2 < |offset| < 1.45u
-  return cbrt_round_exact(x, y);
+  if (__float_as_uint(x) < 0x0d800000u) return cbrt_round_exact(x, cbrtf(x));
+  const float y0 = ex2_approx(__fmul_rn(lg2_approx(x), 0.333333343f));
+  const ff p = two_prod(y0, y0);
+  const ff q = two_prod(y0, p.hi);
+  float r = __fsub_rn(x, q.hi);
+  r = __fsub_rn(r, q.lo);
+  r = __fsub_rn(r, __fmul_rn(y0, p.lo));
+  const float d = __fmul_rn(r, rcp_approx(__fmul_rn(3.0f, p.hi)));
+  const ff y = two_sum(y0, d);
+  const uint32_t yb = __float_as_uint(y.hi);
+  const float half_u = __uint_as_float((yb & 0x7f800000u) - (24u << 23));
+  if ((yb & 0x7fffffu) != 0u && fabsf(y.lo) < __fmul_rn(half_u, 0.99993896484375f)) return y.hi;
+  return cbrt_round_exact(x, y.hi);
 }
 
 // ---------------------------------------------------------------------------
@@ -198,14 +211,15 @@ __device__ __forceinline__ float clamp01(float v) {
   return v;
 }
 
-// Linear interpolation in the sRGB EOTF table (uniform grid, 4096 intervals).
-__device__ __forceinline__ float eotf_lookup(const float *__restrict__ T, float v) {
+// Linear interpolation in the sRGB EOTF table (uniform grid, 4096 intervals),
+// stored as (T[i], T[i+1] - T[i]) pairs.
+__device__ __forceinline__ float eotf_lookup(const float2 *__restrict__ P, float v) {
   float t = __fmul_rn(v, (float)kEotfN);
   int i = (int)t;
   i = i > kEotfN - 1 ? kEotfN - 1 : i;
   float f = __fsub_rn(t, (float)i);
-  float t0 = __ldg(T + i), t1 = __ldg(T + i + 1);
-  return __fmaf_rn(f, __fsub_rn(t1, t0), t0);
+  const float2 e = __ldg(P + i);
+  return __fmaf_rn(f, e.y, e.x);
 }
 
 // Linear RGB -> XYB with the make-positive affine.

@@ -59,6 +59,17 @@ struct PlaneMaps {
 constexpr int kBoxCols = 8, kBoxRows = 32;      // horizontal pass box
 constexpr int kVCols = 32, kVRows = 8;          // vertical pass box
 
+// Tables the pyramid kernel reads.  eotf: 4096 (value, slope) pairs of the
+// sRGB EOTF table, slope = T[i+1] - T[i] rounded to float.  ynorm / cnorm:
+// the limited-range normalisations (v - 16k) / 219k and (v - 128k) / 224k of
+// every sample value v (256 entries at 8 bits, 65536 above), each a
+// correctly rounded float quotient; null means divide on the device.
+struct PyrTabs {
+  const float2 *eotf;
+  const float *ynorm;
+  const float *cnorm;
+};
+
 // Per-pixel constants (fp32 pipeline), rounded from the parameter vector.
 struct Pix {
   float yuv[4];        // cr->R', cb->G' (magnitude), cr->G' (magnitude), cb->B'

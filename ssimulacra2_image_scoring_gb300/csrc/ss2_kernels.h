@@ -9,7 +9,7 @@
 
 namespace ss2 {
 
-cudaError_t launch_pyramid(const Geom &g, const Pix &px, const float *eotf, const uint8_t *ref,
+cudaError_t launch_pyramid(const Geom &g, const Pix &px, const PyrTabs &tabs, const uint8_t *ref,
                            const uint8_t *dis, float *X, int nframes, cudaStream_t st);
 cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, int *err,
                          int nframes, cudaStream_t st);
