@@ -621,7 +621,7 @@ static int run_batch(ss2_ctx *c, Lane &L, const uint8_t *ref, const uint8_t *dis
         "k_pyramid launch");
   if (after_pyramid) CU(cudaEventRecord(after_pyramid, st), "event record");
   TIMED(c, kKHblur, st, launch_hblur(g, c->px, L.maps, c->d_err, nb, st), "k_hblur launch");
-  TIMED(c, kKVblur, st, launch_vblur(g, c->px, L.maps, L.part, c->d_err, nb, st),
+  TIMED(c, kKVblur, st, launch_vblur(g, c->px, L.maps, L.X, L.part, c->d_err, nb, st),
         "k_vblur launch");
   TIMED(c, kKFinalize, st,
         launch_finalize(g, L.part, c->d_params, L.values, L.scores, nb, st),

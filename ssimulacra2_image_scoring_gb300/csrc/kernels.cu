@@ -405,25 +405,27 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
 
 // Column walkers.  One warp per 32 columns of one (frame, scale, channel);
 // lane = column.  TMA brings 8-row chunks of the channel's five blurred
-// planes (one 32 x 8 x 5 box) into a 4-slot ring, up to two chunks ahead,
-// and 8-row chunks of the two XYB planes into a 2-slot ring.  Step n of the
-// recursion takes rows n+4 and n-6 of the blurred planes (taps at +-(R+1));
-// its outputs mu1, mu2, s11, s22, s12 feed the SSIM and edge terms of row n
-// at once, so the vertically blurred planes never exist in memory.
+// planes (one 32 x 8 x 5 box) into a 3-slot ring; the slot of chunk k - 1 is
+// refilled with chunk k + 2 as soon as its last row has been read (after
+// step 5 of chunk k), six steps before that chunk is first needed.  The two
+// XYB rows each step needs are loaded from global memory one chunk ahead
+// into registers.  Step n of the recursion takes rows n+4 and n-6 of the
+// blurred planes (taps at +-(R+1)); its outputs mu1, mu2, s11, s22, s12
+// feed the SSIM and edge terms of row n at once, so the vertically blurred
+// planes never exist in memory.
 constexpr int kVWarps = 4;
-constexpr int kVSlots = 4;
+constexpr int kVSlots = 3;
 constexpr int kVBox = kVRows * kVCols;          // floats per plane box (1 KB)
 
 struct VWarpSmem {
   float h[kVSlots][kNq][kVBox];   // [slot][quantity][row * 32 + col]
-  float x[2][2][kVBox];           // [slot][x1 | x2][row * 32 + col]
 };
-static_assert(sizeof(VWarpSmem) == 24576, "per-warp tile");
-constexpr int kVSmemBytes = kVWarps * (int)sizeof(VWarpSmem) + kVWarps * 8 * 8 + 1024;
+static_assert(sizeof(VWarpSmem) == 15360, "per-warp tile");
+constexpr int kVSmemBytes = kVWarps * (int)sizeof(VWarpSmem) + kVWarps * 4 * 8 + 1024;
 
 __global__ void __launch_bounds__(kVWarps * 32)
-    k_vblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, float2 *__restrict__ part,
-            int *__restrict__ err) {
+    k_vblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, const float *__restrict__ X,
+            float2 *__restrict__ part, int *__restrict__ err) {
   extern __shared__ __align__(16) unsigned char vsm_raw[];
   unsigned char *vsm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(vsm_raw) + 1023) & ~uintptr_t(1023));
@@ -440,43 +442,38 @@ __global__ void __launch_bounds__(kVWarps * 32)
   const int h = g.hs[s];
   const int nchunk = (h + kVRows - 1) / kVRows;
   VWarpSmem &sm = reinterpret_cast<VWarpSmem *>(vsm)[warp];
-  uint64_t *hbar = reinterpret_cast<uint64_t *>(vsm + kVWarps * sizeof(VWarpSmem)) + warp * 8;
-  uint64_t *xbar = hbar + kVSlots;
+  uint64_t *hbar = reinterpret_cast<uint64_t *>(vsm + kVWarps * sizeof(VWarpSmem)) + warp * 4;
   const CUtensorMap *mh = &maps.hv[s];
-  const CUtensorMap *mx = &maps.xv[s];
+  // XYB rows of this lane's column (pitch padding keeps every lane in bounds)
+  const long long pitch = g.pitch[s];
+  const float *x1p = X + (long long)frame * g.x_fs + g.xoff[s] + c * g.plane[s] + col0 + lane;
+  const float *x2p = x1p + 3 * g.plane[s];
 
   if (lane == 0) {
     for (int i = 0; i < kVSlots; ++i) mbar_init(&hbar[i], 1);
-    for (int i = 0; i < 2; ++i) mbar_init(&xbar[i], 1);
     fence_barrier_init();
   }
   __syncwarp();
-  // blurred-plane chunk m (rows 8m .. 8m+7), m >= -1, lives in slot m % 4
+  // blurred-plane chunk m (rows 8m .. 8m+7), m >= -1, lives in slot (m+1) % 3
+  auto slot_of = [](int m) { return (m + 1) % kVSlots; };
   auto issue_h = [&](int m) {
-    const int slot = m & (kVSlots - 1);
+    const int slot = slot_of(m);
     mbar_arrive_expect_tx(&hbar[slot], kNq * kVBox * (int)sizeof(float));
     tma_load_4d(sm.h[slot][0], mh, &hbar[slot], col0, m * kVRows, c * kNq, frame);
   };
-  auto issue_x = [&](int m) {
-    const int slot = m & 1;
-    mbar_arrive_expect_tx(&xbar[slot], 2 * kVBox * (int)sizeof(float));
-    tma_load_4d(sm.x[slot][0], mx, &xbar[slot], col0, m * kVRows, c, frame);
-    tma_load_4d(sm.x[slot][1], mx, &xbar[slot], col0, m * kVRows, 3 + c, frame);
-  };
-  if (lane == 0) {
-    for (int m = -1; m <= 2 && m <= nchunk; ++m) issue_h(m);
-    for (int m = 0; m <= 1 && m < nchunk; ++m) issue_x(m);
-  }
+  if (lane == 0)
+    for (int m = -1; m <= 1 && m <= nchunk; ++m) issue_h(m);
   auto wait_h = [&](int m) -> bool {
-    const bool ok = mbar_wait(&hbar[m & (kVSlots - 1)], (uint32_t)((m + 1) >> 2) & 1u);
+    const bool ok = mbar_wait(&hbar[slot_of(m)], (uint32_t)((m + 1) / kVSlots) & 1u);
     return __all_sync(0xffffffffu, ok);
   };
-  auto wait_x = [&](int m) -> bool {
-    const bool ok = mbar_wait(&xbar[m & 1], (uint32_t)(m >> 1) & 1u);
-    return __all_sync(0xffffffffu, ok);
-  };
-  auto bail = [&]() {
-    if (lane == 0) atomicOr(err, kErrTmaTimeout);
+  auto load_x = [&](int m, float (&xa)[kVRows], float (&xb)[kVRows]) {
+#pragma unroll
+    for (int j = 0; j < kVRows; ++j) {
+      const int row = m * kVRows + j;
+      xa[j] = row < h ? __ldg(x1p + row * pitch) : 0.0f;
+      xb[j] = row < h ? __ldg(x2p + row * pitch) : 0.0f;
+    }
   };
 
   Acc6 acc;
@@ -485,20 +482,29 @@ __global__ void __launch_bounds__(kVWarps * 32)
   Res3 r[kNq];
 #pragma unroll
   for (int q = 0; q < kNq; ++q) res_zero(r[q]);
+  float xc1[kVRows], xc2[kVRows];
+  load_x(0, xc1, xc2);
 
-  if (!wait_h(-1) || !wait_h(0)) { bail(); return; }
+  if (!wait_h(-1) || !wait_h(0)) {
+    if (lane == 0) atomicOr(err, kErrTmaTimeout);
+    return;
+  }
   // warm-up steps producing Y[-4] .. Y[-1]: rows 0..3 ahead, zeros behind
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
 #pragma unroll
     for (int q = 0; q < kNq; ++q)
-      res_step(r[q], px, __fadd_rn(sm.h[0][q][j * kVCols + lane], 0.0f));
+      res_step(r[q], px, __fadd_rn(sm.h[slot_of(0)][q][j * kVCols + lane], 0.0f));
   }
 
   for (int k = 0; k < nchunk; ++k) {
-    if (!wait_h(k + 1) || !wait_x(k)) { bail(); return; }
-    const int sp = (k - 1) & (kVSlots - 1), sk = k & (kVSlots - 1), sn = (k + 1) & (kVSlots - 1);
-    const int xs = k & 1;
+    if (!wait_h(k + 1)) {
+      if (lane == 0) atomicOr(err, kErrTmaTimeout);
+      return;
+    }
+    float xn1[kVRows], xn2[kVRows];
+    load_x(k + 1, xn1, xn2);
+    const int sp = slot_of(k - 1), sk = slot_of(k), sn = slot_of(k + 1);
 #pragma unroll
     for (int j = 0; j < kVRows; ++j) {
       // ahead row 8k + j + 4, behind row 8k + j - 6
@@ -510,18 +516,19 @@ __global__ void __launch_bounds__(kVWarps * 32)
 #pragma unroll
       for (int q = 0; q < kNq; ++q)
         o[q] = res_step(r[q], px, __fadd_rn(ha[q * kVBox], hb[q * kVBox]));
-      const int row = k * kVRows + j;
-      if (active && row < h) {
-        const float x1 = sm.x[xs][0][j * kVCols + lane];
-        const float x2 = sm.x[xs][1][j * kVCols + lane];
-        ssim_edge_terms(px, o[0], o[1], o[2], o[3], o[4], x1, x2, acc);
+      if (j == 5) {
+        // chunk k - 1 is read for the last time: refill its slot with k + 2
+        __syncwarp();
+        if (lane == 0 && k + 2 <= nchunk) issue_h(k + 2);
       }
+      if (active && k * kVRows + j < h)
+        ssim_edge_terms(px, o[0], o[1], o[2], o[3], o[4], xc1[j], xc2[j], acc);
     }
     acc_renorm(acc);
-    __syncwarp();
-    if (lane == 0) {
-      if (k + 3 <= nchunk) issue_h(k + 3);       // into the slot of chunk k - 1
-      if (k + 2 < nchunk) issue_x(k + 2);        // into the slot of chunk k
+#pragma unroll
+    for (int j = 0; j < kVRows; ++j) {
+      xc1[j] = xn1[j];
+      xc2[j] = xn2[j];
     }
   }
   // fixed tree: lane l adds lane l + 2^m for m = 4..0
@@ -644,8 +651,8 @@ cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, float2 *part,
-                         int *err, int nframes, cudaStream_t st) {
+cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, const float *X,
+                         float2 *part, int *err, int nframes, cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -657,7 +664,7 @@ cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, fl
   }
   const int warps = g.vwarp_off[g.nscales];
   dim3 grid((warps + kVWarps - 1) / kVWarps, nframes);
-  k_vblur<<<grid, kVWarps * 32, kVSmemBytes, st>>>(g, px, maps, part, err);
+  k_vblur<<<grid, kVWarps * 32, kVSmemBytes, st>>>(g, px, maps, X, part, err);
   return cudaGetLastError();
 }
 

@@ -147,7 +147,7 @@ SS2_API int ss2_score_frames_noalloc(int width, int height, int bitdepth, int ch
     const long long off = (long long)f0 * g.frame_bytes;
     cudaError_t e = launch_pyramid(g, px, tabs, r8 + off, d8 + off, X, nb, st);
     if (e == cudaSuccess) e = launch_hblur(g, px, maps, err, nb, st);
-    if (e == cudaSuccess) e = launch_vblur(g, px, maps, part, err, nb, st);
+    if (e == cudaSuccess) e = launch_vblur(g, px, maps, X, part, err, nb, st);
     if (e == cudaSuccess) e = launch_finalize(g, part, params, values, scores + f0, nb, st);
     if (e != cudaSuccess) return cuda_fail(e, "allocation-free scoring launch");
   }

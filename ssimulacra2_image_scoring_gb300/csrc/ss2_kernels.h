@@ -13,8 +13,8 @@ cudaError_t launch_pyramid(const Geom &g, const Pix &px, const PyrTabs &tabs, co
                            const uint8_t *dis, float *X, int nframes, cudaStream_t st);
 cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, int *err,
                          int nframes, cudaStream_t st);
-cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, float2 *part,
-                         int *err, int nframes, cudaStream_t st);
+cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, const float *X,
+                         float2 *part, int *err, int nframes, cudaStream_t st);
 cudaError_t launch_finalize(const Geom &g, const float2 *part, const double *params,
                             double *values, double *scores, int nframes, cudaStream_t st);
 
