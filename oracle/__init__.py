@@ -33,6 +33,10 @@ CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
 _lock = threading.Lock()
 _lib = None
 
+# Tests that plant a mistake in a copy of the oracle point this at the copy's
+# build; nothing else sets it.
+SO_OVERRIDE_ENV = "SS2_ORACLE_SO"
+
 
 def _stale() -> bool:
     if not os.path.exists(SO_PATH):
@@ -68,8 +72,10 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(SO_PATH)
+            path = os.environ.get(SO_OVERRIDE_ENV)
+            if not path:
+                path = build()
+            L = ctypes.CDLL(path)
             vp, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
             L.ss2o_default_params.argtypes = [vp]
             L.ss2o_score.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, ctypes.POINTER(Dump)]
@@ -88,6 +94,7 @@ def lib() -> ctypes.CDLL:
             L.ss2o_eotf_lookup.restype = ctypes.c_float
             L.ss2o_yuv_coeffs.argtypes = [vp]
             L.ss2o_iir_coeffs.argtypes = [vp, vp, vp]
+            L.ss2o_xyb_pixel.argtypes = [vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, vp]
             L.ss2o_blur_line.argtypes = [vp, i, vp]
             L.ss2o_downsample.argtypes = [vp, i, i, vp]
             _lib = L
@@ -208,6 +215,14 @@ def yuv_coeffs() -> np.ndarray:
     k = np.zeros(4, np.float32)
     lib().ss2o_yuv_coeffs(_ptr(k))
     return k
+
+
+def xyb_pixel(r: float, g: float, b: float, params: np.ndarray | None = None) -> np.ndarray:
+    params = default_params() if params is None else np.ascontiguousarray(params, np.float64)
+    out = np.zeros(3, np.float32)
+    lib().ss2o_xyb_pixel(_ptr(params), ctypes.c_float(r), ctypes.c_float(g), ctypes.c_float(b),
+                         _ptr(out))
+    return out
 
 
 def iir_coeffs():

@@ -350,6 +350,13 @@ static void pixel_xyb(const pix_params *pp, float r, float g, float b,
     *B = bs + pp->ob;
 }
 
+void ss2o_xyb_pixel(const double *params, float r, float g, float b, float *xyb)
+{
+    pix_params pp;
+    load_pix_params(params, &pp);
+    pixel_xyb(&pp, r, g, b, &xyb[0], &xyb[1], &xyb[2]);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Recursive Gaussian                                                        */
 /* ------------------------------------------------------------------------ */

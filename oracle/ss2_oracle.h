@@ -86,6 +86,8 @@ void ss2o_cbrtf_cr_array(const float *x, float *y, long long n);
 void ss2o_eotf_table(float *table);            /* SS2O_EOTF_N + 1 floats */
 float ss2o_eotf_lookup(const float *table, float v);
 void ss2o_yuv_coeffs(float *coeffs);           /* cr_r, cb_g, cr_g, cb_b */
+void ss2o_xyb_pixel(const double *params, float r, float g, float b,
+                    float *xyb);                /* linear RGB -> X, Y, B */
 void ss2o_iir_coeffs(double *a, float *c2, float *g); /* 3 each */
 void ss2o_blur_line(const float *in, int n, float *out);
 void ss2o_downsample(const float *in, int w, int h, float *out);

@@ -1,0 +1,69 @@
+"""Planted mistakes in the oracle must fail its pins (CPU).
+
+Each case copies oracle/ss2_oracle.c, plants one plausible slip (a dropped
+term, a wrong sign, index or operand, a missed clamp), builds the copy with
+the oracle's own flags and runs tests/test_oracle_pins.py against it in a
+child process.  A pin suite that still passes would not have caught that
+mistake in the real oracle.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "iir_drops_trailing_tap": ("float s = xa + xb;", "float s = xa;"),
+    "iir_recursion_sign": ("float u = fmaf(c->g[k], s, -prev[k]);",
+                           "float u = fmaf(c->g[k], s, prev[k]);"),
+    "iir_drops_a_harmonic": ("out[(ptrdiff_t)(i + 1) * ostride] = t + cur[2];",
+                             "out[(ptrdiff_t)(i + 1) * ostride] = t;"),
+    "iir_fit_wrong_sigma": ("const double sigma = 1.5, pi", "const double sigma = 1.4, pi"),
+    "edge_ratio_inverted": ("return num / den - 1.0;", "return den / num - 1.0;"),
+    "ssim_den_without_c2": ("float den_s = vs + c2;", "float den_s = vs;"),
+    "ssim_cov_sign": ("float cov = s12 - m12;", "float cov = s12 + m12;"),
+    "fourth_power_is_square": ("double t[NSUM] = {d, pow4(d), art, pow4(art), det, pow4(det)};",
+                               "double t[NSUM] = {d, d * d, art, pow4(art), det, pow4(det)};"),
+    "chroma_column_uses_row_shift": ("(size_t)(y >> sy) * cw + (size_t)(x >> sx);",
+                                     "(size_t)(y >> sy) * cw + (size_t)(x >> sy);"),
+    "downsample_wrong_clamp": ("int x0 = 2 * x, x1 = 2 * x + 1 < w ? 2 * x + 1 : w - 1;",
+                               "int x0 = 2 * x, x1 = 2 * x + 1 < w ? 2 * x + 1 : w - 2;"),
+    "xyb_x_uses_s_cone": ("float x = 0.5f * (c[0] - c[1]);", "float x = 0.5f * (c[0] - c[2]);"),
+    "eotf_no_interpolation": ("return fmaf(f, slope, T[i]);", "return T[i];"),
+    "chroma_offset_16": ("float cb = (float)(Us - 128 * k) / dc;",
+                         "float cb = (float)(Us - 16 * k) / dc;"),
+    "matrix_red_from_cb": ("float r = fmaf(c[0], cr, yn);", "float r = fmaf(c[0], cb, yn);"),
+    "cbrt_not_correctly_rounded": ("float y = (float)cbrt((double)x);",
+                                   "return cbrtf(x);\n    float y = (float)cbrt((double)x);"),
+    "avg4_square_root_once": ("double avg4 = sqrt(sqrt(sum[2 * kind + 1] / (double)ns));",
+                              "double avg4 = sqrt(sum[2 * kind + 1] / (double)ns);"),
+    "pool_weight_misindexed": ("double t = params[SS2O_P_WEIGHTS + i] * fabs(values[i]);",
+                               "double t = params[SS2O_P_WEIGHTS + (i + 1) % 108] * fabs(values[i]);"),
+    "scale_stop_at_9": ("while (n < SS2O_NSCALES && w >= 8 && h >= 8) {",
+                        "while (n < SS2O_NSCALES && w >= 9 && h >= 9) {"),
+    "norm_limited_range_219_as_220": ("const float dy = (float)(219 * k), dc = (float)(224 * k);",
+                                      "const float dy = (float)(220 * k), dc = (float)(224 * k);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_fails_the_pins(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(os.path.join(oracle.HERE, "ss2_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation site not found exactly once: {old!r}"
+    (tmp_path / "ss2_oracle.c").write_text(src.replace(old, new))
+    (tmp_path / "ss2_oracle.h").write_text(open(os.path.join(oracle.HERE, "ss2_oracle.h")).read())
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-shared", "-o", str(so),
+                    str(tmp_path / "ss2_oracle.c"), "-lm"], check=True)
+    env = dict(os.environ, **{oracle.SO_OVERRIDE_ENV: str(so)})
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"the pins did not catch '{name}':\n{r.stdout[-2000:]}"

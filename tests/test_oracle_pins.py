@@ -127,6 +127,51 @@ def test_neutral_gray_maps_to_x_zero(depth):
     assert np.all(np.diff(yv[order]) >= 0)
 
 
+def test_xyb_channels_on_the_primaries():
+    """The opsin rows L and M share their blue weight, so pure blue has X = 0;
+    red drives L above M (X > 0), green drives M above L (X < 0); black is
+    the origin; Y grows with every primary; B - Y is largest for blue."""
+    z = oracle.xyb_pixel(0.0, 0.0, 0.0)
+    assert np.array_equal(z, np.zeros(3, np.float32))
+    r = oracle.xyb_pixel(1.0, 0.0, 0.0)
+    g = oracle.xyb_pixel(0.0, 1.0, 0.0)
+    b = oracle.xyb_pixel(0.0, 0.0, 1.0)
+    assert b[0] == 0.0 and r[0] > 1e-3 and g[0] < -1e-3
+    assert r[1] > 0 and g[1] > 0 and b[1] > 0
+    assert b[2] > r[2] and b[2] > g[2] and b[2] > 0
+    w = oracle.xyb_pixel(1.0, 1.0, 1.0)
+    assert abs(w[0]) <= 1e-7 and abs(w[2]) <= 1e-6
+
+
+def test_bt709_round_trip_of_coloured_pixels():
+    """Encode R'G'B' with the forward BT.709 transform (Kr = 0.2126,
+    Kb = 0.0722) at 10 bits; the oracle's decoding must return the colour
+    (through the EOTF) within the quantisation error."""
+    kr, kb = 0.2126, 0.0722
+    kg = 1 - kr - kb
+    cols = [(0.8, 0.3, 0.5), (0.1, 0.9, 0.2), (0.6, 0.2, 0.95), (0.5, 0.5, 0.1)]
+    w, h = 8, 8
+    ys, us, vs = [], [], []
+    for (R, G, B) in cols:
+        Yp = kr * R + kg * G + kb * B
+        cb = (B - Yp) / (2 * (1 - kb))
+        cr = (R - Yp) / (2 * (1 - kr))
+        ys.append(round(64 + 876 * Yp))
+        us.append(round(512 + 896 * cb))
+        vs.append(round(512 + 896 * cr))
+    Y = np.repeat(np.array(ys, np.uint16), 16).reshape(h, w)
+    U = np.repeat(np.array(us, np.uint16), 16).reshape(h, w)
+    V = np.repeat(np.array(vs, np.uint16), 16).reshape(h, w)
+    f = _frame(Y, U, V)
+    _, _, d = oracle.score(f, f, w, h, 10, 444, dump_scale=0)
+    lin = d["lin"][:3].reshape(3, -1)
+    eotf = lambda v: v / 12.92 if v <= 0.04045 else ((v + 0.055) / 1.055) ** 2.4  # noqa: E731
+    for i, (R, G, B) in enumerate(cols):
+        got = lin[:, 16 * i]
+        want = np.array([eotf(R), eotf(G), eotf(B)])
+        assert np.abs(got - want).max() <= 4e-3, (i, got, want)
+
+
 # ---------------------------------------------------------------------------
 # 4. 8x8 sums vs exact sums
 # ---------------------------------------------------------------------------
@@ -157,6 +202,48 @@ def test_8x8_sums_equal_exact_sums():
         art, det = terms[c * 6 + 2], terms[c * 6 + 4]
         assert np.all((art == 0) | (det == 0))
     assert np.any(terms[[2, 8, 14]] > 0) and np.any(terms[[4, 10, 16]] > 0)
+
+
+def _flat(w, h, Y, U, V):
+    cw, ch = synth.chroma_dims(w, h, 444)
+    return _const_frame(w, h, 8, 444, Y, U, V)
+
+
+def test_ssim_term_on_flat_frames_is_the_squared_mean_difference():
+    """Two flat frames: away from the borders every window sees one value,
+    so both variances and the covariance vanish, num_s = den_s = C2 and the
+    SSIM term is 1 - (1 - (x1 - x2)^2) = (x1 - x2)^2 per channel."""
+    w = h = 40
+    a = _flat(w, h, 60, 100, 170)
+    b = _flat(w, h, 180, 150, 90)
+    _, _, d = oracle.score(a, b, w, h, 8, 444, dump_scale=0)
+    xyb, terms = d["xyb"].astype(np.float64), d["terms"]
+    inner = (slice(6, h - 6), slice(6, w - 6))
+    for c in range(3):
+        x1, x2 = xyb[c][inner].mean(), xyb[3 + c][inner].mean()
+        want = (x1 - x2) ** 2
+        got = terms[c * 6 + 0][inner]
+        # fp32 rounding of the recursions leaves variances of ~1e-7 against
+        # C2 = 9e-4, so the term carries ~1e-3 relative noise
+        assert np.abs(got - want).max() <= 2e-5 + 2e-2 * want, (c, got.max(), want)
+    assert (xyb[1][inner].mean() - xyb[4][inner].mean()) ** 2 > 1e-3
+
+
+def test_edge_terms_tell_lost_detail_from_artifacts():
+    """A flat distorted frame against a textured reference loses detail
+    (det >> art); a textured distorted frame against a flat reference has
+    artifacts (art >> det)."""
+    w, h = 48, 40
+    tex = synth.custom(w, h, 8, 444, 1, seed=21, noise=0.0).ref[0]
+    flat = _flat(w, h, 128, 128, 128)
+    _, v1, _ = oracle.score(tex, flat, w, h, 8, 444)
+    _, v2, _ = oracle.score(flat, tex, w, h, 8, 444)
+    v1, v2 = v1.reshape(3, 6, 2, 3), v2.reshape(3, 6, 2, 3)
+    # scale 0, 1-norm: kind 1 = artifact, 2 = detail lost; the flat frame's
+    # borders (zero-extended blur) leave some of the other kind in Y
+    for c in range(3):
+        assert v1[c, 0, 0, 2] > 5 * v1[c, 0, 0, 1], c
+        assert v2[c, 0, 0, 1] > 5 * v2[c, 0, 0, 2], c
 
 
 # ---------------------------------------------------------------------------
