@@ -153,6 +153,16 @@ int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream);
 int ss2_profile_begin(ss2_ctx *ctx);
 int ss2_profile_end(ss2_ctx *ctx, double *ms, int *launches);
 
+/*
+ * ss2_debug_wait_probe — runs a one-warp kernel whose shared-memory barrier
+ * phase is never completed and lets its bounded wait give up after `spins`
+ * polls (the same bounded wait the TMA kernels use).  Returns -EIO when the
+ * kernel reported the timeout (the expected outcome), 0 if the wait
+ * completed, another negative code on a CUDA error.  Synchronises stream.
+ * The device stays usable afterwards.
+ */
+int ss2_debug_wait_probe(unsigned spins, void *stream);
+
 /* ss2_frame_bytes — bytes of one packed frame of the context's geometry. */
 size_t ss2_frame_bytes(const ss2_ctx *ctx);
 

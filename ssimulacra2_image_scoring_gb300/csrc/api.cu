@@ -25,6 +25,7 @@
 #include "ss2_host.h"
 #include "ss2_impl.h"
 #include "ss2_kernels.h"
+#include "ss2_tma.cuh"
 
 #define SS2_API extern "C" __attribute__((visibility("default")))
 
@@ -393,7 +394,27 @@ int ss2::check_device(int *dev) {
   return 0;
 }
 
+// Host-side fault injection for the failure-path tests: SS2_FAULT holds a
+// comma-separated list of "alloc", "launch", "memcpy"; the named step then
+// fails before it touches the device.
+static bool injected(const char *kind) {
+  const char *f = std::getenv("SS2_FAULT");
+  if (!f || !*f) return false;
+  const size_t n = std::strlen(kind);
+  for (const char *p = f; (p = std::strstr(p, kind)) != nullptr; p += n) {
+    const bool starts = p == f || p[-1] == ',';
+    const bool ends = p[n] == '\0' || p[n] == ',';
+    if (starts && ends) return true;
+  }
+  return false;
+}
+
 static int dev_alloc(void **p, size_t bytes, size_t *total) {
+  if (injected("alloc")) {
+    *p = nullptr;
+    return fail(SS2_ENOMEM, "cudaMalloc of %zu bytes failed (injected by SS2_FAULT=alloc)",
+                bytes);
+  }
   cudaError_t e = cudaMalloc(p, bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -617,6 +638,7 @@ static int run_batch(ss2_ctx *c, Lane &L, const uint8_t *ref, const uint8_t *dis
                      cudaEvent_t after_pyramid) {
   const Geom &g = c->g;
   cudaStream_t st = L.st;
+  if (injected("launch")) return fail(SS2_EIO, "kernel launch failed (injected by SS2_FAULT=launch)");
   TIMED(c, kKPyramid, st, launch_pyramid(g, c->px, c->tabs, ref, dis, L.X, nb, st),
         "k_pyramid launch");
   if (after_pyramid) CU(cudaEventRecord(after_pyramid, st), "event record");
@@ -676,6 +698,22 @@ static int check_call(ss2_ctx *ctx, const void *ref, const void *dis, int n) {
   return 0;
 }
 
+// After a failure part of a call's work may still be queued on the lanes:
+// wait for it so that the context can be reused or destroyed safely.
+static int drain(ss2_ctx *c, int rc) {
+  for (Lane &L : c->lane)
+    if (L.st) cudaStreamSynchronize(L.st);
+  if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+  return rc;
+}
+
+static int read_back(ss2_ctx *c, double *dst, const double *src, size_t n, cudaStream_t st) {
+  if (injected("memcpy"))
+    return fail(SS2_EIO, "device-to-host copy failed (injected by SS2_FAULT=memcpy)");
+  CU(cudaMemcpyAsync(dst, src, n * sizeof(double), cudaMemcpyDeviceToHost, st), "read-back");
+  return 0;
+}
+
 static int score_device(ss2_ctx *ctx, const void *ref, const void *dis, int n, double *scores,
                         double *values, void *stream) {
   if (check_call(ctx, ref, dis, n)) return t_err;
@@ -692,18 +730,14 @@ static int score_device(ss2_ctx *ctx, const void *ref, const void *dis, int n, d
   for (int b = 0, f0 = 0; b < nbat; ++b) {
     const int nb = base + (b < extra ? 1 : 0);
     Lane &L = ctx->lane[b % kLanes];
-    if (run_batch(ctx, L, r8 + f0 * fb, d8 + f0 * fb, nb, nullptr)) return t_err;
-    CU(cudaMemcpyAsync(ctx->h_scores + f0, L.scores, nb * sizeof(double),
-                       cudaMemcpyDeviceToHost, L.st),
-       "score read-back");
-    if (values)
-      CU(cudaMemcpyAsync(ctx->h_values + (size_t)f0 * kNValues, L.values,
-                         (size_t)nb * kNValues * sizeof(double), cudaMemcpyDeviceToHost, L.st),
-         "value read-back");
+    if (run_batch(ctx, L, r8 + f0 * fb, d8 + f0 * fb, nb, nullptr) ||
+        read_back(ctx, ctx->h_scores + f0, L.scores, (size_t)nb, L.st) ||
+        (values && read_back(ctx, ctx->h_values + (size_t)f0 * kNValues, L.values,
+                             (size_t)nb * kNValues, L.st)))
+      return drain(ctx, t_err);
     f0 += nb;
   }
-  if (join_lanes(ctx, st)) return t_err;
-  if (enqueue_err_readback(ctx, st)) return t_err;
+  if (join_lanes(ctx, st) || enqueue_err_readback(ctx, st)) return drain(ctx, t_err);
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
   if (check_err_word(ctx, st)) return t_err;
   if (scores) std::memcpy(scores, ctx->h_scores, (size_t)n * sizeof(double));
@@ -766,14 +800,12 @@ SS2_API int ss2_score_frames_host(ss2_ctx *ctx, const void *ref_host, const void
        "dis upload");
     CU(cudaEventRecord(L.ev_copied, ctx->copy_stream), "event record");
     CU(cudaStreamWaitEvent(L.st, L.ev_copied, 0), "upload wait");
-    if (run_batch(ctx, L, dref, ddis, nb, L.ev_consumed)) return t_err;
-    CU(cudaMemcpyAsync(ctx->h_scores + f0, L.scores, nb * sizeof(double),
-                       cudaMemcpyDeviceToHost, L.st),
-       "score read-back");
+    if (run_batch(ctx, L, dref, ddis, nb, L.ev_consumed) ||
+        read_back(ctx, ctx->h_scores + f0, L.scores, (size_t)nb, L.st))
+      return drain(ctx, t_err);
     f0 += nb;
   }
-  if (join_lanes(ctx, st)) return t_err;
-  if (enqueue_err_readback(ctx, st)) return t_err;
+  if (join_lanes(ctx, st) || enqueue_err_readback(ctx, st)) return drain(ctx, t_err);
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
   if (check_err_word(ctx, st)) return t_err;
   std::memcpy(scores, ctx->h_scores, (size_t)n_frames * sizeof(double));
@@ -819,5 +851,24 @@ SS2_API int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream) 
   cudaStream_t st = (cudaStream_t)stream;
   CU(launch_cbrt(x, y, n, st), "k_cbrt launch");
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  return 0;
+}
+
+SS2_API int ss2_debug_wait_probe(unsigned spins, void *stream) {
+  int dev = 0;
+  if (check_device(&dev)) return t_err;
+  int *d_flag = nullptr;
+  CU(cudaMalloc(&d_flag, sizeof(int)), "cudaMalloc");
+  int h_flag = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(d_flag, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_wait_probe(spins, d_flag, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&h_flag, d_flag, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(d_flag);
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe");
+  if (h_flag & kErrTmaTimeout)
+    return fail(SS2_EIO, "the probe kernel gave up waiting on its barrier after %u polls", spins);
   return 0;
 }

@@ -617,8 +617,32 @@ __global__ void k_cbrt(const float *__restrict__ x, float *__restrict__ y, long 
 }
 
 // ---------------------------------------------------------------------------
+// k_wait_probe: a barrier phase that nothing completes (one arrival with a
+// transaction count that no copy ever delivers); the bounded wait must give
+// up, raise the error bit and return.
+// ---------------------------------------------------------------------------
+
+__global__ void k_wait_probe(uint32_t spins, int *__restrict__ err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar, 1024);
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0, spins);
+  if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) atomicOr(err, kErrTmaTimeout);
+}
+
+// ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
+
+cudaError_t launch_wait_probe(uint32_t spins, int *err, cudaStream_t st) {
+  k_wait_probe<<<1, 32, 0, st>>>(spins, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;

@@ -19,5 +19,6 @@ cudaError_t launch_finalize(const Geom &g, const float2 *part, const double *par
                             double *values, double *scores, int nframes, cudaStream_t st);
 
 cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st);
+cudaError_t launch_wait_probe(uint32_t spins, int *err, cudaStream_t st);
 
 }  // namespace ss2

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.ss2_profile_end.restype = i
             L.ss2_score_frames_noalloc.argtypes = [i, i, i, i, vp, vp, i, vp, vp]
             L.ss2_score_frames_noalloc.restype = i
+            L.ss2_debug_wait_probe.argtypes = [ctypes.c_uint, vp]
+            L.ss2_debug_wait_probe.restype = i
             L.ss2_frame_bytes.argtypes = [vp]
             L.ss2_frame_bytes.restype = ctypes.c_size_t
             L.ss2_batch.argtypes = [vp]
