@@ -49,13 +49,17 @@ __global__ void __launch_bounds__(kPyrThreads)
     k_pyramid(Geom g, Pix px, PyrTabs tabs, const uint8_t *__restrict__ ref,
               const uint8_t *__restrict__ dis, float *__restrict__ X) {
   __shared__ float L[6][kLvlTotal];
+  __shared__ float cb_s[3];
   const int frame = blockIdx.z;
   const int tx0 = blockIdx.x * kTile, ty0 = blockIdx.y * kTile;
   float *Xf = X + (long long)frame * g.x_fs;
 
+  // cbrt(bias_i), once per block
+  if (threadIdx.x < 3) cb_s[threadIdx.x] = cbrt_cr(px.bias[threadIdx.x]);
+  __syncthreads();
   float cb[3];
 #pragma unroll
-  for (int i = 0; i < 3; ++i) cb[i] = cbrt_cr(px.bias[i]);
+  for (int i = 0; i < 3; ++i) cb[i] = cb_s[i];
 
   // ---- scale 0: unpack, matrix, EOTF, XYB ----
   {

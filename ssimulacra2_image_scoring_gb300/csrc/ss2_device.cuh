@@ -85,8 +85,8 @@ __device__ __forceinline__ ff ff_div_f(ff a, float b) {
   const float q1 = div_newton(a.hi, b, rb);
   float r = __fmaf_rn(-q1, b, a.hi);
   r = __fadd_rn(r, a.lo);
-  const float q2 = __fmul_rn(r, rb);
-  return quick_two_sum(q1, q2);
+  // |q2| is within an ulp of q1: the pair is usable without renormalising
+  return {q1, __fmul_rn(r, rb)};
 }
 
 // a / b for pairs (same scheme, the denominator's low word enters the
@@ -97,8 +97,7 @@ __device__ __forceinline__ ff ff_div(ff a, ff b) {
   float r = __fmaf_rn(-q1, b.hi, a.hi);
   r = __fadd_rn(r, a.lo);
   r = __fmaf_rn(-q1, b.lo, r);
-  const float q2 = __fmul_rn(r, rb);
-  return quick_two_sum(q1, q2);
+  return {q1, __fmul_rn(r, rb)};
 }
 
 // ---------------------------------------------------------------------------
