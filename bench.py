@@ -286,8 +286,8 @@ def run_ours(args, ws, rank, local):
     ref = torch.from_numpy(wl.ref).to(dev)
     dis = torch.from_numpy(wl.dis).to(dev)
     n = wl.ref.shape[0]
-    sc = Scorer(spec.width, spec.height, spec.depth, spec.chroma,
-                batch=min(n, 1024) if args.frames else None)
+    batch = args.batch or (min(n, 1024) if args.frames else None)
+    sc = Scorer(spec.width, spec.height, spec.depth, spec.chroma, batch=batch)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -398,6 +398,8 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="frames per pass (default: the library's choice for the geometry)")
     ap.add_argument("--frames", type=int, default=0,
                     help="score only the first N frames of the workload (small profiling cases)")
     args = ap.parse_args(argv)

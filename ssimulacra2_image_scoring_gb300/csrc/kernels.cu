@@ -374,10 +374,12 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
   const float v1 = __fsub_rn(s11, __fmul_rn(mu1, mu1));
   const float v2 = __fsub_rn(s22, __fmul_rn(mu2, mu2));
   const float den_s = __fadd_rn(__fadd_rn(v1, v2), px.c2);
-  // float-pair part: q = num_m num_s / den_s, d = max(1 - q, 0)
-  const ff q = ff_div_f(two_prod(num_m, num_s), den_s);
-  const ff one_m = two_sum(1.0f, -q.hi);
-  ff d = quick_two_sum(one_m.hi, __fsub_rn(one_m.lo, q.lo));
+  // float-pair part: d = max(1 - num_m num_s / den_s, 0), formed as
+  // (den_s - num_m num_s) / den_s with the product exact as a pair and the
+  // numerator's leading difference exact (two_sum)
+  const ff p = two_prod(num_m, num_s);
+  const ff nd = two_sum(den_s, -p.hi);
+  ff d = ff_div_f(quick_two_sum(nd.hi, __fsub_rn(nd.lo, p.lo)), den_s);
   if (!(d.hi > 0.0f)) d = {0.0f, 0.0f};
   const ff d2 = ff_mul(d, d);
   const ff d4 = ff_mul(d2, d2);
