@@ -19,7 +19,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
 SO_PATH = os.path.join(BUILD_DIR, "libss2_oracle.so")
-SOURCES = [os.path.join(HERE, "ss2_oracle.c")]
+SOURCES = [os.path.join(HERE, "ss2_oracle.c"), os.path.join(HERE, "fssim_oracle.c")]
 HEADERS = [os.path.join(HERE, "ss2_oracle.h")]
 
 NPARAMS = 133
@@ -95,6 +95,14 @@ def lib() -> ctypes.CDLL:
             L.ss2o_yuv_coeffs.argtypes = [vp]
             L.ss2o_iir_coeffs.argtypes = [vp, vp, vp]
             L.ss2o_xyb_pixel.argtypes = [vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, vp]
+            L.ss2o_fssim_scale.argtypes = [i, i]
+            L.ss2o_fssim_scale.restype = i
+            L.ss2o_fssim_dims.argtypes = [i, i, vp, vp]
+            L.ss2o_fssim_dims.restype = i
+            L.ss2o_fssim_decimate.argtypes = [vp, i, i, i, vp]
+            L.ss2o_fssim_decimate.restype = i
+            L.ss2o_fssim.argtypes = [vp, vp, i, i, i, vp, vp, vp]
+            L.ss2o_fssim.restype = i
             L.ss2o_blur_line.argtypes = [vp, i, vp]
             L.ss2o_downsample.argtypes = [vp, i, i, vp]
             _lib = L
@@ -223,6 +231,42 @@ def xyb_pixel(r: float, g: float, b: float, params: np.ndarray | None = None) ->
     lib().ss2o_xyb_pixel(_ptr(params), ctypes.c_float(r), ctypes.c_float(g), ctypes.c_float(b),
                          _ptr(out))
     return out
+
+
+def fssim_scale(w: int, h: int) -> int:
+    return int(lib().ss2o_fssim_scale(w, h))
+
+
+def fssim_dims(w: int, h: int) -> tuple[int, int, int]:
+    """(factor, decimated width, decimated height)."""
+    wd = np.zeros(1, np.int32)
+    hd = np.zeros(1, np.int32)
+    s = lib().ss2o_fssim_dims(w, h, _ptr(wd), _ptr(hd))
+    return int(s), int(wd[0]), int(hd[0])
+
+
+def fssim_decimate(frame: np.ndarray, w: int, h: int, depth: int) -> np.ndarray:
+    """The decimated luma plane of one frame (float32, hd x wd)."""
+    s, wd, hd = fssim_dims(w, h)
+    out = np.zeros((hd, wd), np.float32)
+    f = np.ascontiguousarray(frame)
+    rc = lib().ss2o_fssim_decimate(_ptr(f), w, h, depth, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"fssim decimation rejected: rc={rc}")
+    return out
+
+
+def fssim(ref: np.ndarray, dis: np.ndarray, w: int, h: int, depth: int):
+    """(score, decimated ref plane, decimated dis plane) of one frame pair."""
+    s, wd, hd = fssim_dims(w, h)
+    a = np.zeros((hd, wd), np.float32)
+    b = np.zeros((hd, wd), np.float32)
+    sc = np.zeros(1, np.float64)
+    rc = lib().ss2o_fssim(_ptr(np.ascontiguousarray(ref)), _ptr(np.ascontiguousarray(dis)),
+                          w, h, depth, _ptr(sc), _ptr(a), _ptr(b))
+    if rc != 0:
+        raise ValueError(f"fssim rejected {w}x{h}: rc={rc}")
+    return float(sc[0]), a, b
 
 
 def iir_coeffs():

@@ -92,6 +92,17 @@ void ss2o_iir_coeffs(double *a, float *c2, float *g); /* 3 each */
 void ss2o_blur_line(const float *in, int n, float *out);
 void ss2o_downsample(const float *in, int w, int h, float *out);
 
+/* float_ssim with decimation (fssim_oracle.c): factor, decimated dims,
+ * one decimated luma plane (frame = packed YUV, luma first), and the score
+ * of a pair (dec_ref / dec_dis may be NULL).  -22 bad arguments, -95 a
+ * decimated plane below 11x11 or a factor above 128.                       */
+int ss2o_fssim_scale(int width, int height);
+int ss2o_fssim_dims(int width, int height, int *wd, int *hd); /* -> factor */
+int ss2o_fssim_decimate(const void *frame, int width, int height, int bitdepth,
+                        float *out);
+int ss2o_fssim(const void *ref, const void *dis, int width, int height,
+               int bitdepth, double *score, float *dec_ref, float *dec_dis);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,10 +1,10 @@
 """Planted mistakes in the oracle must fail its pins (CPU).
 
-Each case copies oracle/ss2_oracle.c, plants one plausible slip (a dropped
-term, a wrong sign, index or operand, a missed clamp), builds the copy with
-the oracle's own flags and runs tests/test_oracle_pins.py against it in a
-child process.  A pin suite that still passes would not have caught that
-mistake in the real oracle.
+Each case copies the oracle's sources, plants one plausible slip in one of
+them (a dropped term, a wrong sign, index or operand, a missed clamp), builds
+the copy with the oracle's own flags and runs that source's pin suite against
+it in a child process.  A pin suite that still passes would not have caught
+that mistake in the real oracle.
 """
 from __future__ import annotations
 
@@ -52,18 +52,47 @@ MUTATIONS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
+# Planted slips in the float_ssim oracle, caught by tests/test_fssim_pins.py.
+FSSIM_MUTATIONS = {
+    "fssim_scale_truncates": ("int s = (int)lround((double)m / 256.0);",
+                              "int s = (int)((double)m / 256.0);"),
+    "fssim_window_not_centred": ("const int lo = -(s / 2), hi = s - 1 - s / 2;",
+                                 "const int lo = 0, hi = s - 1;"),
+    "fssim_mirror_without_edge_repeat": ("if (i < 0) i = -1 - i;", "if (i < 0) i = -i;"),
+    "fssim_tap_in_double": ("float tap = (float)luma(f, w, xx, yy, bps) * wt;",
+                            "double tap = (double)luma(f, w, xx, yy, bps) / (double)(s * s);"),
+    "fssim_c2_with_k1": ("C2 = (0.03 * L) * (0.03 * L);", "C2 = (0.01 * L) * (0.01 * L);"),
+    "fssim_cov_sign": ("cv = s12 - m1 * m2;", "cv = s12 + m1 * m2;"),
+    "fssim_window_sigma": ("g[i] = exp(-t * t / (2.0 * 1.5 * 1.5));",
+                           "g[i] = exp(-t * t / (2.0 * 1.0 * 1.0));"),
+    "fssim_dynamic_range_2_pow_depth": ("const double L = (double)((1 << depth) - 1);",
+                                        "const double L = (double)(1 << depth);"),
+    "fssim_drops_last_window_row": ("for (int y = 0; y + WIN <= h; ++y) {",
+                                    "for (int y = 0; y + WIN < h; ++y) {"),
+}
+
+CASES = {**{n: ("ss2_oracle.c", "test_oracle_pins.py") for n in MUTATIONS},
+         **{n: ("fssim_oracle.c", "test_fssim_pins.py") for n in FSSIM_MUTATIONS}}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
 def test_planted_mistake_fails_the_pins(name, tmp_path):
-    old, new = MUTATIONS[name]
-    src = open(os.path.join(oracle.HERE, "ss2_oracle.c")).read()
-    assert src.count(old) == 1, f"mutation site not found exactly once: {old!r}"
-    (tmp_path / "ss2_oracle.c").write_text(src.replace(old, new))
+    target, pins = CASES[name]
+    old, new = {**MUTATIONS, **FSSIM_MUTATIONS}[name]
+    srcs = []
+    for path in oracle.SOURCES:
+        text = open(path).read()
+        if os.path.basename(path) == target:
+            assert text.count(old) == 1, f"mutation site not found exactly once: {old!r}"
+            text = text.replace(old, new)
+        dst = tmp_path / os.path.basename(path)
+        dst.write_text(text)
+        srcs.append(str(dst))
     (tmp_path / "ss2_oracle.h").write_text(open(os.path.join(oracle.HERE, "ss2_oracle.h")).read())
     so = tmp_path / "libmutant.so"
-    subprocess.run(["gcc", *oracle.CFLAGS, "-shared", "-o", str(so),
-                    str(tmp_path / "ss2_oracle.c"), "-lm"], check=True)
+    subprocess.run(["gcc", *oracle.CFLAGS, "-shared", "-o", str(so), *srcs, "-lm"], check=True)
     env = dict(os.environ, **{oracle.SO_OVERRIDE_ENV: str(so)})
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", pins)],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"the pins did not catch '{name}':\n{r.stdout[-2000:]}"
