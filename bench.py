@@ -5,7 +5,10 @@ synthetic stand-in for the pages' Big Buck Bunny 4K fixture) through the
 C ABI.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline]
+                  [--workload NAME] [--no-cpu-baseline] [--feature ssimulacra2|fssim]
+
+--feature fssim times float_ssim with device decimation instead (frames/s on
+the same workload; the oracle's float_ssim as the CPU baseline).
 
 --impl ours (default): frames resident in HBM, W untimed steps, then K steps
 timed with CUDA events on the scoring stream between a barrier and a
@@ -43,6 +46,7 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "SSIMULACRA2 frames/sec at 3840x2160 8-bit 4:2:0; HBM GB/s vs GB300 peak"
+FSSIM_METRIC = "float_ssim (device decimation) frames/sec; HBM GB/s vs GB300 peak"
 DEFAULT_WORKLOAD = "c3_3840x2160_8b_420"
 KERNELS = ("k_pyramid", "k_hblur", "k_vblur", "k_finalize")
 
@@ -84,18 +88,20 @@ def byte_model(spec) -> dict:
 # ---------------------------------------------------------------------------
 
 KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h"]
+FSSIM_SOURCES = ["fssim.cu"]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "ssimulacra2_image_scoring_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profile_traffic(kernel: str, workload: str, frames_per_launch: float):
+def profile_traffic(kernel: str, workload: str, frames_per_launch: float,
+                    sources=KERNEL_SOURCES):
     """dram read+write bytes per launch of `kernel`, scaled from the per-frame
     figure of its ncu summary; None when there is no summary for this
     workload or the kernels changed since it was captured."""
@@ -107,7 +113,7 @@ def profile_traffic(kernel: str, workload: str, frames_per_launch: float):
         return None
     fields = dict(line.split(":", 1) for line in text.splitlines()
                   if line.startswith(("kernel-source hash:", "traffic_bytes_per_frame:")))
-    if fields.get("kernel-source hash", "").strip() != kernel_source_hash():
+    if fields.get("kernel-source hash", "").strip() != kernel_source_hash(sources):
         return None
     try:
         return float(fields["traffic_bytes_per_frame"]) * frames_per_launch
@@ -247,15 +253,17 @@ def run_reference(args, ws, rank):
     wl = synth.make(args.workload, per_step, workers=min(per_step, cores))
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; the first step pays nothing extra
+    fssim = args.feature == "fssim"
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_throughput(wl, per_step, per_step)
+        (oracle_fssim_throughput if fssim else oracle_throughput)(wl, per_step, per_step)
     dt = time.perf_counter() - t0
     fps = per_step * args.steps / dt
     sample = (f"{per_step} frames of {spec.name} per step, one oracle thread per frame "
               f"on {per_step} host cores")
     line = {
-        "impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s",
+        "impl": "reference", "metric": FSSIM_METRIC if fssim else METRIC, "value": fps,
+        "unit": "frames/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+f64", "data": "synthetic",
@@ -390,6 +398,139 @@ def run_ours(args, ws, rank, local):
     return 0
 
 
+def fssim_byte_model(spec, scale: int) -> dict:
+    """Algorithmic bytes per frame of float_ssim: the luma pair read once
+    (b_min), the two decimated fp32 planes written, then read by the map."""
+    bps = 1 if spec.depth == 8 else 2
+    wd, hd = -(-spec.width // scale), -(-spec.height // scale)
+    luma_pair = 2 * spec.width * spec.height * bps
+    dec = 2 * 4 * wd * hd
+    return {"b_min": luma_pair, "k_fssim_decimate": luma_pair + dec, "k_fssim_map": dec,
+            "k_fssim_final": 0}
+
+
+def oracle_fssim_throughput(wl, n_frames: int, threads: int) -> tuple[float, float]:
+    import concurrent.futures as cf
+
+    import oracle
+    oracle.build()
+    sp = wl.spec
+    idx = [i % wl.ref.shape[0] for i in range(n_frames)]
+
+    def one(j):
+        return oracle.fssim(wl.ref[j], wl.dis[j], sp.width, sp.height, sp.depth)[0]
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, idx))
+    dt = time.perf_counter() - t0
+    return n_frames / dt, dt
+
+
+def run_fssim(args, ws, rank, local):
+    spec = synth.SPECS[args.workload]
+    wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
+    import torch
+    import torch.distributed as dist
+
+    from ssimulacra2_image_scoring_gb300 import FloatSSIM
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ref = torch.from_numpy(wl.ref).to(dev)
+    dis = torch.from_numpy(wl.dis).to(dev)
+    n = wl.ref.shape[0]
+    fs = FloatSSIM(spec.width, spec.height, spec.depth, spec.chroma, batch=args.batch)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        fs.score(ref, dis, stream)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    fs.profile_begin()
+    start.record(stream)
+    for _ in range(args.steps):
+        scores = fs.score(ref, dis, stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    prof = fs.profile_end()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(start.elapsed_time(end), ws)
+    value = n * ws * args.steps / (ms_total / 1000.0)
+
+    bm = fssim_byte_model(spec, fs.scale)
+    dom = "k_fssim_decimate"
+    dom_ms, dom_launches = prof[dom]
+    frames_per_launch = n * args.steps / max(1, dom_launches)
+    algo = bm[dom] * frames_per_launch
+    achieved = algo / (dom_ms / dom_launches / 1000.0) / 1e9
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_src = json.load(f)["hbm_gbs"], "measured"
+    except (OSError, ValueError, KeyError):
+        peak, peak_src = 6800.0, "fallback"
+    traffic = profile_traffic(dom, spec.name, frames_per_launch, FSSIM_SOURCES)
+
+    # e2e: pinned host frames copied in and scores read back every step
+    pr = torch.from_numpy(wl.ref).pin_memory()
+    pd = torch.from_numpy(wl.dis).pin_memory()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(max(1, args.steps)):
+        ref.copy_(pr, non_blocking=True)
+        dis.copy_(pd, non_blocking=True)
+        fs.score(ref, dis, stream)
+    torch.cuda.synchronize()
+    e2e_fps = n * ws * max(1, args.steps) / max_over_ranks(time.perf_counter() - t0, ws)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        k = max(1, min(host_cores(), 16))
+        fps_cpu, dt_cpu = oracle_fssim_throughput(wl, 4 * k, k)
+        cpu = {"value": fps_cpu, "unit": "frames/s", "cores": k, "kind": "oracle",
+               "sample": f"{4 * k} frames of {spec.name}, one oracle thread per frame on {k} "
+                         f"host cores, {dt_cpu:.1f} s"}
+    per_kernel = {k: {"ms_total": prof[k][0], "launches": prof[k][1]} for k in fs.KERNELS}
+    pipe_gbs = bm["b_min"] * value / ws / 1e9
+    line = {
+        "metric": FSSIM_METRIC, "value": value, "unit": "frames/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "feature": "fssim", "scale": fs.scale,
+                   "frames_per_step": n,
+                   "l2": "inputs larger than L2 (YUV 1.24 GB per step, luma read 0.83 GB)"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algo_bytes_per_launch": algo,
+                     "avg_launch_ms": dom_ms / dom_launches},
+        "pipeline": {"b_min_bytes_per_frame": bm["b_min"], "achieved_gbs": pipe_gbs,
+                     "frac": pipe_gbs / peak, "per_kernel": per_kernel},
+        "clocks": clk,
+        "e2e": {"value": e2e_fps, "unit": "frames/s",
+                "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
+                "d2h_bytes_per_step": 8 * n},
+        "gpu_launches": sum(prof[k][1] for k in fs.KERNELS),
+        "cpu_baseline": cpu,
+        "scores_head": [float(x) for x in scores[:3]],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    fs.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,12 +543,16 @@ def main(argv=None) -> int:
                     help="frames per pass (default: the library's choice for the geometry)")
     ap.add_argument("--frames", type=int, default=0,
                     help="score only the first N frames of the workload (small profiling cases)")
+    ap.add_argument("--feature", choices=["ssimulacra2", "fssim"], default="ssimulacra2",
+                    help="fssim: float_ssim with device decimation on the same workload")
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     import __graft_entry__
     __graft_entry__.build()
+    if args.feature == "fssim":
+        return run_fssim(args, ws, rank, local)
     return run_ours(args, ws, rank, local)
 
 

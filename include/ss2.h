@@ -225,6 +225,46 @@ int ss2_score_frames_noalloc(int width, int height, int bitdepth, int chroma,
                              const void *ref, const void *dis, int n_frames,
                              double *scores, void *stream);
 
+/*
+ * float_ssim with decimation on the device ("ADR-1405: float_ssim_hip
+ * decimates on the device, bit-identical to the CPU", Context and Decision
+ * 1 and 4).  The luma plane of each frame (the same packed frames as above;
+ * chroma is not read) is decimated by max(1, round(min(w, h) / 256)): a
+ * scale x scale box of weight RN(1 / scale^2) at (x * scale, y * scale),
+ * offsets -scale/2 .. scale-1-scale/2, symmetric edges, the fp32 taps summed
+ * exactly and rounded once; then SSIM with an 11x11 Gaussian window
+ * (sigma 1.5, K1 = 0.01, K2 = 0.03, L = 2^depth - 1) over the positions
+ * where the window fits, averaged.
+ *   ss2_fssim_create: geometry as ss2_create; max_batch 0 = 64 frames per
+ *     pass.  NULL with -ENOTSUP when the decimated plane is below 11x11 or
+ *     the factor exceeds 128, -EINVAL for bad geometry.
+ *   ss2_fssim_score: ref, dis DEVICE frames (n_frames packed frames each,
+ *     owned by the caller, read only); scores HOST doubles (n_frames); one
+ *     stream synchronisation per call.  0 on success; -EINVAL for a NULL
+ *     context or pointer or a negative count (0 frames: no work); -ENOMEM
+ *     when the pinned staging cannot grow; -EIO on a CUDA failure.  The
+ *     context owns its workspace: 2 fp32 planes of pitch x ceil(h/scale)
+ *     (pitch = ceil(w/scale) rounded up to 32) per frame of the batch.
+ *   ss2_fssim_scale: the decimation factor.
+ *   ss2_fssim_debug_decimated: the two decimated planes of one frame pair
+ *     (HOST floats, ref then dis, each ceil(w/scale) x ceil(h/scale),
+ *     packed).
+ *   ss2_fssim_profile_begin / _end: as ss2_profile_begin / _end, kernel
+ *     classes 0 k_fssim_decimate, 1 k_fssim_map, 2 k_fssim_final (ms: 3
+ *     doubles, launches: 3 ints, either may be NULL).
+ */
+typedef struct ss2_fssim ss2_fssim;
+ss2_fssim *ss2_fssim_create(int width, int height, int bitdepth, int chroma,
+                            int max_batch);
+int ss2_fssim_score(ss2_fssim *ctx, const void *ref, const void *dis,
+                    int n_frames, double *scores, void *stream);
+int ss2_fssim_scale(const ss2_fssim *ctx);
+int ss2_fssim_debug_decimated(ss2_fssim *ctx, const void *ref,
+                              const void *dis, float *planes, void *stream);
+int ss2_fssim_profile_begin(ss2_fssim *ctx);
+int ss2_fssim_profile_end(ss2_fssim *ctx, double *ms, int *launches);
+void ss2_fssim_destroy(ss2_fssim *ctx);
+
 /* Last failure on the calling thread (0 if none yet).                      */
 int ss2_last_error(void);
 const char *ss2_last_error_string(void);

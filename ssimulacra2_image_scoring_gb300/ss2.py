@@ -65,6 +65,20 @@ def lib() -> ctypes.CDLL:
             L.ss2_score_frames_noalloc.restype = i
             L.ss2_debug_wait_probe.argtypes = [ctypes.c_uint, vp]
             L.ss2_debug_wait_probe.restype = i
+            L.ss2_fssim_create.argtypes = [i, i, i, i, i]
+            L.ss2_fssim_create.restype = vp
+            L.ss2_fssim_score.argtypes = [vp, vp, vp, i, vp, vp]
+            L.ss2_fssim_score.restype = i
+            L.ss2_fssim_scale.argtypes = [vp]
+            L.ss2_fssim_scale.restype = i
+            L.ss2_fssim_debug_decimated.argtypes = [vp, vp, vp, vp, vp]
+            L.ss2_fssim_debug_decimated.restype = i
+            L.ss2_fssim_profile_begin.argtypes = [vp]
+            L.ss2_fssim_profile_begin.restype = i
+            L.ss2_fssim_profile_end.argtypes = [vp, vp, vp]
+            L.ss2_fssim_profile_end.restype = i
+            L.ss2_fssim_destroy.argtypes = [vp]
+            L.ss2_fssim_destroy.restype = None
             L.ss2_frame_bytes.argtypes = [vp]
             L.ss2_frame_bytes.restype = ctypes.c_size_t
             L.ss2_batch.argtypes = [vp]
@@ -150,6 +164,69 @@ def _stream_handle(stream) -> int | None:
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream
+
+
+class FloatSSIM:
+    """float_ssim with device decimation for one frame geometry (ss2_fssim_create)."""
+
+    def __init__(self, width: int, height: int, bitdepth: int, chroma: int, batch: int = 0):
+        h = lib().ss2_fssim_create(width, height, bitdepth, chroma, batch)
+        if not h:
+            code, msg = last_error()
+            raise SS2Error(code, msg)
+        self._h = h
+        self.width, self.height = width, height
+        self.scale = int(lib().ss2_fssim_scale(h))
+
+    def score(self, ref, dis, stream=None) -> np.ndarray:
+        import torch
+        for t in (ref, dis):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+                raise TypeError("frames must be contiguous CUDA tensors")
+        n = ref.shape[0]
+        out = np.zeros(n, np.float64)
+        _check(lib().ss2_fssim_score(self._h, ref.data_ptr(), dis.data_ptr(), n,
+                                     out.ctypes.data, _stream_handle(stream)))
+        return out
+
+    def decimated(self, ref, dis, stream=None) -> np.ndarray:
+        """The two decimated luma planes (2, hd, wd) of the first frame pair."""
+        s = self.scale
+        wd, hd = (self.width + s - 1) // s, (self.height + s - 1) // s
+        out = np.zeros((2, hd, wd), np.float32)
+        _check(lib().ss2_fssim_debug_decimated(self._h, ref.data_ptr(), dis.data_ptr(),
+                                               out.ctypes.data, _stream_handle(stream)))
+        return out
+
+    KERNELS = ("k_fssim_decimate", "k_fssim_map", "k_fssim_final")
+
+    def profile_begin(self) -> None:
+        """Starts per-kernel CUDA-event timing of this context's launches."""
+        _check(lib().ss2_fssim_profile_begin(self._h))
+
+    def profile_end(self) -> dict:
+        """Stops timing; returns {kernel: (total ms, launches)}."""
+        ms = np.zeros(3, np.float64)
+        n = np.zeros(3, np.int32)
+        _check(lib().ss2_fssim_profile_end(self._h, ms.ctypes.data, n.ctypes.data))
+        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
+
+    def close(self) -> None:
+        if self._h:
+            lib().ss2_fssim_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Scorer:
