@@ -11,19 +11,25 @@
  *     1.0f / (scale * scale) and decimated: output (x, y) is the filter at
  *     (x * scale, y * scale) with offsets -scale/2 .. scale-1-scale/2 and
  *     symmetric edges; every tap is the fp32 product sample * weight and the
- *     taps are summed exactly, then rounded once to fp32;
+ *     taps are summed exactly (an int64 count of 2^-52 units on the page),
+ *     then rounded once to fp32;
  *   - SSIM on the decimated planes with an 11x11 Gaussian window; planes
  *     smaller than the window or scales above 128 are refused.
- * Readings (the page is silent): decimated dims ceil(w / scale) x
- * ceil(h / scale); "symmetric" edges mirror with the edge sample repeated
- * (-1 -> 0, w -> w-1); SSIM as Wang et al. (2004): Gaussian window sigma 1.5
+ * Readings (the page is silent): samples are taken in the 8-bit range,
+ * raw / 2^(depth - 8) (exact in fp32), and L = 255 -- the page's window sum
+ * in 2^-52 units is exact "up to scale 128" and its planes byte-identical at
+ * 10, 12 and 16 bits only if every sample stays below 2^11, which raw 12- and
+ * 16-bit samples do not; decimated dims ceil(w / scale) x ceil(h / scale);
+ * "symmetric" edges mirror with the edge sample repeated (-1 -> 0,
+ * w -> w-1); SSIM as Wang et al. (2004): Gaussian window sigma 1.5
  * normalised to sum 1, evaluated where the window fits ("valid"), K1 = 0.01,
- * K2 = 0.03, L = 2^depth - 1, the score the mean of the map; luma only.
+ * K2 = 0.03, the score the mean of the map; luma only.
  *
- * The exact window sum: a tap is sample * w rounded to float with
- * w = RN(1 / scale^2) >= 2^-14 (scale <= 128), so every tap is a multiple of
- * 2^-37 and below 2^16, and the window sum (<= 2^16) needs at most 53 bits:
- * an fp64 running sum of the taps is exact.
+ * The exact window sum: a tap is sample * w rounded to float with sample a
+ * multiple of 2^-8 below 256 and w = RN(1 / scale^2) >= 2^-14 (scale <= 128),
+ * so every nonzero tap is at least 2^-22, a multiple of 2^-45, and the window
+ * sum stays below 256 = 2^53 * 2^-45: an fp64 running sum of the taps is
+ * exact.
  */
 #include <math.h>
 #include <stdint.h>
@@ -67,18 +73,25 @@ static int luma(const uint8_t *f, int w, int x, int y, int bps)
     return (int)f[2 * i] | ((int)f[2 * i + 1] << 8);
 }
 
+/* A luma sample in the 8-bit range: raw / 2^(depth - 8), exact in fp32.     */
+static float sample8(const uint8_t *f, int w, int x, int y, int bps, float norm)
+{
+    return (float)luma(f, w, x, y, bps) * norm;
+}
+
 int ss2o_fssim_decimate(const void *frame, int w, int h, int depth, float *out)
 {
     if (w < 1 || h < 1 || depth < 8 || depth > 16) return EINVAL_RC;
     const int s = ss2o_fssim_scale(w, h);
     if (s > 128) return ENOTSUP_RC;
     const int bps = depth > 8 ? 2 : 1;
+    const float norm = 1.0f / (float)(1 << (depth - 8));
     const uint8_t *f = (const uint8_t *)frame;
     int wd, hd;
     ss2o_fssim_dims(w, h, &wd, &hd);
     if (s == 1) {
         for (int y = 0; y < h; ++y)
-            for (int x = 0; x < w; ++x) out[(size_t)y * w + x] = (float)luma(f, w, x, y, bps);
+            for (int x = 0; x < w; ++x) out[(size_t)y * w + x] = sample8(f, w, x, y, bps, norm);
         return 0;
     }
     const float wt = 1.0f / (float)(s * s);
@@ -90,7 +103,7 @@ int ss2o_fssim_decimate(const void *frame, int w, int h, int depth, float *out)
                 int yy = mirror(y * s + dy, h);
                 for (int dx = lo; dx <= hi; ++dx) {
                     int xx = mirror(x * s + dx, w);
-                    float tap = (float)luma(f, w, xx, yy, bps) * wt;
+                    float tap = sample8(f, w, xx, yy, bps, norm) * wt;
                     sum += (double)tap;
                 }
             }
@@ -155,8 +168,7 @@ int ss2o_fssim(const void *ref, const void *dis, int w, int h, int depth, double
     }
     ss2o_fssim_decimate(ref, w, h, depth, a);
     ss2o_fssim_decimate(dis, w, h, depth, b);
-    const double L = (double)((1 << depth) - 1);
-    if (score) *score = ssim_planes(a, b, wd, hd, L);
+    if (score) *score = ssim_planes(a, b, wd, hd, 255.0);
     if (dec_ref) memcpy(dec_ref, a, sizeof(float) * n);
     if (dec_dis) memcpy(dec_dis, b, sizeof(float) * n);
     free(a);

@@ -93,9 +93,10 @@ void ss2o_blur_line(const float *in, int n, float *out);
 void ss2o_downsample(const float *in, int w, int h, float *out);
 
 /* float_ssim with decimation (fssim_oracle.c): factor, decimated dims,
- * one decimated luma plane (frame = packed YUV, luma first), and the score
- * of a pair (dec_ref / dec_dis may be NULL).  -22 bad arguments, -95 a
- * decimated plane below 11x11 or a factor above 128.                       */
+ * one decimated luma plane (frame = packed YUV, luma first; samples in the
+ * 8-bit range, raw / 2^(depth - 8)), and the score of a pair (dec_ref /
+ * dec_dis may be NULL).  -22 bad arguments, -95 a decimated plane below
+ * 11x11 or a factor above 128.                                             */
 int ss2o_fssim_scale(int width, int height);
 int ss2o_fssim_dims(int width, int height, int *wd, int *hd); /* -> factor */
 int ss2o_fssim_decimate(const void *frame, int width, int height, int bitdepth,

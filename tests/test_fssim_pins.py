@@ -2,10 +2,11 @@
 
 Decimation: the factors printed on "ADR-1405: float_ssim_hip decimates on
 the device, bit-identical to the CPU" (Context); the window sum against
-exact integer arithmetic with numpy's own symmetric padding; a constant
-plane.  SSIM: identity, symmetry, two flat frames, and one bright pixel on a
-flat frame, each in closed form from the definition (Wang et al. 2004) and
-an 11-tap sigma-1.5 Gaussian written out here.
+exact integer arithmetic in the page's 2^-52 units (Decision 1) with numpy's
+own symmetric padding; a constant plane.  SSIM: identity, symmetry, two flat
+frames, and one bright pixel on a flat frame, each in closed form from the
+definition (Wang et al. 2004) and an 11-tap sigma-1.5 Gaussian written out
+here.  Samples are in the 8-bit range (raw / 2^(depth - 8)) with L = 255.
 """
 from __future__ import annotations
 
@@ -44,11 +45,26 @@ def test_factor_is_rounded_not_truncated():
     assert oracle.fssim_scale(1100, 1100) == 4                                     # 4.30
 
 
-@pytest.mark.parametrize("size,depth", [(512, 8), (768, 8), (1280, 16), (853, 10)])
+def _f32_of_units(units: int, k: int) -> np.float32:
+    """units * 2^-k rounded once to fp32 (nearest, ties to even)."""
+    if units == 0:
+        return np.float32(0.0)
+    shift = units.bit_length() - 24
+    if shift > 0:
+        q, r = divmod(units, 1 << shift)
+        half = 1 << (shift - 1)
+        if r > half or (r == half and q & 1):
+            q += 1
+        return np.float32(math.ldexp(q, shift - k))      # q <= 2^24: exact
+    return np.float32(math.ldexp(units, -k))
+
+
+@pytest.mark.parametrize("size,depth", [(512, 8), (768, 8), (1280, 16), (853, 10), (700, 12)])
 def test_decimation_is_the_exact_window_sum(size, depth):
     """Every output is the sum of the fp32 taps sample * RN(1/s^2) over the
     s x s window at (x s, y s) with offsets -s/2 .. s-1-s/2 and symmetric
-    edges, summed exactly (Python integers) and rounded once to float."""
+    edges, sample = raw / 2^(depth - 8), counted exactly in 2^-52 units
+    (Python integers) and rounded once to float."""
     w, h = size, size - 3 if size == 853 else size
     rng = np.random.default_rng(size)
     Y = rng.integers(0, 1 << depth, (h, w))
@@ -57,16 +73,17 @@ def test_decimation_is_the_exact_window_sum(size, depth):
     got = oracle.fssim_decimate(_luma_frame(Y, depth=depth), w, h, depth)
     assert got.shape == (hd, wd) and wd == -(-w // s) and hd == -(-h // s)
     wt = np.float32(1.0) / np.float32(s * s)
+    norm = np.float32(2.0 ** (8 - depth))
     lo = s // 2
     pad = np.pad(Y, ((lo, 2 * s), (lo, 2 * s)), mode="symmetric")
     pts = [(0, 0), (0, wd - 1), (hd - 1, 0), (hd - 1, wd - 1)]
     pts += [(int(a), int(b)) for a, b in zip(rng.integers(0, hd, 200), rng.integers(0, wd, 200))]
     for (y, x) in pts:
-        win = pad[y * s:y * s + s, x * s:x * s + s].astype(np.float32)
+        win = pad[y * s:y * s + s, x * s:x * s + s].astype(np.float32) * norm   # exact
         taps = (win * wt).astype(np.float32)            # one fp32 product per tap
-        units = sum(int(t * 2.0 ** 37) for t in taps.ravel().tolist())  # exact: 2^-37 units
-        assert all(float(t * 2.0 ** 37).is_integer() for t in taps.ravel().tolist())
-        want = np.float32(units * 2.0 ** -37)            # exact double, one rounding
+        tl = [float(t) * 2.0 ** 52 for t in taps.ravel().tolist()]
+        assert all(t.is_integer() and t < 2.0 ** 61 for t in tl)   # 2^-52 units fit int64
+        want = _f32_of_units(sum(int(t) for t in tl), 52)
         assert got[y, x] == want, (y, x, got[y, x], want)
 
 
@@ -91,14 +108,19 @@ def test_identical_and_swapped_pairs():
     assert abs(oracle.fssim(a, b, 80, 60, 8)[0] - oracle.fssim(b, a, 80, 60, 8)[0]) <= 1e-15
 
 
-def test_two_flat_frames():
+@pytest.mark.parametrize("depth", [8, 10, 16])
+def test_two_flat_frames(depth):
+    """Means c1, c2 in the 8-bit range, no variance: SSIM is the luminance
+    term (2 c1 c2 + C1) / (c1^2 + c2^2 + C1), C1 = (0.01 * 255)^2."""
     L = 255.0
     C1 = (K1 * L) ** 2
-    for c1, c2 in ((40, 200), (128, 130), (0, 255)):
-        a = _luma_frame(np.full((48, 64), c1))
-        b = _luma_frame(np.full((48, 64), c2))
+    k = 1 << (depth - 8)
+    for r1, r2 in ((40 * k, 200 * k + 1), (128 * k, 130 * k), (0, 255 * k + k - 1)):
+        a = _luma_frame(np.full((48, 64), r1), depth=depth)
+        b = _luma_frame(np.full((48, 64), r2), depth=depth)
+        c1, c2 = r1 / k, r2 / k
         want = (2 * c1 * c2 + C1) / (c1 * c1 + c2 * c2 + C1)
-        assert abs(oracle.fssim(a, b, 64, 48, 8)[0] - want) <= 1e-12
+        assert abs(oracle.fssim(a, b, 64, 48, depth)[0] - want) <= 1e-12
 
 
 def test_one_bright_pixel_on_a_flat_frame():

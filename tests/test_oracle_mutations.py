@@ -59,14 +59,16 @@ FSSIM_MUTATIONS = {
     "fssim_window_not_centred": ("const int lo = -(s / 2), hi = s - 1 - s / 2;",
                                  "const int lo = 0, hi = s - 1;"),
     "fssim_mirror_without_edge_repeat": ("if (i < 0) i = -1 - i;", "if (i < 0) i = -i;"),
-    "fssim_tap_in_double": ("float tap = (float)luma(f, w, xx, yy, bps) * wt;",
-                            "double tap = (double)luma(f, w, xx, yy, bps) / (double)(s * s);"),
+    "fssim_tap_in_double": ("float tap = sample8(f, w, xx, yy, bps, norm) * wt;",
+                            "double tap = (double)sample8(f, w, xx, yy, bps, norm) / (s * s);"),
     "fssim_c2_with_k1": ("C2 = (0.03 * L) * (0.03 * L);", "C2 = (0.01 * L) * (0.01 * L);"),
     "fssim_cov_sign": ("cv = s12 - m1 * m2;", "cv = s12 + m1 * m2;"),
     "fssim_window_sigma": ("g[i] = exp(-t * t / (2.0 * 1.5 * 1.5));",
                            "g[i] = exp(-t * t / (2.0 * 1.0 * 1.0));"),
-    "fssim_dynamic_range_2_pow_depth": ("const double L = (double)((1 << depth) - 1);",
-                                        "const double L = (double)(1 << depth);"),
+    "fssim_raw_samples_above_8_bits": ("const float norm = 1.0f / (float)(1 << (depth - 8));",
+                                       "const float norm = 1.0f;"),
+    "fssim_dynamic_range_256": ("*score = ssim_planes(a, b, wd, hd, 255.0);",
+                                "*score = ssim_planes(a, b, wd, hd, 256.0);"),
     "fssim_drops_last_window_row": ("for (int y = 0; y + WIN <= h; ++y) {",
                                     "for (int y = 0; y + WIN < h; ++y) {"),
 }
