@@ -229,12 +229,13 @@ int ss2_score_frames_noalloc(int width, int height, int bitdepth, int chroma,
  * float_ssim with decimation on the device ("ADR-1405: float_ssim_hip
  * decimates on the device, bit-identical to the CPU", Context and Decision
  * 1 and 4).  The luma plane of each frame (the same packed frames as above;
- * chroma is not read) is decimated by max(1, round(min(w, h) / 256)): a
- * scale x scale box of weight RN(1 / scale^2) at (x * scale, y * scale),
- * offsets -scale/2 .. scale-1-scale/2, symmetric edges, the fp32 taps summed
- * exactly and rounded once; then SSIM with an 11x11 Gaussian window
- * (sigma 1.5, K1 = 0.01, K2 = 0.03, L = 2^depth - 1) over the positions
- * where the window fits, averaged.
+ * chroma is not read), in the 8-bit range (raw / 2^(depth - 8)), is
+ * decimated by max(1, round(min(w, h) / 256)): a scale x scale box of weight
+ * RN(1 / scale^2) at (x * scale, y * scale), offsets -scale/2 ..
+ * scale-1-scale/2, symmetric edges, the fp32 taps summed exactly (int64
+ * units of 2^-52) and rounded once; then SSIM with an 11x11 Gaussian window
+ * (sigma 1.5, K1 = 0.01, K2 = 0.03, L = 255) over the positions where the
+ * window fits, averaged.
  *   ss2_fssim_create: geometry as ss2_create; max_batch 0 = 64 frames per
  *     pass.  NULL with -ENOTSUP when the decimated plane is below 11x11 or
  *     the factor exceeds 128, -EINVAL for bad geometry.

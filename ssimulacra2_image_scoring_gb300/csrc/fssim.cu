@@ -5,15 +5,19 @@
 // to the CPU" (vmafx documentation), Context and Decision 1 and 4: the
 // factor max(1, round(min(w, h) / 256)); a scale x scale box of weight
 // 1.0f / (scale * scale) at (x * scale, y * scale), offsets -scale/2 ..
-// scale-1-scale/2, symmetric edges, fp32 taps summed exactly and rounded
-// once; SSIM with an 11x11 Gaussian on the decimated planes; -ENOTSUP for a
-// decimated plane below 11x11 or a factor above 128.
+// scale-1-scale/2, symmetric edges, fp32 taps summed exactly in int64 units
+// of 2^-52 and rounded once; SSIM with an 11x11 Gaussian on the decimated
+// planes; -ENOTSUP for a decimated plane below 11x11 or a factor above 128.
+// Samples are taken in the 8-bit range, raw / 2^(depth - 8) (exact), and
+// L = 255: only then does a window sum in 2^-52 units fit an int64 at every
+// depth, as the page states for 10, 12 and 16 bits.
 //
 //   k_fssim_decimate  one thread per decimated pixel of both images; the
-//                     window sum is an int64 count of 2^-37 units: every tap
-//                     (a float product sample * w with w >= 2^-14) is a
-//                     multiple of 2^-37 below 2^16 and the sum stays below
-//                     2^53, so the sum is exact and one conversion rounds it.
+//                     window sum is an int64 count of 2^-52 units: every
+//                     nonzero tap (a float product sample * w, sample a
+//                     multiple of 2^-8 below 256, w >= 2^-14) is a multiple
+//                     of 2^-45 below 256, so the count stays below 2^61, is
+//                     exact, and one conversion rounds it.
 //   k_fssim_map       16x16 map tiles: separable 11-tap Gaussian sums of
 //                     x1, x2, x1^2, x2^2, x1 x2 in fp32 on samples shifted by
 //                     a per-tile offset (variances and covariance do not
@@ -45,6 +49,7 @@ struct FGeom {
   long long frame_bytes, plane;          // plane = pitch * hd floats
   int ow, oh, tiles_x, tiles_y;          // map outputs ("valid") and tiles
   float wt;                              // RN(1 / scale^2)
+  float norm;                            // 2^(8 - depth): samples in the 8-bit range
   float C1, C2;
   float gauss[kWin];
 };
@@ -77,14 +82,15 @@ __global__ void __launch_bounds__(256)
   float *out = D + (long long)frame * 2 * g.plane + (long long)y * g.pitch + x;
   if (g.scale == 1) {
 #pragma unroll
-    for (int img = 0; img < 2; ++img) out[img * g.plane] = (float)luma_at<BPS>(fr[img], g.w, x, y);
+    for (int img = 0; img < 2; ++img)
+      out[img * g.plane] = __fmul_rn((float)luma_at<BPS>(fr[img], g.w, x, y), g.norm);
     return;
   }
   const int lo = -(g.scale / 2), hi = g.scale - 1 - g.scale / 2;
   const int x0 = x * g.scale + lo, y0 = y * g.scale + lo;
   // windows wholly inside the frame need no mirroring (all but the edges)
   const bool inner = x0 >= 0 && y0 >= 0 && x * g.scale + hi < g.w && y * g.scale + hi < g.h;
-  const float two37 = 137438953472.0f;  // 2^37
+  const float two52 = 4503599627370496.0f;  // 2^52
 #pragma unroll
   for (int img = 0; img < 2; ++img) {
     long long acc = 0;
@@ -94,8 +100,8 @@ __global__ void __launch_bounds__(256)
       for (int yy = y0; yy < y0 + g.scale; ++yy) {
 #pragma unroll 4
         for (int xx = x0; xx < x0 + g.scale; ++xx) {
-          const float tap = __fmul_rn((float)luma_at<BPS>(f, g.w, xx, yy), g.wt);
-          acc += __float2ll_rn(__fmul_rn(tap, two37));   // exact: an integer below 2^53
+          const float smp = __fmul_rn((float)luma_at<BPS>(f, g.w, xx, yy), g.norm);  // exact
+          acc += __float2ll_rn(__fmul_rn(__fmul_rn(smp, g.wt), two52));   // exact integer
         }
       }
     } else {
@@ -105,12 +111,12 @@ __global__ void __launch_bounds__(256)
 #pragma unroll 1
         for (int dx = lo; dx <= hi; ++dx) {
           const int xx = mirror(x * g.scale + dx, g.w);
-          const float tap = __fmul_rn((float)luma_at<BPS>(fr[img], g.w, xx, yy), g.wt);
-          acc += __float2ll_rn(__fmul_rn(tap, two37));
+          const float smp = __fmul_rn((float)luma_at<BPS>(fr[img], g.w, xx, yy), g.norm);
+          acc += __float2ll_rn(__fmul_rn(__fmul_rn(smp, g.wt), two52));
         }
       }
     }
-    out[img * g.plane] = __fmul_rn(__ll2float_rn(acc), 1.0f / two37);
+    out[img * g.plane] = __fmul_rn(__ll2float_rn(acc), 1.0f / two52);   // exact scaling
   }
 }
 
@@ -246,7 +252,8 @@ SS2_API ss2_fssim *ss2_fssim_create(int width, int height, int bitdepth, int chr
   g.tiles_x = (g.ow + kTileO - 1) / kTileO;
   g.tiles_y = (g.oh + kTileO - 1) / kTileO;
   g.wt = 1.0f / (float)(g.scale * g.scale);
-  const double L = (double)((1 << bitdepth) - 1);
+  g.norm = 1.0f / (float)(1 << (bitdepth - 8));
+  const double L = 255.0;
   g.C1 = (float)((0.01 * L) * (0.01 * L));
   g.C2 = (float)((0.03 * L) * (0.03 * L));
   double gs[kWin], tot = 0.0;
