@@ -19,7 +19,8 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
 SO_PATH = os.path.join(BUILD_DIR, "libss2_oracle.so")
-SOURCES = [os.path.join(HERE, "ss2_oracle.c"), os.path.join(HERE, "fssim_oracle.c")]
+SOURCES = [os.path.join(HERE, "ss2_oracle.c"), os.path.join(HERE, "fssim_oracle.c"),
+           os.path.join(HERE, "msssim_oracle.c")]
 HEADERS = [os.path.join(HERE, "ss2_oracle.h")]
 
 NPARAMS = 133
@@ -103,6 +104,14 @@ def lib() -> ctypes.CDLL:
             L.ss2o_fssim_decimate.restype = i
             L.ss2o_fssim.argtypes = [vp, vp, i, i, i, vp, vp, vp]
             L.ss2o_fssim.restype = i
+            L.ss2o_msssim_dims.argtypes = [i, i, vp]
+            L.ss2o_msssim_dims.restype = None
+            L.ss2o_msssim_pyramid_len.argtypes = [i, i]
+            L.ss2o_msssim_pyramid_len.restype = ctypes.c_size_t
+            L.ss2o_msssim_pyramid.argtypes = [vp, i, i, i, vp]
+            L.ss2o_msssim_pyramid.restype = i
+            L.ss2o_msssim.argtypes = [vp, vp, i, i, i, vp, vp]
+            L.ss2o_msssim.restype = i
             L.ss2o_blur_line.argtypes = [vp, i, vp]
             L.ss2o_downsample.argtypes = [vp, i, i, vp]
             _lib = L
@@ -267,6 +276,42 @@ def fssim(ref: np.ndarray, dis: np.ndarray, w: int, h: int, depth: int):
     if rc != 0:
         raise ValueError(f"fssim rejected {w}x{h}: rc={rc}")
     return float(sc[0]), a, b
+
+
+MSSSIM_SCALES = 5
+MSSSIM_BETA = (0.0448, 0.2856, 0.3001, 0.2363, 0.1333)
+
+
+def msssim_dims(w: int, h: int) -> list[tuple[int, int]]:
+    d = np.zeros(2 * MSSSIM_SCALES, np.int32)
+    lib().ss2o_msssim_dims(w, h, _ptr(d))
+    return [(int(d[2 * j]), int(d[2 * j + 1])) for j in range(MSSSIM_SCALES)]
+
+
+def msssim_pyramid(frame: np.ndarray, w: int, h: int, depth: int) -> list[np.ndarray]:
+    """The five luma levels of one frame (float64, h_j x w_j each)."""
+    dims = msssim_dims(w, h)
+    buf = np.zeros(int(lib().ss2o_msssim_pyramid_len(w, h)), np.float64)
+    rc = lib().ss2o_msssim_pyramid(_ptr(np.ascontiguousarray(frame)), w, h, depth, _ptr(buf))
+    if rc != 0:
+        raise ValueError(f"msssim pyramid rejected: rc={rc}")
+    out, off = [], 0
+    for (wj, hj) in dims:
+        out.append(buf[off:off + wj * hj].reshape(hj, wj))
+        off += wj * hj
+    return out
+
+
+def msssim(ref: np.ndarray, dis: np.ndarray, w: int, h: int, depth: int):
+    """(score, values[5][5]) of one frame pair: per scale the means of
+    l, c, s, cs and l cs."""
+    sc = np.zeros(1, np.float64)
+    v = np.zeros((MSSSIM_SCALES, 5), np.float64)
+    rc = lib().ss2o_msssim(_ptr(np.ascontiguousarray(ref)), _ptr(np.ascontiguousarray(dis)),
+                           w, h, depth, _ptr(sc), _ptr(v))
+    if rc != 0:
+        raise ValueError(f"msssim rejected {w}x{h}: rc={rc}")
+    return float(sc[0]), v
 
 
 def iir_coeffs():

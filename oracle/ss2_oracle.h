@@ -104,6 +104,18 @@ int ss2o_fssim_decimate(const void *frame, int width, int height, int bitdepth,
 int ss2o_fssim(const void *ref, const void *dis, int width, int height,
                int bitdepth, double *score, float *dec_ref, float *dec_dis);
 
+/* MS-SSIM of the luma plane (msssim_oracle.c): per-scale dims (w, h pairs,
+ * 5 scales), the 5-level pyramid of one frame (levels concatenated, fp64,
+ * samples in the 8-bit range), and the score of a pair with the per-scale
+ * means values[5][5] = (l, c, s, cs, l cs) per scale (may be NULL).
+ * -22 bad arguments, -95 a scale-5 plane below 11x11.                      */
+void ss2o_msssim_dims(int width, int height, int *dims);
+size_t ss2o_msssim_pyramid_len(int width, int height);
+int ss2o_msssim_pyramid(const void *frame, int width, int height, int bitdepth,
+                        double *levels);
+int ss2o_msssim(const void *ref, const void *dis, int width, int height,
+                int bitdepth, double *score, double *values);
+
 #ifdef __cplusplus
 }
 #endif

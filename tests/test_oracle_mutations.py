@@ -73,14 +73,37 @@ FSSIM_MUTATIONS = {
                                     "for (int y = 0; y + WIN < h; ++y) {"),
 }
 
+# Planted slips in the MS-SSIM oracle, caught by tests/test_msssim_pins.py.
+MSSSIM_MUTATIONS = {
+    "msssim_betas_swapped": ("{0.0448, 0.2856, 0.3001, 0.2363, 0.1333}",
+                             "{0.2856, 0.0448, 0.3001, 0.2363, 0.1333}"),
+    "msssim_beta4_as_beta3": ("{0.0448, 0.2856, 0.3001, 0.2363, 0.1333}",
+                              "{0.0448, 0.2856, 0.3001, 0.3001, 0.1333}"),
+    "msssim_subsample_without_average": (
+        "out[(size_t)y * wo + x] = (in[(size_t)y0 * w + x0] + in[(size_t)y0 * w + x1] +",
+        "out[(size_t)y * wo + x] = 4.0 * in[(size_t)y0 * w + x0] / 4.0 + 0.0 * (in[(size_t)y0 * w + x1] +"),
+    "msssim_edge_clamp_off_by_one": ("const int x0 = 2 * x, x1 = 2 * x + 1 < w ? 2 * x + 1 : w - 1;",
+                                     "const int x0 = 2 * x, x1 = 2 * x + 1 < w ? 2 * x + 1 : w - 2;"),
+    "msssim_c3_equals_c2": ("C3 = C2 / 2.0;", "C3 = C2;"),
+    "msssim_last_scale_cs_only": ("ms *= pow(m[NSCALE - 1][4], kBeta[NSCALE - 1]);",
+                                  "ms *= pow(m[NSCALE - 1][3], kBeta[NSCALE - 1]);"),
+    "msssim_contrast_without_root": ("const double c = (2.0 * sd1 * sd2 + C2) / (v1 + v2 + C2);",
+                                     "const double c = (2.0 * v1 * v2 + C2) / (v1 + v2 + C2);"),
+    "msssim_no_depth_normalisation": ("const double norm = 1.0 / (double)(1 << (depth - 8));",
+                                      "const double norm = 1.0;"),
+    "msssim_product_skips_scale_4": ("for (int j = 0; j < NSCALE - 1; ++j) ms *= pow(m[j][3], kBeta[j]);",
+                                     "for (int j = 0; j < NSCALE - 2; ++j) ms *= pow(m[j][3], kBeta[j]);"),
+}
+
 CASES = {**{n: ("ss2_oracle.c", "test_oracle_pins.py") for n in MUTATIONS},
-         **{n: ("fssim_oracle.c", "test_fssim_pins.py") for n in FSSIM_MUTATIONS}}
+         **{n: ("fssim_oracle.c", "test_fssim_pins.py") for n in FSSIM_MUTATIONS},
+         **{n: ("msssim_oracle.c", "test_msssim_pins.py") for n in MSSSIM_MUTATIONS}}
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_planted_mistake_fails_the_pins(name, tmp_path):
     target, pins = CASES[name]
-    old, new = {**MUTATIONS, **FSSIM_MUTATIONS}[name]
+    old, new = {**MUTATIONS, **FSSIM_MUTATIONS, **MSSSIM_MUTATIONS}[name]
     srcs = []
     for path in oracle.SOURCES:
         text = open(path).read()
