@@ -88,7 +88,7 @@ def byte_model(spec) -> dict:
 # ---------------------------------------------------------------------------
 
 KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h"]
-FSSIM_SOURCES = ["fssim.cu"]
+FSSIM_SOURCES = ["fssim.cu", "ss2_tma.cuh"]
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
@@ -105,20 +105,22 @@ def profile_traffic(kernel: str, workload: str, frames_per_launch: float,
     """dram read+write bytes per launch of `kernel`, scaled from the per-frame
     figure of its ncu summary; None when there is no summary for this
     workload or the kernels changed since it was captured."""
+    import glob
     short = workload.split("_")[0]
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{short}_4frames.md")
-    try:
-        text = open(path).read()
-    except OSError:
-        return None
-    fields = dict(line.split(":", 1) for line in text.splitlines()
-                  if line.startswith(("kernel-source hash:", "traffic_bytes_per_frame:")))
-    if fields.get("kernel-source hash", "").strip() != kernel_source_hash(sources):
-        return None
-    try:
-        return float(fields["traffic_bytes_per_frame"]) * frames_per_launch
-    except (KeyError, ValueError):
-        return None
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"{kernel}_{short}_*frames.md"))):
+        try:
+            text = open(path).read()
+        except OSError:
+            continue
+        fields = dict(line.split(":", 1) for line in text.splitlines()
+                      if line.startswith(("kernel-source hash:", "traffic_bytes_per_frame:")))
+        if fields.get("kernel-source hash", "").strip() != kernel_source_hash(sources):
+            continue
+        try:
+            return float(fields["traffic_bytes_per_frame"]) * frames_per_launch
+        except (KeyError, ValueError):
+            continue
+    return None
 
 
 # ---------------------------------------------------------------------------

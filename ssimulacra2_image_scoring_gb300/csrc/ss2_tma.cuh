@@ -71,6 +71,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// Non-tensor bulk copy global -> shared of `bytes` bytes (both addresses
+// 16-byte aligned, bytes a multiple of 16), completion counted on bar.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // 4-D tiled store shared -> global (bulk group); out-of-bounds parts of the
 // box are not written.
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int x, int y,
