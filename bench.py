@@ -8,7 +8,8 @@ C ABI.  Prints one JSON line.
                   [--workload NAME] [--no-cpu-baseline] [--feature ssimulacra2|fssim]
 
 --feature fssim times float_ssim with device decimation instead (frames/s on
-the same workload; the oracle's float_ssim as the CPU baseline).
+the same workload; the oracle's float_ssim as the CPU baseline); --feature
+msssim times MS-SSIM of the luma plane the same way.
 
 --impl ours (default): frames resident in HBM, W untimed steps, then K steps
 timed with CUDA events on the scoring stream between a barrier and a
@@ -47,6 +48,10 @@ import synth  # noqa: E402
 
 METRIC = "SSIMULACRA2 frames/sec at 3840x2160 8-bit 4:2:0; HBM GB/s vs GB300 peak"
 FSSIM_METRIC = "float_ssim (device decimation) frames/sec; HBM GB/s vs GB300 peak"
+MSSSIM_METRIC = "MS-SSIM (luma, 5 scales) frames/sec; FP32 TFLOP/s vs GB300 peak"
+# FP32 peak for ALU-bound kernels: 152 SMs x 128 FP32 lanes x 2 flops x the
+# SM clock (2,070 MHz maximum): 80.5 TFLOP/s.
+FP32_LANES = 152 * 128
 DEFAULT_WORKLOAD = "c3_3840x2160_8b_420"
 KERNELS = ("k_pyramid", "k_hblur", "k_vblur", "k_finalize")
 
@@ -89,6 +94,7 @@ def byte_model(spec) -> dict:
 
 KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h"]
 FSSIM_SOURCES = ["fssim.cu", "ss2_tma.cuh"]
+MSSSIM_SOURCES = ["msssim.cu"]
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
@@ -255,16 +261,18 @@ def run_reference(args, ws, rank):
     wl = synth.make(args.workload, per_step, workers=min(per_step, cores))
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; the first step pays nothing extra
-    fssim = args.feature == "fssim"
+    leg, metric = {"fssim": (oracle_fssim_throughput, FSSIM_METRIC),
+                   "msssim": (oracle_msssim_throughput, MSSSIM_METRIC)}.get(
+        args.feature, (oracle_throughput, METRIC))
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        (oracle_fssim_throughput if fssim else oracle_throughput)(wl, per_step, per_step)
+        leg(wl, per_step, per_step)
     dt = time.perf_counter() - t0
     fps = per_step * args.steps / dt
     sample = (f"{per_step} frames of {spec.name} per step, one oracle thread per frame "
               f"on {per_step} host cores")
     line = {
-        "impl": "reference", "metric": FSSIM_METRIC if fssim else METRIC, "value": fps,
+        "impl": "reference", "metric": metric, "value": fps,
         "unit": "frames/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
@@ -429,6 +437,141 @@ def oracle_fssim_throughput(wl, n_frames: int, threads: int) -> tuple[float, flo
     return n_frames / dt, dt
 
 
+# algorithmic flops per window position of MS-SSIM: the separable 11-tap
+# sums of five quantities (2 x 55 FMAs), three products and ~25 for the
+# l, c, s, cs terms
+MSSSIM_FLOPS_PER_POSITION = 2 * 2 * 55 + 3 + 25
+
+
+def msssim_model(spec) -> dict:
+    w, h, pos, pyr = spec.width, spec.height, 0, 0
+    for j in range(5):
+        pos += (w - 10) * (h - 10)
+        if j:
+            pyr += w * h
+        w, h = (w + 1) // 2, (h + 1) // 2
+    bps = 1 if spec.depth == 8 else 2
+    luma_pair = 2 * spec.width * spec.height * bps
+    # luma pair read once; scales 2..5 of both images written once, read once
+    return {"positions": pos, "flops": pos * MSSSIM_FLOPS_PER_POSITION,
+            "bytes": luma_pair + 2 * 2 * 4 * pyr, "b_min": luma_pair}
+
+
+def oracle_msssim_throughput(wl, n_frames: int, threads: int) -> tuple[float, float]:
+    import concurrent.futures as cf
+
+    import oracle
+    oracle.build()
+    sp = wl.spec
+    idx = [i % wl.ref.shape[0] for i in range(n_frames)]
+
+    def one(j):
+        return oracle.msssim(wl.ref[j], wl.dis[j], sp.width, sp.height, sp.depth)[0]
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, idx))
+    dt = time.perf_counter() - t0
+    return n_frames / dt, dt
+
+
+def run_msssim(args, ws, rank, local):
+    spec = synth.SPECS[args.workload]
+    wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
+    import torch
+    import torch.distributed as dist
+
+    from ssimulacra2_image_scoring_gb300 import MSSSIM
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ref = torch.from_numpy(wl.ref).to(dev)
+    dis = torch.from_numpy(wl.dis).to(dev)
+    n = wl.ref.shape[0]
+    ms = MSSSIM(spec.width, spec.height, spec.depth, spec.chroma, batch=args.batch or n)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ms.score(ref, dis, stream)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ms.profile_begin()
+    start.record(stream)
+    for _ in range(args.steps):
+        scores = ms.score(ref, dis, stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    prof = ms.profile_end()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(start.elapsed_time(end), ws)
+    value = n * ws * args.steps / (ms_total / 1000.0)
+
+    mm = msssim_model(spec)
+    dom = "k_msssim_level"
+    dom_ms, dom_launches = prof[dom]
+    frames_timed = n * args.steps
+    achieved_tf = mm["flops"] * frames_timed / (dom_ms / 1000.0) / 1e12
+    sm_mhz = clk.get("sm_mhz") or 2070.0
+    peak_tf = FP32_LANES * 2 * 2070.0e6 / 1e12
+    gbs = mm["bytes"] * frames_timed / (dom_ms / 1000.0) / 1e9
+
+    pr = torch.from_numpy(wl.ref).pin_memory()
+    pd = torch.from_numpy(wl.dis).pin_memory()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(max(1, args.steps)):
+        ref.copy_(pr, non_blocking=True)
+        dis.copy_(pd, non_blocking=True)
+        ms.score(ref, dis, stream)
+    torch.cuda.synchronize()
+    e2e_fps = n * ws * max(1, args.steps) / max_over_ranks(time.perf_counter() - t0, ws)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        k = max(1, min(host_cores(), 16))
+        fps_cpu, dt_cpu = oracle_msssim_throughput(wl, k, k)
+        cpu = {"value": fps_cpu, "unit": "frames/s", "cores": k, "kind": "oracle",
+               "sample": f"{k} frames of {spec.name}, one oracle thread per frame on {k} "
+                         f"host cores, {dt_cpu:.1f} s"}
+    line = {
+        "metric": MSSSIM_METRIC, "value": value, "unit": "frames/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "feature": "msssim", "frames_per_step": n,
+                   "batch": args.batch or n,
+                   "l2": "inputs larger than L2 (YUV 1.24 GB per step, luma read 0.83 GB)"},
+        "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved_tf, "peak": peak_tf,
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz",
+                     "unit": "TFLOP/s", "frac": achieved_tf / peak_tf, "traffic": None,
+                     "flops_per_frame": mm["flops"], "hbm_gbs": gbs,
+                     "avg_launch_ms": dom_ms / dom_launches, "sm_mhz_median": sm_mhz},
+        "per_kernel": {k: {"ms_total": prof[k][0], "launches": prof[k][1]} for k in ms.KERNELS},
+        "clocks": clk,
+        "e2e": {"value": e2e_fps, "unit": "frames/s",
+                "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
+                "d2h_bytes_per_step": 8 * n},
+        "gpu_launches": sum(prof[k][1] for k in ms.KERNELS),
+        "cpu_baseline": cpu,
+        "scores_head": [float(x) for x in scores[:3]],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ms.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_fssim(args, ws, rank, local):
     spec = synth.SPECS[args.workload]
     wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
@@ -545,8 +688,10 @@ def main(argv=None) -> int:
                     help="frames per pass (default: the library's choice for the geometry)")
     ap.add_argument("--frames", type=int, default=0,
                     help="score only the first N frames of the workload (small profiling cases)")
-    ap.add_argument("--feature", choices=["ssimulacra2", "fssim"], default="ssimulacra2",
-                    help="fssim: float_ssim with device decimation on the same workload")
+    ap.add_argument("--feature", choices=["ssimulacra2", "fssim", "msssim"],
+                    default="ssimulacra2",
+                    help="fssim: float_ssim with device decimation; msssim: MS-SSIM of the "
+                         "luma plane; both on the same workload")
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
     if args.impl == "reference":
@@ -555,6 +700,8 @@ def main(argv=None) -> int:
     __graft_entry__.build()
     if args.feature == "fssim":
         return run_fssim(args, ws, rank, local)
+    if args.feature == "msssim":
+        return run_msssim(args, ws, rank, local)
     return run_ours(args, ws, rank, local)
 
 

@@ -266,6 +266,46 @@ int ss2_fssim_profile_begin(ss2_fssim *ctx);
 int ss2_fssim_profile_end(ss2_fssim *ctx, double *ms, int *launches);
 void ss2_fssim_destroy(ss2_fssim *ctx);
 
+/*
+ * MS-SSIM of the luma plane ("Research-1363: Device-resident ssimulacra2 and
+ * a single-wait MS-SSIM on SYCL", Findings 6 and 9; the method of Wang,
+ * Simoncelli and Bovik, "Multi-scale structural similarity for image quality
+ * assessment", 2003).  Samples in the 8-bit range (raw / 2^(depth - 8));
+ * five scales, scale j + 1 the 2x2 mean of scale j with the edge sample
+ * repeated (ceil halving); at every scale the 11x11 Gaussian (sigma 1.5)
+ * SSIM statistics wherever the window fits, K1 = 0.01, K2 = 0.03,
+ * C3 = C2 / 2, L = 255, and the means of l, c, s, cs and l cs; the score
+ * prod_{j<5} mean(cs_j)^beta_j * mean(l cs)_5^beta_5, beta = (0.0448,
+ * 0.2856, 0.3001, 0.2363, 0.1333).  All scales of a batch are enqueued at
+ * once; one stream synchronisation per call.
+ *   ss2_msssim_create: geometry as ss2_create; max_batch 0 = 32 frames per
+ *     pass.  NULL with -ENOTSUP when the scale-5 plane is below 11x11 (a
+ *     side below 161), -EINVAL for bad geometry, -ENOMEM.
+ *   ss2_msssim_score: ref, dis DEVICE frames (n_frames packed frames each,
+ *     owned by the caller, read only); scores HOST doubles (n_frames);
+ *     values HOST doubles (n_frames x 5 scales x (l, c, s, cs, l cs)) or
+ *     NULL.  0 on success; -EINVAL for a NULL context or pointer or a
+ *     negative count (0 frames: no work); -ENOMEM when the pinned staging
+ *     cannot grow; -EIO on a CUDA failure.  The context owns its workspace:
+ *     scales 2..5 of both images (fp32, rows padded to 32 floats) and the
+ *     per-(frame, scale, tile) partial sums of each frame of the batch.
+ *   ss2_msssim_debug_pyramid: scales 2..5 of one frame pair (HOST floats:
+ *     ref scales 2..5 then dis scales 2..5, each w_j x h_j packed).
+ *   ss2_msssim_profile_begin / _end: as ss2_profile_begin / _end, kernel
+ *     classes 0 k_msssim_level (all scales), 1 k_msssim_final (ms: 2
+ *     doubles, launches: 2 ints, either may be NULL).
+ */
+typedef struct ss2_msssim ss2_msssim;
+ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int chroma,
+                              int max_batch);
+int ss2_msssim_score(ss2_msssim *ctx, const void *ref, const void *dis,
+                     int n_frames, double *scores, double *values, void *stream);
+int ss2_msssim_debug_pyramid(ss2_msssim *ctx, const void *ref, const void *dis,
+                             float *planes, void *stream);
+int ss2_msssim_profile_begin(ss2_msssim *ctx);
+int ss2_msssim_profile_end(ss2_msssim *ctx, double *ms, int *launches);
+void ss2_msssim_destroy(ss2_msssim *ctx);
+
 /* Last failure on the calling thread (0 if none yet).                      */
 int ss2_last_error(void);
 const char *ss2_last_error_string(void);

@@ -1,0 +1,485 @@
+// msssim.cu — MS-SSIM of the luma plane on the device (ss2_msssim_* in
+// include/ss2.h).
+//
+// Source: "Research-1363: Device-resident ssimulacra2 and a single-wait
+// MS-SSIM on SYCL" (vmafx documentation), Finding 6: every scale of a frame
+// is enqueued at once, each scale's partial sums go to a span of their own,
+// and the host waits once.  The method is Wang, Simoncelli and Bovik,
+// "Multi-scale structural similarity for image quality assessment" (2003):
+// five scales of a 2x2-average pyramid (edge sample repeated), the SSIM
+// statistics of an 11x11 Gaussian window (sigma 1.5) wherever it fits,
+// K1 = 0.01, K2 = 0.03, C3 = C2 / 2, L = 255 on samples in the 8-bit range
+// (raw / 2^(depth - 8)); per scale the means of l, c, s, cs and l cs; the
+// score prod_{j<5} mean(cs_j)^beta_j * mean(l cs)_5^beta_5 with the
+// published exponents.
+//
+//   k_msssim_level  one launch per scale over the batch; a block takes a
+//                   32x16 tile of window positions: the 42x26 input tile
+//                   (raw luma at scale 1, fp32 planes after), shifted by
+//                   the tile's first reference sample (variances and
+//                   covariance do not change, cancellation does); the five
+//                   Gaussian means in fp32 (separable, products formed once
+//                   per pixel); l, c, s, cs, l cs per position; a fixed fp64
+//                   tree per block into the (frame, scale, tile) span.  It
+//                   also writes its share of the next scale: 2x2 means,
+//                   exact in fp32 (a level-5 value is at most 2^24 units of
+//                   2^-16, so every partial sum is representable).
+//   k_msssim_final  per frame: each span summed in a fixed warp order, the
+//                   means, and the product of powers (fp64).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "../../include/ss2.h"
+#include "ss2_host.h"
+
+#define SS2_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using namespace ss2;
+
+constexpr int kScales = 5;
+constexpr int kQ = 5;                      // l, c, s, cs, l cs
+constexpr int kWin = 11;
+constexpr int kTX = 32, kTY = 16;          // window positions per block
+constexpr int kIX = kTX + kWin - 1;        // input tile 42 x 26
+constexpr int kIY = kTY + kWin - 1;
+
+struct MGeom {
+  int w, h, depth, bps;
+  long long frame_bytes;
+  float norm;                    // 2^(8 - depth)
+  int ws[kScales], hs[kScales];  // plane size per scale
+  int pitch[kScales];            // fp32 pitch of scales 2..5 (index 1..4)
+  long long lvl_off[kScales];    // float offset of scales 2..5 in an image's pyramid
+  long long img_floats;          // floats of one image's scales 2..5
+  int tx[kScales], ty[kScales];  // tiles per scale
+  int tile_off[kScales], tiles_total;
+  float C1, C2, C3;
+  float gauss[kWin];
+  double beta[kScales];
+};
+
+// Sample (x, y) of image `img` of frame `frame` at scale j (MODE 0: raw
+// 8-bit luma, 1: raw 16-bit luma, 2: an fp32 pyramid plane), 8-bit range.
+template <int MODE>
+__device__ __forceinline__ float sample(const MGeom &g, int j, const uint8_t *__restrict__ raw,
+                                        const float *__restrict__ plane, int x, int y) {
+  if (MODE == 0) return (float)__ldg(raw + (long long)y * g.w + x);   // norm = 1
+  if (MODE == 1)
+    return __fmul_rn((float)__ldg(reinterpret_cast<const uint16_t *>(raw) + (long long)y * g.w + x),
+                     g.norm);
+  return __ldg(plane + (long long)y * g.pitch[j] + x);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256)
+    k_msssim_level(MGeom g, int j, const uint8_t *__restrict__ ref, const uint8_t *__restrict__ dis,
+                   float *__restrict__ pyr, double *__restrict__ part) {
+  __shared__ __align__(16) float P[kQ][kIY][kIX + 1];   // later: the block's fp64 sums
+  __shared__ float H[kQ][kIY][kTX];
+  const int frame = blockIdx.z, t = threadIdx.x;
+  const int W = g.ws[j], Hh = g.hs[j];
+  const int ox0 = blockIdx.x * kTX, oy0 = blockIdx.y * kTY;
+  const int ow = W - kWin + 1, oh = Hh - kWin + 1;
+  const uint8_t *ra = ref + (long long)frame * g.frame_bytes;
+  const uint8_t *rb = dis + (long long)frame * g.frame_bytes;
+  const float *pa = pyr + (long long)(2 * frame) * g.img_floats + g.lvl_off[j];
+  const float *pb = pa + g.img_floats;
+
+  // the 2x2 means of this block's share of the next scale
+  if (j + 1 < kScales) {
+    const int Wn = g.ws[j + 1], Hn = g.hs[j + 1];
+    const int X0 = blockIdx.x * (kTX / 2), Y0 = blockIdx.y * (kTY / 2);
+    const int X1 = blockIdx.x + 1 == gridDim.x ? Wn : X0 + kTX / 2;
+    const int Y1 = blockIdx.y + 1 == gridDim.y ? Hn : Y0 + kTY / 2;
+    const int nx = X1 - X0, n = nx * (Y1 - Y0);
+    float *na = pyr + (long long)(2 * frame) * g.img_floats + g.lvl_off[j + 1];
+    float *nb = na + g.img_floats;
+    for (int i = t; i < n; i += 256) {
+      const int X = X0 + i % nx, Y = Y0 + i / nx;
+      const int x0 = 2 * X, x1 = min(2 * X + 1, W - 1), y0 = 2 * Y, y1 = min(2 * Y + 1, Hh - 1);
+      const float a = __fadd_rn(__fadd_rn(sample<MODE>(g, j, ra, pa, x0, y0),
+                                          sample<MODE>(g, j, ra, pa, x1, y0)),
+                                __fadd_rn(sample<MODE>(g, j, ra, pa, x0, y1),
+                                          sample<MODE>(g, j, ra, pa, x1, y1)));
+      const float b = __fadd_rn(__fadd_rn(sample<MODE>(g, j, rb, pb, x0, y0),
+                                          sample<MODE>(g, j, rb, pb, x1, y0)),
+                                __fadd_rn(sample<MODE>(g, j, rb, pb, x0, y1),
+                                          sample<MODE>(g, j, rb, pb, x1, y1)));
+      na[(long long)Y * g.pitch[j + 1] + X] = __fmul_rn(a, 0.25f);
+      nb[(long long)Y * g.pitch[j + 1] + X] = __fmul_rn(b, 0.25f);
+    }
+  }
+
+  // input tile, shifted by the tile's first reference sample
+  const float off = sample<MODE>(g, j, ra, pa, ox0, oy0);
+  for (int i = t; i < kIY * kIX; i += 256) {
+    const int r = i / kIX, c = i % kIX;
+    const int y = min(oy0 + r, Hh - 1), x = min(ox0 + c, W - 1);
+    const float p = __fsub_rn(sample<MODE>(g, j, ra, pa, x, y), off);
+    const float q = __fsub_rn(sample<MODE>(g, j, rb, pb, x, y), off);
+    P[0][r][c] = p;
+    P[1][r][c] = q;
+    P[2][r][c] = __fmul_rn(p, p);
+    P[3][r][c] = __fmul_rn(q, q);
+    P[4][r][c] = __fmul_rn(p, q);
+  }
+  __syncthreads();
+  // horizontal sums: a thread takes 4 adjacent positions of one input row
+  if (t < kIY * (kTX / 4)) {
+    const int r = t / (kTX / 4), c0 = 4 * (t % (kTX / 4));
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      float v[kWin + 3];
+#pragma unroll
+      for (int k = 0; k < kWin + 3; ++k) v[k] = P[q][r][c0 + k];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kWin; ++k) acc = __fmaf_rn(g.gauss[k], v[i + k], acc);
+        H[q][r][c0 + i] = acc;
+      }
+    }
+  }
+  __syncthreads();
+  // vertical sums and the terms of two positions (rows 2 oy, 2 oy + 1)
+  const int oc = t % kTX, orow = 2 * (t / kTX);
+  const int ox = ox0 + oc;
+  float m[2][kQ];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    float v[kWin + 1];
+#pragma unroll
+    for (int k = 0; k < kWin + 1; ++k) v[k] = H[q][orow + k][oc];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int k = 0; k < kWin; ++k) acc = __fmaf_rn(g.gauss[k], v[i + k], acc);
+      m[i][q] = acc;
+    }
+  }
+  double sum[kQ] = {0, 0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int oy = oy0 + orow + i;
+    if (ox < ow && oy < oh) {
+      const float m1 = m[i][0], m2 = m[i][1];
+      const float v1 = fmaxf(__fsub_rn(m[i][2], __fmul_rn(m1, m1)), 0.0f);
+      const float v2 = fmaxf(__fsub_rn(m[i][3], __fmul_rn(m2, m2)), 0.0f);
+      const float cv = __fsub_rn(m[i][4], __fmul_rn(m1, m2));
+      const float mu1 = __fadd_rn(m1, off), mu2 = __fadd_rn(m2, off);
+      const float sd1 = __fsqrt_rn(v1), sd2 = __fsqrt_rn(v2);
+      const float vden = __fadd_rn(__fadd_rn(v1, v2), g.C2);
+      const float l = __fdiv_rn(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(mu1, mu2)), g.C1),
+                                __fadd_rn(__fadd_rn(__fmul_rn(mu1, mu1), __fmul_rn(mu2, mu2)), g.C1));
+      const float c = __fdiv_rn(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(sd1, sd2)), g.C2), vden);
+      const float s = __fdiv_rn(__fadd_rn(cv, g.C3), __fadd_rn(__fmul_rn(sd1, sd2), g.C3));
+      const float cs = __fdiv_rn(__fadd_rn(__fmul_rn(2.0f, cv), g.C2), vden);
+      sum[0] = __dadd_rn(sum[0], (double)l);
+      sum[1] = __dadd_rn(sum[1], (double)c);
+      sum[2] = __dadd_rn(sum[2], (double)s);
+      sum[3] = __dadd_rn(sum[3], (double)cs);
+      sum[4] = __dadd_rn(sum[4], __dmul_rn((double)l, (double)cs));
+    }
+  }
+  // P is no longer read (the horizontal pass ended before the last barrier)
+  double(*red)[256] = reinterpret_cast<double(*)[256]>(&P[0][0][0]);
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) red[q][t] = sum[q];
+  __syncthreads();
+#pragma unroll
+  for (int st = 128; st > 0; st >>= 1) {
+    if (t < st) {
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) red[q][t] = __dadd_rn(red[q][t], red[q][t + st]);
+    }
+    __syncthreads();
+  }
+  if (t < kQ) {
+    const long long tile = g.tile_off[j] + blockIdx.y * g.tx[j] + blockIdx.x;
+    part[((long long)frame * g.tiles_total + tile) * kQ + t] = red[t][0];
+  }
+}
+
+// One block per frame, one warp per (scale, quantity): the span summed with
+// lane l taking tiles l, l + 32, ... in order and a fixed xor tree; then the
+// means and the score.
+__global__ void __launch_bounds__(kScales * kQ * 32)
+    k_msssim_final(MGeom g, const double *__restrict__ part, double *__restrict__ scores,
+                   double *__restrict__ values) {
+  __shared__ double mean[kScales * kQ];
+  const int frame = blockIdx.x, wq = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int j = wq / kQ, q = wq % kQ;
+  const int n = g.tx[j] * g.ty[j];
+  const double *p = part + ((long long)frame * g.tiles_total + g.tile_off[j]) * kQ + q;
+  double s = 0.0;
+  for (int i = lane; i < n; i += 32) s = __dadd_rn(s, p[(long long)i * kQ]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+  if (lane == 0) {
+    const double cnt = (double)(g.ws[j] - kWin + 1) * (double)(g.hs[j] - kWin + 1);
+    mean[wq] = s / cnt;
+    values[(long long)frame * kScales * kQ + wq] = s / cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double ms = 1.0;
+    for (int k = 0; k + 1 < kScales; ++k) ms *= pow(mean[k * kQ + 3], g.beta[k]);
+    ms *= pow(mean[(kScales - 1) * kQ + 4], g.beta[kScales - 1]);
+    scores[frame] = ms;
+  }
+}
+
+}  // namespace
+
+struct ss2_msssim {
+  MGeom g;
+  int batch, device;
+  float *d_pyr = nullptr;                  // scales 2..5 of both images, per frame
+  double *d_part = nullptr, *d_scores = nullptr, *d_values = nullptr;
+  double *h_scores = nullptr, *h_values = nullptr;
+  size_t h_cap = 0;
+  bool prof = false;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<std::pair<int, int>> ev_used;  // (kernel class, index of start event)
+};
+
+static void msssim_free(ss2_msssim *c) {
+  if (!c) return;
+  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+  cudaFree(c->d_pyr);
+  cudaFree(c->d_part);
+  cudaFree(c->d_scores);
+  cudaFree(c->d_values);
+  if (c->h_scores) cudaFreeHost(c->h_scores);
+  if (c->h_values) cudaFreeHost(c->h_values);
+  delete c;
+}
+
+SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int chroma,
+                                      int max_batch) {
+  if (check_geometry(width, height, bitdepth, chroma)) return nullptr;
+  if (max_batch < 0 || max_batch > 4096) {
+    fail(SS2_EINVAL, "batch %d is outside 0..4096", max_batch);
+    return nullptr;
+  }
+  MGeom g;
+  std::memset(&g, 0, sizeof(g));
+  g.w = width; g.h = height; g.depth = bitdepth; g.bps = bitdepth > 8 ? 2 : 1;
+  Geom full;
+  make_geom(width, height, bitdepth, chroma, full);
+  g.frame_bytes = full.frame_bytes;
+  g.norm = 1.0f / (float)(1 << (bitdepth - 8));
+  int w = width, h = height;
+  long long off = 0;
+  for (int j = 0; j < kScales; ++j) {
+    g.ws[j] = w;
+    g.hs[j] = h;
+    if (j > 0) {
+      g.pitch[j] = (w + 31) & ~31;
+      g.lvl_off[j] = off;
+      off += (long long)g.pitch[j] * h;
+    }
+    w = (w + 1) / 2;
+    h = (h + 1) / 2;
+  }
+  g.img_floats = (off + 63) & ~63LL;
+  if (g.ws[kScales - 1] < kWin || g.hs[kScales - 1] < kWin) {
+    fail(SS2_ENOTSUP, "MS-SSIM: the scale-5 plane %dx%d is below the 11x11 window",
+         g.ws[kScales - 1], g.hs[kScales - 1]);
+    return nullptr;
+  }
+  int tiles = 0;
+  for (int j = 0; j < kScales; ++j) {
+    g.tx[j] = (g.ws[j] - kWin + 1 + kTX - 1) / kTX;
+    g.ty[j] = (g.hs[j] - kWin + 1 + kTY - 1) / kTY;
+    g.tile_off[j] = tiles;
+    tiles += g.tx[j] * g.ty[j];
+  }
+  g.tiles_total = tiles;
+  const double L = 255.0;
+  g.C1 = (float)((0.01 * L) * (0.01 * L));
+  g.C2 = (float)((0.03 * L) * (0.03 * L));
+  g.C3 = (float)((0.03 * L) * (0.03 * L) / 2.0);
+  double gs[kWin], tot = 0.0;
+  for (int i = 0; i < kWin; ++i) {
+    const double t = i - kWin / 2;
+    gs[i] = std::exp(-t * t / (2.0 * 1.5 * 1.5));
+    tot += gs[i];
+  }
+  for (int i = 0; i < kWin; ++i) g.gauss[i] = (float)(gs[i] / tot);
+  const double beta[kScales] = {0.0448, 0.2856, 0.3001, 0.2363, 0.1333};
+  for (int j = 0; j < kScales; ++j) g.beta[j] = beta[j];
+  int dev = 0;
+  if (check_device(&dev)) return nullptr;
+  ss2_msssim *c = new (std::nothrow) ss2_msssim();
+  if (!c) {
+    fail(SS2_ENOMEM, "host allocation failed");
+    return nullptr;
+  }
+  c->g = g;
+  c->device = dev;
+  c->batch = max_batch ? max_batch : 32;
+  const size_t B = (size_t)c->batch;
+  if (cudaMalloc(&c->d_pyr, B * 2 * g.img_floats * sizeof(float)) != cudaSuccess ||
+      cudaMalloc(&c->d_part, B * g.tiles_total * kQ * sizeof(double)) != cudaSuccess ||
+      cudaMalloc(&c->d_scores, B * sizeof(double)) != cudaSuccess ||
+      cudaMalloc(&c->d_values, B * kScales * kQ * sizeof(double)) != cudaSuccess) {
+    cudaGetLastError();
+    fail(SS2_ENOMEM, "MS-SSIM workspace allocation failed");
+    msssim_free(c);
+    return nullptr;
+  }
+  return c;
+}
+
+SS2_API void ss2_msssim_destroy(ss2_msssim *ctx) { msssim_free(ctx); }
+
+// Records the start (start = true) or end event of one launch of kernel
+// class cls while profiling.
+static cudaError_t msssim_mark(ss2_msssim *c, int cls, bool start, cudaStream_t st) {
+  if (!c->prof) return cudaSuccess;
+  size_t idx;
+  if (start) {
+    idx = c->ev_used.size() * 2;
+    while (c->ev_pool.size() < idx + 2) {
+      cudaEvent_t e;
+      cudaError_t r = cudaEventCreate(&e);
+      if (r != cudaSuccess) return r;
+      c->ev_pool.push_back(e);
+    }
+    c->ev_used.push_back({cls, (int)idx});
+  } else {
+    idx = (size_t)c->ev_used.back().second + 1;
+  }
+  return cudaEventRecord(c->ev_pool[idx], st);
+}
+
+SS2_API int ss2_msssim_profile_begin(ss2_msssim *ctx) {
+  if (!ctx) return fail(SS2_EINVAL, "NULL context");
+  ctx->prof = true;
+  ctx->ev_used.clear();
+  return 0;
+}
+
+SS2_API int ss2_msssim_profile_end(ss2_msssim *ctx, double *ms, int *launches) {
+  if (!ctx) return fail(SS2_EINVAL, "NULL context");
+  double t[2] = {0, 0};
+  int n[2] = {0, 0};
+  for (const auto &u : ctx->ev_used) {
+    cudaError_t e = cudaEventSynchronize(ctx->ev_pool[u.second + 1]);
+    float dt = 0.0f;
+    if (e == cudaSuccess)
+      e = cudaEventElapsedTime(&dt, ctx->ev_pool[u.second], ctx->ev_pool[u.second + 1]);
+    if (e != cudaSuccess) {
+      ctx->prof = false;
+      ctx->ev_used.clear();
+      return cuda_fail(e, "MS-SSIM profile events");
+    }
+    t[u.first] += dt;
+    n[u.first] += 1;
+  }
+  ctx->prof = false;
+  ctx->ev_used.clear();
+  for (int i = 0; i < 2; ++i) {
+    if (ms) ms[i] = t[i];
+    if (launches) launches[i] = n[i];
+  }
+  return 0;
+}
+
+// The five scale launches and the final one for nb frames.
+static cudaError_t msssim_batch(ss2_msssim *c, const uint8_t *ref, const uint8_t *dis, int nb,
+                                cudaStream_t st) {
+  const MGeom &g = c->g;
+  cudaError_t e = cudaSuccess;
+  for (int j = 0; j < kScales && e == cudaSuccess; ++j) {
+    e = msssim_mark(c, 0, true, st);
+    if (e != cudaSuccess) break;
+    const dim3 grid(g.tx[j], g.ty[j], nb);
+    if (j > 0)
+      k_msssim_level<2><<<grid, 256, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
+    else if (g.bps == 1)
+      k_msssim_level<0><<<grid, 256, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
+    else
+      k_msssim_level<1><<<grid, 256, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = msssim_mark(c, 0, false, st);
+  }
+  if (e == cudaSuccess) e = msssim_mark(c, 1, true, st);
+  if (e == cudaSuccess) {
+    k_msssim_final<<<nb, kScales * kQ * 32, 0, st>>>(g, c->d_part, c->d_scores, c->d_values);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = msssim_mark(c, 1, false, st);
+  return e;
+}
+
+SS2_API int ss2_msssim_score(ss2_msssim *ctx, const void *ref, const void *dis, int n_frames,
+                             double *scores, double *values, void *stream) {
+  if (!ctx) return fail(SS2_EINVAL, "NULL context");
+  if (n_frames < 0) return fail(SS2_EINVAL, "negative frame count %d", n_frames);
+  if (n_frames == 0) return 0;
+  if (!ref || !dis || !scores) return fail(SS2_EINVAL, "NULL pointer");
+  if ((size_t)n_frames > ctx->h_cap) {
+    if (ctx->h_scores) cudaFreeHost(ctx->h_scores);
+    if (ctx->h_values) cudaFreeHost(ctx->h_values);
+    ctx->h_scores = ctx->h_values = nullptr;
+    ctx->h_cap = 0;
+    if (cudaMallocHost(&ctx->h_scores, (size_t)n_frames * sizeof(double)) != cudaSuccess ||
+        cudaMallocHost(&ctx->h_values, (size_t)n_frames * kScales * kQ * sizeof(double)) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return fail(SS2_ENOMEM, "pinned allocation failed");
+    }
+    ctx->h_cap = (size_t)n_frames;
+  }
+  const MGeom &g = ctx->g;
+  cudaStream_t st = (cudaStream_t)stream;
+  const uint8_t *r8 = (const uint8_t *)ref, *d8 = (const uint8_t *)dis;
+  for (int f0 = 0; f0 < n_frames; f0 += ctx->batch) {
+    const int nb = std::min(ctx->batch, n_frames - f0);
+    cudaError_t e = msssim_batch(ctx, r8 + f0 * g.frame_bytes, d8 + f0 * g.frame_bytes, nb, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ctx->h_scores + f0, ctx->d_scores, nb * sizeof(double),
+                          cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && values)
+      e = cudaMemcpyAsync(ctx->h_values + (size_t)f0 * kScales * kQ, ctx->d_values,
+                          (size_t)nb * kScales * kQ * sizeof(double), cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "MS-SSIM launch");
+  }
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  std::memcpy(scores, ctx->h_scores, (size_t)n_frames * sizeof(double));
+  if (values)
+    std::memcpy(values, ctx->h_values, (size_t)n_frames * kScales * kQ * sizeof(double));
+  return 0;
+}
+
+SS2_API int ss2_msssim_debug_pyramid(ss2_msssim *ctx, const void *ref, const void *dis,
+                                     float *planes, void *stream) {
+  if (!ctx || !ref || !dis || !planes) return fail(SS2_EINVAL, "NULL argument");
+  const MGeom &g = ctx->g;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = msssim_batch(ctx, (const uint8_t *)ref, (const uint8_t *)dis, 1, st);
+  size_t off = 0;
+  for (int img = 0; img < 2 && e == cudaSuccess; ++img)
+    for (int j = 1; j < kScales && e == cudaSuccess; ++j) {
+      e = cudaMemcpy2DAsync(planes + off, g.ws[j] * sizeof(float),
+                            ctx->d_pyr + img * g.img_floats + g.lvl_off[j],
+                            g.pitch[j] * sizeof(float), g.ws[j] * sizeof(float), g.hs[j],
+                            cudaMemcpyDeviceToHost, st);
+      off += (size_t)g.ws[j] * g.hs[j];
+    }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "MS-SSIM pyramid");
+  return 0;
+}

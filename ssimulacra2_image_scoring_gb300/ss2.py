@@ -77,6 +77,18 @@ def lib() -> ctypes.CDLL:
             L.ss2_fssim_profile_begin.restype = i
             L.ss2_fssim_profile_end.argtypes = [vp, vp, vp]
             L.ss2_fssim_profile_end.restype = i
+            L.ss2_msssim_create.argtypes = [i, i, i, i, i]
+            L.ss2_msssim_create.restype = vp
+            L.ss2_msssim_score.argtypes = [vp, vp, vp, i, vp, vp, vp]
+            L.ss2_msssim_score.restype = i
+            L.ss2_msssim_debug_pyramid.argtypes = [vp, vp, vp, vp, vp]
+            L.ss2_msssim_debug_pyramid.restype = i
+            L.ss2_msssim_profile_begin.argtypes = [vp]
+            L.ss2_msssim_profile_begin.restype = i
+            L.ss2_msssim_profile_end.argtypes = [vp, vp, vp]
+            L.ss2_msssim_profile_end.restype = i
+            L.ss2_msssim_destroy.argtypes = [vp]
+            L.ss2_msssim_destroy.restype = None
             L.ss2_fssim_destroy.argtypes = [vp]
             L.ss2_fssim_destroy.restype = None
             L.ss2_frame_bytes.argtypes = [vp]
@@ -214,6 +226,84 @@ class FloatSSIM:
     def close(self) -> None:
         if self._h:
             lib().ss2_fssim_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MSSSIM:
+    """MS-SSIM of the luma plane for one frame geometry (ss2_msssim_create)."""
+
+    SCALES = 5
+    KERNELS = ("k_msssim_level", "k_msssim_final")
+
+    def __init__(self, width: int, height: int, bitdepth: int, chroma: int, batch: int = 0):
+        h = lib().ss2_msssim_create(width, height, bitdepth, chroma, batch)
+        if not h:
+            code, msg = last_error()
+            raise SS2Error(code, msg)
+        self._h = h
+        self.width, self.height = width, height
+
+    def _dims(self):
+        w, h, out = self.width, self.height, []
+        for _ in range(self.SCALES):
+            out.append((w, h))
+            w, h = (w + 1) // 2, (h + 1) // 2
+        return out
+
+    def score(self, ref, dis, stream=None, values: bool = False):
+        """Scores (n,), and with values=True also the per-scale means
+        (n, 5, 5): l, c, s, cs, l cs."""
+        import torch
+        for t in (ref, dis):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+                raise TypeError("frames must be contiguous CUDA tensors")
+        n = ref.shape[0]
+        out = np.zeros(n, np.float64)
+        v = np.zeros((n, self.SCALES, 5), np.float64) if values else None
+        _check(lib().ss2_msssim_score(self._h, ref.data_ptr(), dis.data_ptr(), n, out.ctypes.data,
+                                      v.ctypes.data if values else None, _stream_handle(stream)))
+        return (out, v) if values else out
+
+    def pyramid(self, ref, dis, stream=None):
+        """Scales 2..5 of the first frame pair: ([ref planes], [dis planes])."""
+        dims = self._dims()[1:]
+        total = sum(w * h for w, h in dims)
+        buf = np.zeros(2 * total, np.float32)
+        _check(lib().ss2_msssim_debug_pyramid(self._h, ref.data_ptr(), dis.data_ptr(),
+                                              buf.ctypes.data, _stream_handle(stream)))
+        out, off = [], 0
+        for _ in range(2):
+            planes = []
+            for w, h in dims:
+                planes.append(buf[off:off + w * h].reshape(h, w))
+                off += w * h
+            out.append(planes)
+        return out[0], out[1]
+
+    def profile_begin(self) -> None:
+        _check(lib().ss2_msssim_profile_begin(self._h))
+
+    def profile_end(self) -> dict:
+        ms = np.zeros(2, np.float64)
+        n = np.zeros(2, np.int32)
+        _check(lib().ss2_msssim_profile_end(self._h, ms.ctypes.data, n.ctypes.data))
+        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
+
+    def close(self) -> None:
+        if self._h:
+            lib().ss2_msssim_destroy(self._h)
             self._h = None
 
     def __enter__(self):
