@@ -93,8 +93,8 @@ def byte_model(spec) -> dict:
 # ---------------------------------------------------------------------------
 
 KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h"]
-FSSIM_SOURCES = ["fssim.cu", "ss2_tma.cuh"]
-MSSSIM_SOURCES = ["msssim.cu"]
+FSSIM_SOURCES = ["fssim.cu", "ss2_tma.cuh", "ss2_f32x2.cuh"]
+MSSSIM_SOURCES = ["msssim.cu", "ss2_f32x2.cuh"]
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:

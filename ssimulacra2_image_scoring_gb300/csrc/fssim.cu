@@ -22,10 +22,11 @@
 //                     2^61), or for a power-of-two scale, where every tap is
 //                     exact, the raw sample sum; one conversion rounds it.
 //   k_fssim_map       32x16 map tiles: separable 11-tap Gaussian sums of
-//                     x1, x2, x1^2, x2^2, x1 x2 in fp32 on samples shifted by
-//                     a per-tile offset (variances and covariance do not
-//                     change, cancellation does), SSIM per pixel, one
-//                     fixed-order fp64 block sum.
+//                     x1, x2, x1^2, x2^2, x1 x2 in fp32 as three packed pairs
+//                     (fma.rn.f32x2) on samples shifted by a per-tile offset
+//                     (variances and covariance do not change, cancellation
+//                     does), SSIM per pixel, fp32 warp sums in a fixed tree
+//                     and an fp64 sum of the block's warps.
 //   k_fssim_final     per frame: block sums in a fixed warp order (fp64), mean.
 #include <cuda_runtime.h>
 
@@ -38,6 +39,7 @@
 #include <vector>
 
 #include "../../include/ss2.h"
+#include "ss2_f32x2.cuh"
 #include "ss2_host.h"
 #include "ss2_tma.cuh"
 
@@ -470,11 +472,12 @@ __global__ void __launch_bounds__(256)
 
 __global__ void __launch_bounds__(256)
     k_fssim_map(FGeom g, const float *__restrict__ D, double *__restrict__ part) {
-  // P: the shifted samples a, b and the products a a, b b, a b of the input
-  // tile; H: their horizontal Gaussian sums for every input row
-  __shared__ float P[5][kInY][kInX + 1];
-  __shared__ float H[5][kInY][kTileX];
-  __shared__ double red[256];
+  // the five quantities as three fp32 pairs (a, b), (a a, b b), (a b, 0):
+  // PP for the input tile, HH for the horizontal sums of every input row
+  // (rows padded by one pair: the horizontal pass runs row-fastest)
+  __shared__ __align__(16) f2 PP[3][kInY][kInX + 1];
+  __shared__ __align__(16) f2 HH[3][kInY][kTileX + 1];
+  __shared__ float wsum[8];
   const int frame = blockIdx.z;
   const int ox0 = blockIdx.x * kTileX, oy0 = blockIdx.y * kTileY;
   const float *pa = D + (long long)frame * 2 * g.plane;
@@ -482,32 +485,50 @@ __global__ void __launch_bounds__(256)
   const int t = threadIdx.x;
   // per-tile offset: the reference sample at the tile origin (same for both)
   const float off = pa[(long long)oy0 * g.pitch + ox0];
-  for (int i = t; i < kInY * kInX; i += 256) {
-    const int r = i / kInX, c = i % kInX;
-    const int y = min(oy0 + r, g.hd - 1), x = min(ox0 + c, g.wd - 1);
-    const float p = __fsub_rn(pa[(long long)y * g.pitch + x], off);
-    const float q = __fsub_rn(pb[(long long)y * g.pitch + x], off);
-    P[0][r][c] = p;
-    P[1][r][c] = q;
-    P[2][r][c] = __fmul_rn(p, p);
-    P[3][r][c] = __fmul_rn(q, q);
-    P[4][r][c] = __fmul_rn(p, q);
+  // every load of a thread is issued before the first is used
+  constexpr int kPer = (kInY * kInX + 255) / 256;
+  float va[kPer], vb[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = t + 256 * k;
+    if (i < kInY * kInX) {
+      const int r = i / kInX, c = i % kInX;
+      const int y = min(oy0 + r, g.hd - 1), x = min(ox0 + c, g.wd - 1);
+      va[k] = pa[(long long)y * g.pitch + x];
+      vb[k] = pb[(long long)y * g.pitch + x];
+    }
   }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = t + 256 * k;
+    if (i < kInY * kInX) {
+      const int r = i / kInX, c = i % kInX;
+      const float p = __fsub_rn(va[k], off);
+      const float q = __fsub_rn(vb[k], off);
+      PP[0][r][c] = f2_pack(p, q);
+      PP[1][r][c] = f2_pack(__fmul_rn(p, p), __fmul_rn(q, q));
+      PP[2][r][c] = f2_pack(__fmul_rn(p, q), 0.0f);
+    }
+  }
+  f2 gk[kWin];
+#pragma unroll
+  for (int k = 0; k < kWin; ++k) gk[k] = f2_pack(g.gauss[k], g.gauss[k]);
   __syncthreads();
-  // horizontal sums: a thread takes 4 adjacent outputs of one input row
+  // horizontal sums: a thread takes 4 adjacent outputs of one input row,
+  // rows fastest across threads (conflict-free 64-bit shared accesses)
   if (t < kInY * (kTileX / 4)) {
-    const int r = t / (kTileX / 4), c0 = 4 * (t % (kTileX / 4));
+    const int r = t % kInY, c0 = 4 * (t / kInY);
 #pragma unroll
-    for (int q = 0; q < 5; ++q) {
-      float v[kWin + 3];
+    for (int q = 0; q < 3; ++q) {
+      f2 v[kWin + 3];
 #pragma unroll
-      for (int k = 0; k < kWin + 3; ++k) v[k] = P[q][r][c0 + k];
+      for (int k = 0; k < kWin + 3; ++k) v[k] = PP[q][r][c0 + k];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float acc = 0.0f;
+        f2 acc = 0ull;
 #pragma unroll
-        for (int k = 0; k < kWin; ++k) acc = __fmaf_rn(g.gauss[k], v[j + k], acc);
-        H[q][r][c0 + j] = acc;
+        for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[j + k], acc);
+        HH[q][r][c0 + j] = acc;
       }
     }
   }
@@ -515,47 +536,53 @@ __global__ void __launch_bounds__(256)
   // vertical sums and the SSIM terms of two outputs (rows 2 oy, 2 oy + 1)
   const int oc = t % kTileX, orow = 2 * (t / kTileX);
   const int ox = ox0 + oc;
-  float m[2][5];
+  f2 m[2][3];
 #pragma unroll
-  for (int q = 0; q < 5; ++q) {
-    float v[kWin + 1];
+  for (int q = 0; q < 3; ++q) {
+    f2 v[kWin + 1];
 #pragma unroll
-    for (int k = 0; k < kWin + 1; ++k) v[k] = H[q][orow + k][oc];
+    for (int k = 0; k < kWin + 1; ++k) v[k] = HH[q][orow + k][oc];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      float acc = 0.0f;
+      f2 acc = 0ull;
 #pragma unroll
-      for (int k = 0; k < kWin; ++k) acc = __fmaf_rn(g.gauss[k], v[j + k], acc);
+      for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[j + k], acc);
       m[j][q] = acc;
     }
   }
-  double tile = 0.0;
+  float tile = 0.0f;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int oy = oy0 + orow + j;
     if (ox < g.ow && oy < g.oh) {
-      const float m1 = m[j][0], m2 = m[j][1];
-      const float v1 = __fsub_rn(m[j][2], __fmul_rn(m1, m1));
-      const float v2 = __fsub_rn(m[j][3], __fmul_rn(m2, m2));
-      const float cv = __fsub_rn(m[j][4], __fmul_rn(m1, m2));
+      float m1, m2, e11, e22, e12, unused;
+      f2_unpack(m[j][0], m1, m2);
+      f2_unpack(m[j][1], e11, e22);
+      f2_unpack(m[j][2], e12, unused);
+      const float v1 = __fsub_rn(e11, __fmul_rn(m1, m1));
+      const float v2 = __fsub_rn(e22, __fmul_rn(m2, m2));
+      const float cv = __fsub_rn(e12, __fmul_rn(m1, m2));
       const float mu1 = __fadd_rn(m1, off), mu2 = __fadd_rn(m2, off);
       const float num = __fmul_rn(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(mu1, mu2)), g.C1),
                                   __fadd_rn(__fmul_rn(2.0f, cv), g.C2));
       const float den = __fmul_rn(
           __fadd_rn(__fadd_rn(__fmul_rn(mu1, mu1), __fmul_rn(mu2, mu2)), g.C1),
           __fadd_rn(__fadd_rn(v1, v2), g.C2));
-      tile = __dadd_rn(tile, (double)__fdiv_rn(num, den));
+      tile = __fadd_rn(tile, __fdiv_rn(num, den));
     }
   }
-  red[t] = tile;
-  __syncthreads();
+  // warp sums in fp32 (a fixed xor tree; lane 0's order is fixed), then the
+  // block's eight warp sums in fp64 in warp order (fp64 is slow on this part)
 #pragma unroll
-  for (int s = 128; s > 0; s >>= 1) {
-    if (t < s) red[t] = __dadd_rn(red[t], red[t + s]);
-    __syncthreads();
+  for (int o = 16; o > 0; o >>= 1) tile = __fadd_rn(tile, __shfl_xor_sync(0xffffffffu, tile, o));
+  if ((t & 31) == 0) wsum[t >> 5] = tile;
+  __syncthreads();
+  if (t == 0) {
+    double acc = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc = __dadd_rn(acc, (double)wsum[w]);
+    part[(long long)frame * g.tiles_x * g.tiles_y + blockIdx.y * g.tiles_x + blockIdx.x] = acc;
   }
-  if (t == 0)
-    part[(long long)frame * g.tiles_x * g.tiles_y + blockIdx.y * g.tiles_x + blockIdx.x] = red[0];
 }
 
 // One warp per frame: lane l adds the block sums l, l + 32, ... in order,

@@ -18,9 +18,12 @@
 //                   (raw luma at scale 1, fp32 planes after), shifted by
 //                   the tile's first reference sample (variances and
 //                   covariance do not change, cancellation does); the five
-//                   Gaussian means in fp32 (separable, products formed once
-//                   per pixel); l, c, s, cs, l cs per position; a fixed fp64
-//                   tree per block into the (frame, scale, tile) span.  It
+//                   Gaussian means in fp32 as three packed pairs (separable,
+//                   fma.rn.f32x2, products formed once per pixel); l, c, s,
+//                   cs, l cs per position (approximate reciprocals and root
+//                   refined to about an ulp); sums in fp32 per warp (fixed
+//                   tree) and fp64 over the block's warps into the (frame,
+//                   scale, tile) span (fp64 is slow on this part).  It
 //                   also writes its share of the next scale: 2x2 means,
 //                   exact in fp32 (a level-5 value is at most 2^24 units of
 //                   2^-16, so every partial sum is representable).
@@ -35,6 +38,7 @@
 #include <vector>
 
 #include "../../include/ss2.h"
+#include "ss2_f32x2.cuh"
 #include "ss2_host.h"
 
 #define SS2_API extern "C" __attribute__((visibility("default")))
@@ -77,12 +81,40 @@ __device__ __forceinline__ float sample(const MGeom &g, int j, const uint8_t *__
   return __ldg(plane + (long long)y * g.pitch[j] + x);
 }
 
+// The terms need about 1e-7 relative, not IEEE exactness: quotients from
+// the approximate reciprocal (MUFU) and one Newton step on the residual
+// (Markstein, IBM J. Res. Dev. 34(1), 1990), faithful to about an ulp; the
+// square root from the approximate MUFU root (relative error near 2^-22).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float r;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// a / b given rb ~ 1 / b
+__device__ __forceinline__ float div_by(float a, float b, float rb) {
+  const float q = __fmul_rn(a, rb);
+  return __fmaf_rn(__fmaf_rn(-q, b, a), rb, q);
+}
+
+__device__ __forceinline__ float div_fast(float a, float b) { return div_by(a, b, rcp_approx(b)); }
+
 template <int MODE>
 __global__ void __launch_bounds__(256)
     k_msssim_level(MGeom g, int j, const uint8_t *__restrict__ ref, const uint8_t *__restrict__ dis,
                    float *__restrict__ pyr, double *__restrict__ part) {
-  __shared__ __align__(16) float P[kQ][kIY][kIX + 1];   // later: the block's fp64 sums
-  __shared__ float H[kQ][kIY][kTX];
+  // the five quantities as three fp32 pairs (p, q), (p p, q q), (p q, 0):
+  // PP for the input tile, HH for the horizontal sums of every input row
+  // (rows padded by one pair: the horizontal pass runs row-fastest)
+  __shared__ __align__(16) f2 PP[3][kIY][kIX + 1];
+  __shared__ __align__(16) f2 HH[3][kIY][kTX + 1];
+  __shared__ float wsum[8][kQ];
   const int frame = blockIdx.z, t = threadIdx.x;
   const int W = g.ws[j], Hh = g.hs[j];
   const int ox0 = blockIdx.x * kTX, oy0 = blockIdx.y * kTY;
@@ -92,7 +124,40 @@ __global__ void __launch_bounds__(256)
   const float *pa = pyr + (long long)(2 * frame) * g.img_floats + g.lvl_off[j];
   const float *pb = pa + g.img_floats;
 
-  // the 2x2 means of this block's share of the next scale
+  // input tile (clamped to the plane), shifted by the tile's first reference
+  // sample; every load of a thread is issued before the first is used
+  const float off = sample<MODE>(g, j, ra, pa, ox0, oy0);
+  constexpr int kPer = (kIY * kIX + 255) / 256;
+  float va[kPer], vb[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = t + 256 * k;
+    if (i < kIY * kIX) {
+      const int r = i / kIX, c = i % kIX;
+      const int y = min(oy0 + r, Hh - 1), x = min(ox0 + c, W - 1);
+      va[k] = sample<MODE>(g, j, ra, pa, x, y);
+      vb[k] = sample<MODE>(g, j, rb, pb, x, y);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = t + 256 * k;
+    if (i < kIY * kIX) {
+      const int r = i / kIX, c = i % kIX;
+      const float p = __fsub_rn(va[k], off);     // exact: both lie on the same grid below 256
+      const float q = __fsub_rn(vb[k], off);
+      PP[0][r][c] = f2_pack(p, q);
+      PP[1][r][c] = f2_pack(__fmul_rn(p, p), __fmul_rn(q, q));
+      PP[2][r][c] = f2_pack(__fmul_rn(p, q), 0.0f);
+    }
+  }
+  f2 gk[kWin];
+#pragma unroll
+  for (int k = 0; k < kWin; ++k) gk[k] = f2_pack(g.gauss[k], g.gauss[k]);
+  __syncthreads();
+
+  // the 2x2 means of this block's share of the next scale, from the tile
+  // (p + off restores each sample exactly; clamping matches the tile's)
   if (j + 1 < kScales) {
     const int Wn = g.ws[j + 1], Hn = g.hs[j + 1];
     const int X0 = blockIdx.x * (kTX / 2), Y0 = blockIdx.y * (kTY / 2);
@@ -103,48 +168,37 @@ __global__ void __launch_bounds__(256)
     float *nb = na + g.img_floats;
     for (int i = t; i < n; i += 256) {
       const int X = X0 + i % nx, Y = Y0 + i / nx;
-      const int x0 = 2 * X, x1 = min(2 * X + 1, W - 1), y0 = 2 * Y, y1 = min(2 * Y + 1, Hh - 1);
-      const float a = __fadd_rn(__fadd_rn(sample<MODE>(g, j, ra, pa, x0, y0),
-                                          sample<MODE>(g, j, ra, pa, x1, y0)),
-                                __fadd_rn(sample<MODE>(g, j, ra, pa, x0, y1),
-                                          sample<MODE>(g, j, ra, pa, x1, y1)));
-      const float b = __fadd_rn(__fadd_rn(sample<MODE>(g, j, rb, pb, x0, y0),
-                                          sample<MODE>(g, j, rb, pb, x1, y0)),
-                                __fadd_rn(sample<MODE>(g, j, rb, pb, x0, y1),
-                                          sample<MODE>(g, j, rb, pb, x1, y1)));
+      const int c0 = 2 * X - ox0, c1 = min(2 * X + 1, W - 1) - ox0;
+      const int r0 = 2 * Y - oy0, r1 = min(2 * Y + 1, Hh - 1) - oy0;
+      float a00, b00, a01, b01, a10, b10, a11, b11;
+      f2_unpack(PP[0][r0][c0], a00, b00);
+      f2_unpack(PP[0][r0][c1], a01, b01);
+      f2_unpack(PP[0][r1][c0], a10, b10);
+      f2_unpack(PP[0][r1][c1], a11, b11);
+      const float a = __fadd_rn(__fadd_rn(__fadd_rn(a00, off), __fadd_rn(a01, off)),
+                                __fadd_rn(__fadd_rn(a10, off), __fadd_rn(a11, off)));
+      const float b = __fadd_rn(__fadd_rn(__fadd_rn(b00, off), __fadd_rn(b01, off)),
+                                __fadd_rn(__fadd_rn(b10, off), __fadd_rn(b11, off)));
       na[(long long)Y * g.pitch[j + 1] + X] = __fmul_rn(a, 0.25f);
       nb[(long long)Y * g.pitch[j + 1] + X] = __fmul_rn(b, 0.25f);
     }
   }
 
-  // input tile, shifted by the tile's first reference sample
-  const float off = sample<MODE>(g, j, ra, pa, ox0, oy0);
-  for (int i = t; i < kIY * kIX; i += 256) {
-    const int r = i / kIX, c = i % kIX;
-    const int y = min(oy0 + r, Hh - 1), x = min(ox0 + c, W - 1);
-    const float p = __fsub_rn(sample<MODE>(g, j, ra, pa, x, y), off);
-    const float q = __fsub_rn(sample<MODE>(g, j, rb, pb, x, y), off);
-    P[0][r][c] = p;
-    P[1][r][c] = q;
-    P[2][r][c] = __fmul_rn(p, p);
-    P[3][r][c] = __fmul_rn(q, q);
-    P[4][r][c] = __fmul_rn(p, q);
-  }
-  __syncthreads();
-  // horizontal sums: a thread takes 4 adjacent positions of one input row
+  // horizontal sums: a thread takes 4 adjacent positions of one input row,
+  // rows fastest across threads (conflict-free 64-bit shared accesses)
   if (t < kIY * (kTX / 4)) {
-    const int r = t / (kTX / 4), c0 = 4 * (t % (kTX / 4));
+    const int r = t % kIY, c0 = 4 * (t / kIY);
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-      float v[kWin + 3];
+    for (int q = 0; q < 3; ++q) {
+      f2 v[kWin + 3];
 #pragma unroll
-      for (int k = 0; k < kWin + 3; ++k) v[k] = P[q][r][c0 + k];
+      for (int k = 0; k < kWin + 3; ++k) v[k] = PP[q][r][c0 + k];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float acc = 0.0f;
+        f2 acc = 0ull;                                   // (+0, +0)
 #pragma unroll
-        for (int k = 0; k < kWin; ++k) acc = __fmaf_rn(g.gauss[k], v[i + k], acc);
-        H[q][r][c0 + i] = acc;
+        for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[i + k], acc);
+        HH[q][r][c0 + i] = acc;
       }
     }
   }
@@ -152,60 +206,67 @@ __global__ void __launch_bounds__(256)
   // vertical sums and the terms of two positions (rows 2 oy, 2 oy + 1)
   const int oc = t % kTX, orow = 2 * (t / kTX);
   const int ox = ox0 + oc;
-  float m[2][kQ];
+  f2 m[2][3];
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
-    float v[kWin + 1];
+  for (int q = 0; q < 3; ++q) {
+    f2 v[kWin + 1];
 #pragma unroll
-    for (int k = 0; k < kWin + 1; ++k) v[k] = H[q][orow + k][oc];
+    for (int k = 0; k < kWin + 1; ++k) v[k] = HH[q][orow + k][oc];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      float acc = 0.0f;
+      f2 acc = 0ull;
 #pragma unroll
-      for (int k = 0; k < kWin; ++k) acc = __fmaf_rn(g.gauss[k], v[i + k], acc);
+      for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[i + k], acc);
       m[i][q] = acc;
     }
   }
-  double sum[kQ] = {0, 0, 0, 0, 0};
+  float sum[kQ] = {0, 0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int oy = oy0 + orow + i;
     if (ox < ow && oy < oh) {
-      const float m1 = m[i][0], m2 = m[i][1];
-      const float v1 = fmaxf(__fsub_rn(m[i][2], __fmul_rn(m1, m1)), 0.0f);
-      const float v2 = fmaxf(__fsub_rn(m[i][3], __fmul_rn(m2, m2)), 0.0f);
-      const float cv = __fsub_rn(m[i][4], __fmul_rn(m1, m2));
+      float m1, m2, e11, e22, e12, unused;
+      f2_unpack(m[i][0], m1, m2);
+      f2_unpack(m[i][1], e11, e22);
+      f2_unpack(m[i][2], e12, unused);
+      const float v1 = fmaxf(__fsub_rn(e11, __fmul_rn(m1, m1)), 0.0f);
+      const float v2 = fmaxf(__fsub_rn(e22, __fmul_rn(m2, m2)), 0.0f);
+      const float cv = __fsub_rn(e12, __fmul_rn(m1, m2));
       const float mu1 = __fadd_rn(m1, off), mu2 = __fadd_rn(m2, off);
-      const float sd1 = __fsqrt_rn(v1), sd2 = __fsqrt_rn(v2);
+      // s1 s2 = sqrt(v1 v2) (0 for a flat window); c and cs share 1 / vden
+      const float sd12 = sqrt_approx(__fmul_rn(v1, v2));
       const float vden = __fadd_rn(__fadd_rn(v1, v2), g.C2);
-      const float l = __fdiv_rn(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(mu1, mu2)), g.C1),
-                                __fadd_rn(__fadd_rn(__fmul_rn(mu1, mu1), __fmul_rn(mu2, mu2)), g.C1));
-      const float c = __fdiv_rn(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(sd1, sd2)), g.C2), vden);
-      const float s = __fdiv_rn(__fadd_rn(cv, g.C3), __fadd_rn(__fmul_rn(sd1, sd2), g.C3));
-      const float cs = __fdiv_rn(__fadd_rn(__fmul_rn(2.0f, cv), g.C2), vden);
-      sum[0] = __dadd_rn(sum[0], (double)l);
-      sum[1] = __dadd_rn(sum[1], (double)c);
-      sum[2] = __dadd_rn(sum[2], (double)s);
-      sum[3] = __dadd_rn(sum[3], (double)cs);
-      sum[4] = __dadd_rn(sum[4], __dmul_rn((double)l, (double)cs));
+      const float rv = rcp_approx(vden);
+      const float l = div_fast(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(mu1, mu2)), g.C1),
+                               __fadd_rn(__fadd_rn(__fmul_rn(mu1, mu1), __fmul_rn(mu2, mu2)), g.C1));
+      const float c = div_by(__fadd_rn(__fmul_rn(2.0f, sd12), g.C2), vden, rv);
+      const float s = div_fast(__fadd_rn(cv, g.C3), __fadd_rn(sd12, g.C3));
+      const float cs = div_by(__fadd_rn(__fmul_rn(2.0f, cv), g.C2), vden, rv);
+      sum[0] = __fadd_rn(sum[0], l);
+      sum[1] = __fadd_rn(sum[1], c);
+      sum[2] = __fadd_rn(sum[2], s);
+      sum[3] = __fadd_rn(sum[3], cs);
+      sum[4] = __fadd_rn(sum[4], __fmul_rn(l, cs));
     }
   }
-  // P is no longer read (the horizontal pass ended before the last barrier)
-  double(*red)[256] = reinterpret_cast<double(*)[256]>(&P[0][0][0]);
+  // warp sums in fp32 (a fixed xor tree; lane 0's order is fixed), then the
+  // block's eight warp sums in fp64 in warp order
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) red[q][t] = sum[q];
+  for (int q = 0; q < kQ; ++q) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum[q] = __fadd_rn(sum[q], __shfl_xor_sync(0xffffffffu, sum[q], o));
+  }
+  if ((t & 31) == 0) {
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) wsum[t >> 5][q] = sum[q];
+  }
   __syncthreads();
-#pragma unroll
-  for (int st = 128; st > 0; st >>= 1) {
-    if (t < st) {
-#pragma unroll
-      for (int q = 0; q < kQ; ++q) red[q][t] = __dadd_rn(red[q][t], red[q][t + st]);
-    }
-    __syncthreads();
-  }
   if (t < kQ) {
+    double acc = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc = __dadd_rn(acc, (double)wsum[w][t]);
     const long long tile = g.tile_off[j] + blockIdx.y * g.tx[j] + blockIdx.x;
-    part[((long long)frame * g.tiles_total + tile) * kQ + t] = red[t][0];
+    part[((long long)frame * g.tiles_total + tile) * kQ + t] = acc;
   }
 }
 
