@@ -20,7 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
 SO_PATH = os.path.join(BUILD_DIR, "libss2_oracle.so")
 SOURCES = [os.path.join(HERE, "ss2_oracle.c"), os.path.join(HERE, "fssim_oracle.c"),
-           os.path.join(HERE, "msssim_oracle.c")]
+           os.path.join(HERE, "msssim_oracle.c"), os.path.join(HERE, "cambi_oracle.c")]
 HEADERS = [os.path.join(HERE, "ss2_oracle.h")]
 
 NPARAMS = 133
@@ -104,6 +104,12 @@ def lib() -> ctypes.CDLL:
             L.ss2o_fssim_decimate.restype = i
             L.ss2o_fssim.argtypes = [vp, vp, i, i, i, vp, vp, vp]
             L.ss2o_fssim.restype = i
+            L.ss2o_cambi_recip.argtypes = [i]
+            L.ss2o_cambi_recip.restype = ctypes.c_float
+            L.ss2o_cambi_cvalues.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
+            L.ss2o_cambi_cvalues.restype = i
+            L.ss2o_cambi_topk.argtypes = [vp, ctypes.c_long, ctypes.c_long, vp, vp, vp, vp]
+            L.ss2o_cambi_topk.restype = i
             L.ss2o_msssim_dims.argtypes = [i, i, vp]
             L.ss2o_msssim_dims.restype = None
             L.ss2o_msssim_pyramid_len.argtypes = [i, i]
@@ -276,6 +282,38 @@ def fssim(ref: np.ndarray, dis: np.ndarray, w: int, h: int, depth: int):
     if rc != 0:
         raise ValueError(f"fssim rejected {w}x{h}: rc={rc}")
     return float(sc[0]), a, b
+
+
+def cambi_recip(n: int) -> float:
+    return float(lib().ss2o_cambi_recip(n))
+
+
+def cambi_cvalues(levels: np.ndarray, window: int, diffs, weights, mask=None) -> np.ndarray:
+    """c-values of one level plane (h x w uint16 levels below 1024)."""
+    lv = np.ascontiguousarray(levels, dtype=np.uint16)
+    h, w = lv.shape
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+    d = np.ascontiguousarray(diffs, dtype=np.int32)
+    wt = np.ascontiguousarray(weights, dtype=np.int32)
+    out = np.zeros((h, w), np.float32)
+    rc = lib().ss2o_cambi_cvalues(_ptr(lv), _ptr(m), w, h, window, len(d), _ptr(d), _ptr(wt),
+                                  _ptr(out))
+    if rc != 0:
+        raise ValueError(f"cambi c-values rejected: rc={rc}")
+    return out
+
+
+def cambi_topk(c: np.ndarray, k: int):
+    """(exact sum in units of 2^-24 as a Python int, k-th largest value, mean)."""
+    cc = np.ascontiguousarray(c, dtype=np.float32).ravel()
+    lo = np.zeros(1, np.uint64)
+    hi = np.zeros(1, np.uint64)
+    t = np.zeros(1, np.float32)
+    mean = np.zeros(1, np.float64)
+    rc = lib().ss2o_cambi_topk(_ptr(cc), cc.size, k, _ptr(lo), _ptr(hi), _ptr(t), _ptr(mean))
+    if rc != 0:
+        raise ValueError(f"cambi top-k rejected: rc={rc}")
+    return (int(hi[0]) << 64) | int(lo[0]), float(t[0]), float(mean[0])
 
 
 MSSSIM_SCALES = 5

@@ -28,6 +28,7 @@
 #define SS2_ORACLE_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -109,6 +110,18 @@ int ss2o_fssim(const void *ref, const void *dis, int width, int height,
  * samples in the 8-bit range), and the score of a pair with the per-scale
  * means values[5][5] = (l, c, s, cs, l cs) per scale (may be NULL).
  * -22 bad arguments, -95 a scale-5 plane below 11x11.                      */
+/* CAMBI c-values and top-K pool (cambi_oracle.c).  levels: w x h 10-bit
+ * levels (< 1024); mask: w x h bytes, nonzero = counted, or NULL; window
+ * odd with window^2 <= 4225; ndiff 1..4 (d >= 1, w in 1..9); out: w x h
+ * floats.  topk: the exact top-k sum of c in units of 2^-24 (128 bits as
+ * lo, hi), the k-th largest value and the mean.  -22 bad arguments.       */
+float ss2o_cambi_recip(int n);
+int ss2o_cambi_cvalues(const uint16_t *levels, const uint8_t *mask, int w, int h,
+                       int window, int ndiff, const int *diffs, const int *weights,
+                       float *out);
+int ss2o_cambi_topk(const float *c, long n, long k, uint64_t *sum_lo,
+                    uint64_t *sum_hi, float *threshold, double *mean);
+
 void ss2o_msssim_dims(int width, int height, int *dims);
 size_t ss2o_msssim_pyramid_len(int width, int height);
 int ss2o_msssim_pyramid(const void *frame, int width, int height, int bitdepth,

@@ -95,7 +95,22 @@ MSSSIM_MUTATIONS = {
                                      "for (int j = 0; j < NSCALE - 2; ++j) ms *= pow(m[j][3], kBeta[j]);"),
 }
 
+# Planted slips in the CAMBI oracle, caught by tests/test_cambi_pins.py.
+CAMBI_MUTATIONS = {
+    "cambi_window_radius_short": ("const int r = window / 2;", "const int r = window / 2 - 1;"),
+    "cambi_diff_downwards": ("if (v == L + diffs[i]) ++pm[i];", "if (v == L - diffs[i]) ++pm[i];"),
+    "cambi_weight_ignored": ("const long num = (long)weights[i] * p0 * pm[i];",
+                             "const long num = (long)p0 * pm[i];"),
+    "cambi_reciprocal_off_by_one": ("ss2o_cambi_recip((int)(p0 + pm[i]));",
+                                    "ss2o_cambi_recip((int)(p0 + pm[i] + 1));"),
+    "cambi_mask_not_applied_to_counts": ("if (mask && !mask[j]) continue;", "(void)j;"),
+    "cambi_ties_counted_as_above": ("if (c[i] > T) {", "if (c[i] >= T) {"),
+    "cambi_recip_in_double": ("return 1.0f / (float)n;   /* IEEE division: correctly rounded */",
+                              "return (float)(1.0 / (double)n + 1e-12);"),
+}
+
 CASES = {**{n: ("ss2_oracle.c", "test_oracle_pins.py") for n in MUTATIONS},
+         **{n: ("cambi_oracle.c", "test_cambi_pins.py") for n in CAMBI_MUTATIONS},
          **{n: ("fssim_oracle.c", "test_fssim_pins.py") for n in FSSIM_MUTATIONS},
          **{n: ("msssim_oracle.c", "test_msssim_pins.py") for n in MSSSIM_MUTATIONS}}
 
@@ -103,7 +118,7 @@ CASES = {**{n: ("ss2_oracle.c", "test_oracle_pins.py") for n in MUTATIONS},
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_planted_mistake_fails_the_pins(name, tmp_path):
     target, pins = CASES[name]
-    old, new = {**MUTATIONS, **FSSIM_MUTATIONS, **MSSSIM_MUTATIONS}[name]
+    old, new = {**MUTATIONS, **FSSIM_MUTATIONS, **MSSSIM_MUTATIONS, **CAMBI_MUTATIONS}[name]
     srcs = []
     for path in oracle.SOURCES:
         text = open(path).read()
