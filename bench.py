@@ -9,7 +9,8 @@ C ABI.  Prints one JSON line.
 
 --feature fssim times float_ssim with device decimation instead (frames/s on
 the same workload; the oracle's float_ssim as the CPU baseline); --feature
-msssim times MS-SSIM of the luma plane the same way.
+msssim times MS-SSIM of the luma plane the same way; --feature cambi times
+CAMBI c-values and top-K pooling of the distorted luma as 10-bit levels.
 
 --impl ours (default): frames resident in HBM, W untimed steps, then K steps
 timed with CUDA events on the scoring stream between a barrier and a
@@ -49,6 +50,16 @@ import synth  # noqa: E402
 METRIC = "SSIMULACRA2 frames/sec at 3840x2160 8-bit 4:2:0; HBM GB/s vs GB300 peak"
 FSSIM_METRIC = "float_ssim (device decimation) frames/sec; HBM GB/s vs GB300 peak"
 MSSSIM_METRIC = "MS-SSIM (luma, 5 scales) frames/sec; FP32 TFLOP/s vs GB300 peak"
+CAMBI_METRIC = ("CAMBI c-values (65x65 window) + top-K frames/sec; "
+                "window updates/s vs GB300 shared-memory pipe")
+# CAMBI benchmark configuration (not CAMBI defaults: the pages give none):
+# 8-bit luma as 10-bit levels (x 4), the largest window, diffs of one to four
+# 8-bit code values weighted 1..4, the top quarter of the pixels pooled.
+CAMBI_WINDOW = 65
+CAMBI_DIFFS = (4, 8, 12, 16)
+CAMBI_WEIGHTS = (1, 2, 3, 4)
+# one 32-lane shared-memory operation per SM per clock: 152 x 32 x 2,070 MHz
+SMEM_OPS_PEAK = 152 * 32 * 2070.0e6
 # FP32 peak for ALU-bound kernels: 152 SMs x 128 FP32 lanes x 2 flops x the
 # SM clock (2,070 MHz maximum): 80.5 TFLOP/s.
 FP32_LANES = 152 * 128
@@ -95,6 +106,7 @@ def byte_model(spec) -> dict:
 KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h"]
 FSSIM_SOURCES = ["fssim.cu", "ss2_tma.cuh", "ss2_f32x2.cuh"]
 MSSSIM_SOURCES = ["msssim.cu", "ss2_f32x2.cuh"]
+CAMBI_SOURCES = ["cambi.cu"]
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
@@ -261,16 +273,29 @@ def run_reference(args, ws, rank):
     wl = synth.make(args.workload, per_step, workers=min(per_step, cores))
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; the first step pays nothing extra
-    leg, metric = {"fssim": (oracle_fssim_throughput, FSSIM_METRIC),
-                   "msssim": (oracle_msssim_throughput, MSSSIM_METRIC)}.get(
-        args.feature, (oracle_throughput, METRIC))
+    if args.feature == "cambi":
+        # the oracle's brute-force window scan is slow: a sixteenth of each
+        # frame (a full-width band) per thread, counted as a sixteenth
+        lv = cambi_levels(wl)[:, :spec.height // 16, :]
+        kb = (spec.height // 16) * spec.width // 4
+
+        def leg(_wl, n_frames, threads):
+            return oracle_cambi_throughput(lv, n_frames, threads, kb)
+        metric = CAMBI_METRIC
+        scale = 1.0 / 16.0
+    else:
+        leg, metric = {"fssim": (oracle_fssim_throughput, FSSIM_METRIC),
+                       "msssim": (oracle_msssim_throughput, MSSSIM_METRIC)}.get(
+            args.feature, (oracle_throughput, METRIC))
+        scale = 1.0
     t0 = time.perf_counter()
     for _ in range(args.steps):
         leg(wl, per_step, per_step)
     dt = time.perf_counter() - t0
-    fps = per_step * args.steps / dt
+    fps = scale * per_step * args.steps / dt
     sample = (f"{per_step} frames of {spec.name} per step, one oracle thread per frame "
-              f"on {per_step} host cores")
+              f"on {per_step} host cores" + ("; CAMBI: a full-width sixteenth of each frame, "
+                                             "scaled to frames" if scale != 1.0 else ""))
     line = {
         "impl": "reference", "metric": metric, "value": fps,
         "unit": "frames/s",
@@ -572,6 +597,142 @@ def run_msssim(args, ws, rank, local):
     return 0
 
 
+def cambi_levels(wl):
+    """(n, h, w) uint16 10-bit levels: the distorted luma x 4 (8-bit) or
+    shifted to 10 bits (deeper)."""
+    sp = wl.spec
+    n = sp.width * sp.height
+    if sp.depth == 8:
+        y = wl.dis[:, :n].astype(np.uint16) * 4
+    else:
+        y = wl.dis[:, :n].astype(np.uint16)
+        y = (y >> (sp.depth - 10)) if sp.depth >= 10 else (y << (10 - sp.depth))
+    return np.ascontiguousarray(y.reshape(-1, sp.height, sp.width))
+
+
+def cambi_updates(w, h, win):
+    """Window-histogram updates of one plane: the first window, then a row
+    out and a row in per step (columns clipped at the edges)."""
+    r = win // 2
+    cols = sum(min(w - 1, x + r) - max(0, x - r) + 1 for x in range(w))
+    rows_in = min(r, h - 1) + 1 + sum(
+        (1 if y - r - 1 >= 0 else 0) + (1 if y + r < h else 0) for y in range(1, h))
+    return cols * rows_in
+
+
+def oracle_cambi_throughput(levels, n_frames: int, threads: int, k: int):
+    import concurrent.futures as cf
+
+    import oracle
+    oracle.build()
+
+    def one(j):
+        c = oracle.cambi_cvalues(levels[j % levels.shape[0]], CAMBI_WINDOW, CAMBI_DIFFS,
+                                 CAMBI_WEIGHTS)
+        return oracle.cambi_topk(c, k)[2]
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, range(n_frames)))
+    dt = time.perf_counter() - t0
+    return n_frames / dt, dt
+
+
+def run_cambi(args, ws, rank, local):
+    spec = synth.SPECS[args.workload]
+    wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
+    lv_host = cambi_levels(wl)
+    import torch
+    import torch.distributed as dist
+
+    from ssimulacra2_image_scoring_gb300 import Cambi
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lv = torch.from_numpy(lv_host).to(dev)
+    n, h, w = lv_host.shape
+    k = (h * w) // 4
+    cb = Cambi(w, h, CAMBI_WINDOW, CAMBI_DIFFS, CAMBI_WEIGHTS, batch=args.batch or 0)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        cb.pool(lv, k, stream=stream)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    cb.profile_begin()
+    start.record(stream)
+    for _ in range(args.steps):
+        sums, thr, means = cb.pool(lv, k, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    prof = cb.profile_end()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(start.elapsed_time(end), ws)
+    value = n * ws * args.steps / (ms_total / 1000.0)
+
+    dom = "k_cambi_cvalues"
+    dom_ms, dom_launches = prof[dom]
+    upd = cambi_updates(w, h, CAMBI_WINDOW)
+    achieved = upd * n * args.steps / (dom_ms / 1000.0)
+
+    pl = torch.from_numpy(lv_host).pin_memory()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(max(1, args.steps)):
+        lv.copy_(pl, non_blocking=True)
+        cb.pool(lv, k, stream=stream)
+    torch.cuda.synchronize()
+    e2e_fps = n * ws * max(1, args.steps) / max_over_ranks(time.perf_counter() - t0, ws)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cores = max(1, min(host_cores(), 16))
+        fps_cpu, dt_cpu = oracle_cambi_throughput(lv_host[:, :h // 16, :], cores, cores,
+                                                  (h // 16) * w // 4)
+        cpu = {"value": fps_cpu / 16.0, "unit": "frames/s", "cores": cores, "kind": "oracle",
+               "sample": f"{cores} bands of {w}x{h // 16} (a sixteenth of a frame each, "
+                         f"scaled to frames), one oracle thread per band, {dt_cpu:.1f} s"}
+    line = {
+        "metric": CAMBI_METRIC, "value": value, "unit": "frames/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16+f32",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "feature": "cambi", "frames_per_step": n,
+                   "window": CAMBI_WINDOW, "diffs": list(CAMBI_DIFFS),
+                   "weights": list(CAMBI_WEIGHTS), "k": k,
+                   "levels": "distorted luma as 10-bit levels",
+                   "l2": "inputs larger than L2 (levels 0.83 GB, c-values 1.66 GB per step)"},
+        "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved / 1e9,
+                     "peak": SMEM_OPS_PEAK / 1e9,
+                     "peak_source": "derived: 152 SMs x 32 lanes x 2070 MHz shared-memory ops",
+                     "unit": "G window updates/s", "frac": achieved / SMEM_OPS_PEAK,
+                     "traffic": None, "updates_per_frame": upd,
+                     "avg_launch_ms": dom_ms / dom_launches},
+        "per_kernel": {kk: {"ms_total": prof[kk][0], "launches": prof[kk][1]} for kk in cb.KERNELS},
+        "clocks": clk,
+        "e2e": {"value": e2e_fps, "unit": "frames/s",
+                "h2d_bytes_per_step": int(lv_host.nbytes), "d2h_bytes_per_step": 28 * n},
+        "gpu_launches": sum(prof[kk][1] for kk in cb.KERNELS),
+        "cpu_baseline": cpu,
+        "means_head": [float(x) for x in means[:3]],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    cb.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_fssim(args, ws, rank, local):
     spec = synth.SPECS[args.workload]
     wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
@@ -688,7 +849,7 @@ def main(argv=None) -> int:
                     help="frames per pass (default: the library's choice for the geometry)")
     ap.add_argument("--frames", type=int, default=0,
                     help="score only the first N frames of the workload (small profiling cases)")
-    ap.add_argument("--feature", choices=["ssimulacra2", "fssim", "msssim"],
+    ap.add_argument("--feature", choices=["ssimulacra2", "fssim", "msssim", "cambi"],
                     default="ssimulacra2",
                     help="fssim: float_ssim with device decimation; msssim: MS-SSIM of the "
                          "luma plane; both on the same workload")
@@ -702,6 +863,8 @@ def main(argv=None) -> int:
         return run_fssim(args, ws, rank, local)
     if args.feature == "msssim":
         return run_msssim(args, ws, rank, local)
+    if args.feature == "cambi":
+        return run_cambi(args, ws, rank, local)
     return run_ours(args, ws, rank, local)
 
 

@@ -37,6 +37,7 @@
 #define SS2_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -305,6 +306,54 @@ int ss2_msssim_debug_pyramid(ss2_msssim *ctx, const void *ref, const void *dis,
 int ss2_msssim_profile_begin(ss2_msssim *ctx);
 int ss2_msssim_profile_end(ss2_msssim *ctx, double *ms, int *launches);
 void ss2_msssim_destroy(ss2_msssim *ctx);
+
+/*
+ * CAMBI c-values and top-K pooling ("ADR-1357: Run the SYCL CAMBI extractor
+ * entirely on the device", Decision).  The stages before them (10-bit
+ * conversion, spatial mask, decimation, mode filter) are the caller's: a
+ * plane here is a w x h array of 10-bit levels (uint16, < 1024, rows packed)
+ * with an optional mask (uint8, nonzero = counted, same layout).
+ *   c-value of a counted pixel of level L: the largest over the (d, w) table
+ *     of (float)(w p0 pm) * RN(1 / (p0 + pm)), with p0 and pm the counts of
+ *     levels L and L + d among the counted pixels of the window x window
+ *     square centred on it, clipped to the plane (a term with pm = 0 is 0);
+ *     0 for a pixel that is not counted.  Every nonzero value lies in
+ *     [0.5, 2^14) and so on the 2^-24 grid.
+ *   top-K pool of a plane's c-values: T the k-th largest, the exact sum
+ *     S = sum(v > T) + (k - #(v > T)) T in units of 2^-24 (128 bits), the
+ *     mean S 2^-24 / k in fp64.
+ *   ss2_cambi_create: window odd with window^2 <= 4225 (at most 65), 1..4
+ *     (diff, weight) pairs (diff 1..1023, weight 1..9), max_batch 0 = 16
+ *     planes per pass (at most 1024).  NULL with -EINVAL for bad arguments,
+ *     -ENOMEM.
+ *   ss2_cambi_cvalues: levels (and mask, or NULL) DEVICE, n_planes planes;
+ *     cvalues DEVICE floats, n_planes planes.  -EINVAL for a level >= 1024.
+ *   ss2_cambi_topk: cvalues DEVICE (values 0 or on the 2^-24 grid below
+ *     2^14, else -EINVAL); k in 1..w h; sums HOST (lo, hi) pairs of
+ *     uint64, thresholds HOST floats, means HOST doubles, n_planes each;
+ *     any output pointer may be NULL.
+ *   ss2_cambi_pool: both stages, the c-values kept in the context's own
+ *     workspace; outputs as ss2_cambi_topk.
+ *   All three: 0 on success, -EINVAL (NULL context or input, negative
+ *   count; 0 planes: no work), -ENOMEM (pinned staging), -EIO (CUDA
+ *   failure); one stream synchronisation per call.  The context owns its
+ *   workspace (one batch of c-values, radix histograms, block sums).
+ *   ss2_cambi_profile_begin / _end: kernel classes 0 k_cambi_cvalues, 1 the
+ *     top-K kernels (ms: 2 doubles, launches: 2 ints, either may be NULL).
+ */
+typedef struct ss2_cambi ss2_cambi;
+ss2_cambi *ss2_cambi_create(int width, int height, int window, int ndiff,
+                            const int *diffs, const int *weights, int max_batch);
+int ss2_cambi_cvalues(ss2_cambi *ctx, const uint16_t *levels, const uint8_t *mask,
+                      int n_planes, float *cvalues, void *stream);
+int ss2_cambi_topk(ss2_cambi *ctx, const float *cvalues, int n_planes, long long k,
+                   uint64_t *sums, float *thresholds, double *means, void *stream);
+int ss2_cambi_pool(ss2_cambi *ctx, const uint16_t *levels, const uint8_t *mask,
+                   int n_planes, long long k, uint64_t *sums, float *thresholds,
+                   double *means, void *stream);
+int ss2_cambi_profile_begin(ss2_cambi *ctx);
+int ss2_cambi_profile_end(ss2_cambi *ctx, double *ms, int *launches);
+void ss2_cambi_destroy(ss2_cambi *ctx);
 
 /* Last failure on the calling thread (0 if none yet).                      */
 int ss2_last_error(void);

@@ -108,6 +108,8 @@ def lib() -> ctypes.CDLL:
             L.ss2o_cambi_recip.restype = ctypes.c_float
             L.ss2o_cambi_cvalues.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
             L.ss2o_cambi_cvalues.restype = i
+            L.ss2o_cambi_cvalue_at.argtypes = [vp, vp, i, i, i, i, vp, vp, i, i, vp]
+            L.ss2o_cambi_cvalue_at.restype = i
             L.ss2o_cambi_topk.argtypes = [vp, ctypes.c_long, ctypes.c_long, vp, vp, vp, vp]
             L.ss2o_cambi_topk.restype = i
             L.ss2o_msssim_dims.argtypes = [i, i, vp]
@@ -301,6 +303,24 @@ def cambi_cvalues(levels: np.ndarray, window: int, diffs, weights, mask=None) ->
     if rc != 0:
         raise ValueError(f"cambi c-values rejected: rc={rc}")
     return out
+
+
+def cambi_cvalue_at(levels: np.ndarray, window: int, diffs, weights, points, mask=None):
+    """c-values of the listed (y, x) pixels of one level plane, one by one."""
+    lv = np.ascontiguousarray(levels, dtype=np.uint16)
+    h, w = lv.shape
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+    d = np.ascontiguousarray(diffs, dtype=np.int32)
+    wt = np.ascontiguousarray(weights, dtype=np.int32)
+    out = np.zeros(1, np.float32)
+    res = []
+    for (y, x) in points:
+        rc = lib().ss2o_cambi_cvalue_at(_ptr(lv), _ptr(m), w, h, window, len(d), _ptr(d),
+                                        _ptr(wt), int(x), int(y), _ptr(out))
+        if rc != 0:
+            raise ValueError(f"cambi c-value rejected: rc={rc}")
+        res.append(float(out[0]))
+    return np.array(res, np.float32)
 
 
 def cambi_topk(c: np.ndarray, k: int):

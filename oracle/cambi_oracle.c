@@ -42,6 +42,38 @@ float ss2o_cambi_recip(int n)
     return 1.0f / (float)n;   /* IEEE division: correctly rounded */
 }
 
+/* The c-value of pixel (x, y): counts over its clipped window by a direct
+ * scan, then the largest term of the diff table.                          */
+static float cvalue_at(const uint16_t *levels, const uint8_t *mask, int w, int h, int window,
+                       int ndiff, const int *diffs, const int *weights, int x, int y)
+{
+    const size_t at = (size_t)y * w + x;
+    if (mask && !mask[at]) return 0.0f;
+    const int r = window / 2;
+    const int L = levels[at];
+    long p0 = 0, pm[4] = {0, 0, 0, 0};
+    for (int yy = y - r; yy <= y + r; ++yy) {
+        if (yy < 0 || yy >= h) continue;
+        for (int xx = x - r; xx <= x + r; ++xx) {
+            if (xx < 0 || xx >= w) continue;
+            const size_t j = (size_t)yy * w + xx;
+            if (mask && !mask[j]) continue;
+            const int v = levels[j];
+            if (v == L) ++p0;
+            for (int i = 0; i < ndiff; ++i)
+                if (v == L + diffs[i]) ++pm[i];
+        }
+    }
+    float best = 0.0f;
+    for (int i = 0; i < ndiff; ++i) {
+        if (pm[i] == 0) continue;
+        const long num = (long)weights[i] * p0 * pm[i];
+        const float c = (float)num * ss2o_cambi_recip((int)(p0 + pm[i]));
+        if (c > best) best = c;
+    }
+    return best;
+}
+
 int ss2o_cambi_cvalues(const uint16_t *levels, const uint8_t *mask, int w, int h, int window,
                        int ndiff, const int *diffs, const int *weights, float *out)
 {
@@ -53,38 +85,19 @@ int ss2o_cambi_cvalues(const uint16_t *levels, const uint8_t *mask, int w, int h
             return -22;
     for (size_t i = 0; i < (size_t)w * h; ++i)
         if (levels[i] >= CAMBI_LEVELS) return -22;
-    const int r = window / 2;
-    for (int y = 0; y < h; ++y) {
-        for (int x = 0; x < w; ++x) {
-            const size_t at = (size_t)y * w + x;
-            if (mask && !mask[at]) {
-                out[at] = 0.0f;
-                continue;
-            }
-            const int L = levels[at];
-            long p0 = 0, pm[4] = {0, 0, 0, 0};
-            for (int yy = y - r; yy <= y + r; ++yy) {
-                if (yy < 0 || yy >= h) continue;
-                for (int xx = x - r; xx <= x + r; ++xx) {
-                    if (xx < 0 || xx >= w) continue;
-                    const size_t j = (size_t)yy * w + xx;
-                    if (mask && !mask[j]) continue;
-                    const int v = levels[j];
-                    if (v == L) ++p0;
-                    for (int i = 0; i < ndiff; ++i)
-                        if (v == L + diffs[i]) ++pm[i];
-                }
-            }
-            float best = 0.0f;
-            for (int i = 0; i < ndiff; ++i) {
-                if (pm[i] == 0) continue;
-                const long num = (long)weights[i] * p0 * pm[i];
-                const float c = (float)num * ss2o_cambi_recip((int)(p0 + pm[i]));
-                if (c > best) best = c;
-            }
-            out[at] = best;
-        }
-    }
+    for (int y = 0; y < h; ++y)
+        for (int x = 0; x < w; ++x)
+            out[(size_t)y * w + x] = cvalue_at(levels, mask, w, h, window, ndiff, diffs,
+                                               weights, x, y);
+    return 0;
+}
+
+int ss2o_cambi_cvalue_at(const uint16_t *levels, const uint8_t *mask, int w, int h, int window,
+                         int ndiff, const int *diffs, const int *weights, int x, int y,
+                         float *out)
+{
+    if (x < 0 || x >= w || y < 0 || y >= h) return -22;
+    *out = cvalue_at(levels, mask, w, h, window, ndiff, diffs, weights, x, y);
     return 0;
 }
 

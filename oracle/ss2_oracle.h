@@ -119,6 +119,9 @@ float ss2o_cambi_recip(int n);
 int ss2o_cambi_cvalues(const uint16_t *levels, const uint8_t *mask, int w, int h,
                        int window, int ndiff, const int *diffs, const int *weights,
                        float *out);
+int ss2o_cambi_cvalue_at(const uint16_t *levels, const uint8_t *mask, int w, int h,
+                         int window, int ndiff, const int *diffs, const int *weights,
+                         int x, int y, float *out);
 int ss2o_cambi_topk(const float *c, long n, long k, uint64_t *sum_lo,
                     uint64_t *sum_hi, float *threshold, double *mean);
 

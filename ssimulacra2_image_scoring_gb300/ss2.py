@@ -77,6 +77,21 @@ def lib() -> ctypes.CDLL:
             L.ss2_fssim_profile_begin.restype = i
             L.ss2_fssim_profile_end.argtypes = [vp, vp, vp]
             L.ss2_fssim_profile_end.restype = i
+            ll = ctypes.c_longlong
+            L.ss2_cambi_create.argtypes = [i, i, i, i, vp, vp, i]
+            L.ss2_cambi_create.restype = vp
+            L.ss2_cambi_cvalues.argtypes = [vp, vp, vp, i, vp, vp]
+            L.ss2_cambi_cvalues.restype = i
+            L.ss2_cambi_topk.argtypes = [vp, vp, i, ll, vp, vp, vp, vp]
+            L.ss2_cambi_topk.restype = i
+            L.ss2_cambi_pool.argtypes = [vp, vp, vp, i, ll, vp, vp, vp, vp]
+            L.ss2_cambi_pool.restype = i
+            L.ss2_cambi_profile_begin.argtypes = [vp]
+            L.ss2_cambi_profile_begin.restype = i
+            L.ss2_cambi_profile_end.argtypes = [vp, vp, vp]
+            L.ss2_cambi_profile_end.restype = i
+            L.ss2_cambi_destroy.argtypes = [vp]
+            L.ss2_cambi_destroy.restype = None
             L.ss2_msssim_create.argtypes = [i, i, i, i, i]
             L.ss2_msssim_create.restype = vp
             L.ss2_msssim_score.argtypes = [vp, vp, vp, i, vp, vp, vp]
@@ -226,6 +241,96 @@ class FloatSSIM:
     def close(self) -> None:
         if self._h:
             lib().ss2_fssim_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Cambi:
+    """CAMBI c-values and top-K pooling for one plane size (ss2_cambi_create)."""
+
+    KERNELS = ("k_cambi_cvalues", "k_cambi_topk")
+
+    def __init__(self, width: int, height: int, window: int, diffs, weights, batch: int = 0):
+        d = np.ascontiguousarray(diffs, dtype=np.int32)
+        w = np.ascontiguousarray(weights, dtype=np.int32)
+        if d.size != w.size:
+            raise ValueError("diffs and weights differ in length")
+        h = lib().ss2_cambi_create(width, height, window, d.size, d.ctypes.data, w.ctypes.data,
+                                   batch)
+        if not h:
+            code, msg = last_error()
+            raise SS2Error(code, msg)
+        self._h = h
+        self.width, self.height = width, height
+
+    @staticmethod
+    def _dev(t, dtype):
+        import torch
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous() and t.dtype == dtype):
+            raise TypeError(f"expected a contiguous CUDA tensor of {dtype}")
+        return t.data_ptr()
+
+    def cvalues(self, levels, mask=None, stream=None):
+        """levels: (n, h, w) uint16 CUDA tensor; returns (n, h, w) float32 CUDA c-values."""
+        import torch
+        n = levels.shape[0]
+        out = torch.empty((n, self.height, self.width), dtype=torch.float32, device=levels.device)
+        _check(lib().ss2_cambi_cvalues(self._h, self._dev(levels, torch.uint16),
+                                       None if mask is None else self._dev(mask, torch.uint8), n,
+                                       out.data_ptr(), _stream_handle(stream)))
+        return out
+
+    def _pooled(self, n):
+        return np.zeros((n, 2), np.uint64), np.zeros(n, np.float32), np.zeros(n, np.float64)
+
+    @staticmethod
+    def _result(s, t, m):
+        return [(int(hi) << 64) | int(lo) for lo, hi in s], t, m
+
+    def topk(self, cvalues, k: int, stream=None):
+        """(exact sums in 2^-24 units as Python ints, thresholds, means) per plane."""
+        import torch
+        n = cvalues.shape[0]
+        s, t, m = self._pooled(n)
+        _check(lib().ss2_cambi_topk(self._h, self._dev(cvalues, torch.float32), n, k,
+                                    s.ctypes.data, t.ctypes.data, m.ctypes.data,
+                                    _stream_handle(stream)))
+        return self._result(s, t, m)
+
+    def pool(self, levels, k: int, mask=None, stream=None):
+        """c-values and top-K in one call: as topk()."""
+        import torch
+        n = levels.shape[0]
+        s, t, m = self._pooled(n)
+        _check(lib().ss2_cambi_pool(self._h, self._dev(levels, torch.uint16),
+                                    None if mask is None else self._dev(mask, torch.uint8), n, k,
+                                    s.ctypes.data, t.ctypes.data, m.ctypes.data,
+                                    _stream_handle(stream)))
+        return self._result(s, t, m)
+
+    def profile_begin(self) -> None:
+        _check(lib().ss2_cambi_profile_begin(self._h))
+
+    def profile_end(self) -> dict:
+        ms = np.zeros(2, np.float64)
+        n = np.zeros(2, np.int32)
+        _check(lib().ss2_cambi_profile_end(self._h, ms.ctypes.data, n.ctypes.data))
+        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
+
+    def close(self) -> None:
+        if self._h:
+            lib().ss2_cambi_destroy(self._h)
             self._h = None
 
     def __enter__(self):
