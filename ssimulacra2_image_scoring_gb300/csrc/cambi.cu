@@ -12,14 +12,13 @@
 // (d, w) pairs with the largest term taken, the reciprocal 1/n rounded to
 // nearest (__frcp_rn), the pool the mean of the exact sum.
 //
-//   k_cambi_cvalues  one warp per 32 columns of a plane; lane = column.  The
-//                    lane's window histogram (1024 bins of 16 bits, two per
-//                    32-bit word, interleaved by lane) lives in shared
-//                    memory; moving down a row removes the leaving row's
-//                    window segment and adds the entering one with shared
-//                    atomic adds of +-2^(16 (lane & 1)) (no return value: no
-//                    dependency chains; counts stay in 0..4225, so nothing
-//                    carries or borrows into the neighbour's half).
+//   k_cambi_cvalues  one warp per 32 columns of a plane; lane = column.  Each
+//                    step the warp stages the leaving and entering row
+//                    segments in shared memory (fetched one step ahead); the
+//                    lane's window histogram (1024 bins of 16 bits,
+//                    interleaved by lane so each lane owns its elements) is
+//                    updated with plain loads and stores, a column whose
+//                    leaving and entering pixels agree being skipped.
 //   k_cambi_hist     radix histogram of one 11/11/10-bit digit of the values
 //                    that match the digits chosen so far.
 //   k_cambi_select   one block per plane: the digit holding the k-th largest
@@ -60,56 +59,108 @@ struct CGeom {
   int sum_blocks;           // per plane
 };
 
-// Histogram bin of level v for lane l: 16-bit half of word v * 16 + l / 2.
-// +1 adds 1 << s to the word, -1 subtracts it: a count stays in 0..4225, so
-// neither carries nor borrows across the halves, and the two lanes sharing
-// a word update it with commuting atomics.
-__device__ __forceinline__ void hist_add(unsigned *hist, int v, int lane, bool add) {
-  const unsigned one = 1u << (16 * (lane & 1));
-  atomicAdd(hist + v * 16 + (lane >> 1), add ? one : 0u - one);
+// Histogram bin of level v for lane l: the 16-bit element v * 32 + l, which
+// only that lane touches (plain loads and stores; shared-memory order within
+// a thread keeps successive updates of one bin correct).  A count stays in
+// 0..4225.
+__device__ __forceinline__ unsigned hist_get(const uint16_t *hist, int v, int lane) {
+  return hist[v * 32 + lane];
 }
 
-__device__ __forceinline__ unsigned hist_get(const unsigned *hist, int v, int lane) {
-  return (hist[v * 16 + (lane >> 1)] >> (16 * (lane & 1))) & 0xFFFFu;
-}
+constexpr int kSeg = 32 + 64;                      // a row's window columns for 32 lanes
+constexpr unsigned kSkip = 0xFFFFu;                // outside the plane or not counted
+constexpr int kBatch = 16;                         // columns whose levels are read ahead
 
 __global__ void __launch_bounds__(32)
     k_cambi_cvalues(CGeom g, const uint16_t *__restrict__ levels, const uint8_t *__restrict__ mask,
                     float *__restrict__ out, int *__restrict__ err) {
-  extern __shared__ unsigned cv_hist[];            // kLevels * 16 words
+  extern __shared__ uint16_t cv_hist[];            // kLevels x 32 lanes
+  // the leaving and entering row segments of the current step: columns
+  // x0 - r .. x0 + 31 + r (kSkip where outside the plane or not counted)
+  __shared__ uint16_t seg[2][kSeg];
   const int lane = threadIdx.x;
-  const int x = blockIdx.x * 32 + lane;
+  const int x0 = blockIdx.x * 32, x = x0 + lane;
   const long long base = (long long)blockIdx.y * g.plane;
   const uint16_t *L = levels + base;
   const uint8_t *M = mask ? mask + base : nullptr;
-  for (int i = lane; i < kLevels * 16; i += 32) cv_hist[i] = 0u;
-  __syncwarp();
+  for (int i = lane; i < kLevels * 32; i += 32) cv_hist[i] = 0u;
   const int r = g.window / 2;
+  const int nseg = 32 + 2 * r;
   const bool col = x < g.w;
-  const int xa = max(0, x - r), xb = min(g.w - 1, x + r);
   bool bad = false;
-  // one row's window segment added or removed
-  auto apply_row = [&](int yy, bool add) {
-    const uint16_t *row = L + (long long)yy * g.w;
-    const uint8_t *mrow = M ? M + (long long)yy * g.w : nullptr;
-    for (int xx = xa; xx <= xb; ++xx) {
-      if (mrow && !__ldg(mrow + xx)) continue;
-      int v = __ldg(row + xx);
-      if (v >= kLevels) {
-        bad = true;
-        v = kLevels - 1;              // stays in bounds; the call reports -EINVAL
+  // the segment values of row yy (kSkip for rows outside the plane): three
+  // per lane, loaded together
+  auto fetch = [&](int yy, unsigned (&v)[3]) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int i = lane + 32 * j, xx = x0 - r + i;
+      v[j] = kSkip;
+      if (i < nseg && yy >= 0 && yy < g.h && xx >= 0 && xx < g.w) {
+        const long long at = (long long)yy * g.w + xx;
+        if (!M || __ldg(M + at)) {
+          unsigned lv = __ldg(L + at);
+          if (lv >= kLevels) {
+            bad = true;
+            lv = kLevels - 1;              // stays in bounds; the call reports -EINVAL
+          }
+          v[j] = lv;
+        }
       }
-      hist_add(cv_hist, v, lane, add);
     }
   };
-  if (col)
-    for (int yy = 0; yy <= min(r, g.h - 1); ++yy) apply_row(yy, true);
-  for (int y = 0; y < g.h; ++y) {
-    if (col) {
-      if (y > 0) {
-        if (y - r - 1 >= 0) apply_row(y - r - 1, false);
-        if (y + r < g.h) apply_row(y + r, true);
+  auto put = [&](int s_, const unsigned (&v)[3]) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+      if (lane + 32 * j < kSeg) seg[s_][lane + 32 * j] = (uint16_t)v[j];
+  };
+  // the lane's window columns lane .. lane + 2r: remove seg[0], add seg[1]
+  // (a column whose two pixels agree is skipped); the levels of kBatch
+  // columns are read before their updates
+  auto apply = [&](bool remove) {
+    for (int i0 = 0; i0 <= 2 * r; i0 += kBatch) {
+      unsigned a[kBatch], b[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + k;
+        a[k] = (remove && i <= 2 * r) ? seg[0][lane + i] : kSkip;
+        b[k] = i <= 2 * r ? seg[1][lane + i] : kSkip;
       }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (a[k] == b[k]) continue;                 // the column's count does not change
+        // a != b: two different bins, both read before either is written
+        const unsigned ca = a[k] != kSkip ? cv_hist[a[k] * 32 + lane] : 0u;
+        const unsigned cb = b[k] != kSkip ? cv_hist[b[k] * 32 + lane] : 0u;
+        if (a[k] != kSkip) cv_hist[a[k] * 32 + lane] = (uint16_t)(ca - 1u);
+        if (b[k] != kSkip) cv_hist[b[k] * 32 + lane] = (uint16_t)(cb + 1u);
+      }
+    }
+  };
+  __syncwarp();
+  // the first window: rows 0 .. r added
+  for (int yy = 0; yy <= min(r, g.h - 1); ++yy) {
+    unsigned v[3];
+    fetch(yy, v);
+    put(1, v);
+    __syncwarp();
+    if (col) apply(false);
+    __syncwarp();
+  }
+  // step y moves the window from rows y-1-r .. y-1+r to y-r .. y+r; the
+  // rows of step y + 1 are fetched while step y is applied
+  unsigned nout[3], nin[3];
+  fetch(-r, nout);                                  // step 1: leaving row -r, entering row 1 + r
+  fetch(1 + r, nin);
+  for (int y = 0; y < g.h; ++y) {
+    if (y > 0) {
+      put(0, nout);
+      put(1, nin);
+      __syncwarp();
+      fetch(y - r, nout);                           // rows of step y + 1
+      fetch(y + 1 + r, nin);
+      if (col) apply(true);
+    }
+    if (col) {
       const long long at = (long long)y * g.w + x;
       float best = 0.0f;
       if (!M || __ldg(M + at)) {
@@ -131,6 +182,7 @@ __global__ void __launch_bounds__(32)
       }
       out[base + at] = best;
     }
+    __syncwarp();                                   // seg is rewritten next step
   }
   if (bad) atomicOr(err, kErrLevel);
 }
