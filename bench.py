@@ -5,7 +5,8 @@ synthetic stand-in for the pages' Big Buck Bunny 4K fixture) through the
 C ABI.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline] [--feature ssimulacra2|fssim]
+                  [--workload NAME] [--no-cpu-baseline]
+                  [--feature ssimulacra2|fssim|msssim|cambi] [--frames N] [--batch B]
 
 --feature fssim times float_ssim with device decimation instead (frames/s on
 the same workload; the oracle's float_ssim as the CPU baseline); --feature
@@ -416,7 +417,8 @@ def run_ours(args, ws, rank, local):
                      "algo_bytes_per_launch": algo_bytes_launch,
                      "avg_launch_ms": dom_ms / dom_launches},
         "pipeline": {"b_min_bytes_per_frame": bm["b_min"], "achieved_gbs": pipe_gbs,
-                     "frac": pipe_gbs / peak, "per_kernel": per_kernel},
+                     "frac": pipe_gbs / peak, "frac_vs_nominal_8tbs": pipe_gbs / 8000.0,
+                     "per_kernel": per_kernel},
         "clocks": clk,
         "e2e": {"value": e2e_fps, "unit": "frames/s",
                 "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
@@ -820,7 +822,8 @@ def run_fssim(args, ws, rank, local):
                      "traffic": traffic, "algo_bytes_per_launch": algo,
                      "avg_launch_ms": dom_ms / dom_launches},
         "pipeline": {"b_min_bytes_per_frame": bm["b_min"], "achieved_gbs": pipe_gbs,
-                     "frac": pipe_gbs / peak, "per_kernel": per_kernel},
+                     "frac": pipe_gbs / peak, "frac_vs_nominal_8tbs": pipe_gbs / 8000.0,
+                     "per_kernel": per_kernel},
         "clocks": clk,
         "e2e": {"value": e2e_fps, "unit": "frames/s",
                 "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
