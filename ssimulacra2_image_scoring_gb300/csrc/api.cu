@@ -210,10 +210,7 @@ struct ss2_ctx {
   double *h_values = nullptr;
   int *h_err = nullptr;
   size_t h_cap = 0;  // frames
-  // per-kernel event timing (ss2_profile_begin / ss2_profile_end)
-  bool prof = false;
-  std::vector<cudaEvent_t> ev_pool;
-  std::vector<std::pair<int, int>> ev_used;  // (kernel class, index of start event)
+  KernelTimer timer;  // per-kernel event timing (ss2_profile_begin / ss2_profile_end)
   cudaStream_t copy_stream = nullptr;   // host-input path uploads
 };
 
@@ -360,7 +357,6 @@ static void set_pix(ss2_ctx *c) { build_pix(c->params, c->px); }
 
 static void free_ctx(ss2_ctx *c) {
   if (!c) return;
-  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   for (Lane &L : c->lane) {
     cudaFree(L.X); cudaFree(L.H); cudaFree(L.part); cudaFree(L.values); cudaFree(L.scores);
     cudaFree(L.in);
@@ -577,56 +573,22 @@ SS2_API int ss2_host_tables(float *eotf, float *iir) {
 
 enum { kKPyramid = 0, kKHblur = 1, kKVblur = 2, kKFinalize = 3, kKClasses = 4 };
 
-static cudaError_t prof_mark(ss2_ctx *c, int cls, bool start, cudaStream_t st) {
-  if (!c->prof) return cudaSuccess;
-  size_t idx;
-  if (start) {
-    idx = c->ev_used.empty() ? 0 : (size_t)c->ev_used.back().second + 2;
-    while (c->ev_pool.size() < idx + 2) {
-      cudaEvent_t e;
-      cudaError_t r = cudaEventCreate(&e);
-      if (r != cudaSuccess) return r;
-      c->ev_pool.push_back(e);
-    }
-    c->ev_used.push_back({cls, (int)idx});
-  } else {
-    idx = (size_t)c->ev_used.back().second + 1;
-  }
-  return cudaEventRecord(c->ev_pool[idx], st);
-}
-
-#define TIMED(c, cls, st, launch, what)          \
-  do {                                            \
-    CU(prof_mark(c, cls, true, st), "event");     \
-    CU(launch, what);                             \
-    CU(prof_mark(c, cls, false, st), "event");    \
+#define TIMED(c, cls, st, launch, what)                  \
+  do {                                                    \
+    CU((c)->timer.mark(cls, true, st), "event");          \
+    CU(launch, what);                                     \
+    CU((c)->timer.mark(cls, false, st), "event");         \
   } while (0)
 
 SS2_API int ss2_profile_begin(ss2_ctx *ctx) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  ctx->prof = true;
-  ctx->ev_used.clear();
+  ctx->timer.begin();
   return 0;
 }
 
 SS2_API int ss2_profile_end(ss2_ctx *ctx, double *ms, int *launches) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  double t[kKClasses] = {0, 0, 0, 0};
-  int n[kKClasses] = {0, 0, 0, 0};
-  for (const auto &u : ctx->ev_used) {
-    CU(cudaEventSynchronize(ctx->ev_pool[u.second + 1]), "event sync");
-    float e = 0.0f;
-    CU(cudaEventElapsedTime(&e, ctx->ev_pool[u.second], ctx->ev_pool[u.second + 1]),
-       "event elapsed");
-    t[u.first] += e;
-    n[u.first] += 1;
-  }
-  ctx->prof = false;
-  ctx->ev_used.clear();
-  for (int i = 0; i < kKClasses; ++i) {
-    if (ms) ms[i] = t[i];
-    if (launches) launches[i] = n[i];
-  }
+  CU(ctx->timer.finish(kKClasses, ms, launches), "profile events");
   return 0;
 }
 

@@ -346,14 +346,11 @@ struct ss2_cambi {
   float *h_thr = nullptr;
   double *h_means = nullptr;
   size_t h_cap = 0;
-  bool prof = false;
-  std::vector<cudaEvent_t> ev_pool;
-  std::vector<std::pair<int, int>> ev_used;
+  KernelTimer timer;                         // per-kernel event timing
 };
 
 static void cambi_free(ss2_cambi *c) {
   if (!c) return;
-  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   cudaFree(c->d_c);
   cudaFree(c->d_st);
   cudaFree(c->d_hist);
@@ -435,72 +432,33 @@ SS2_API ss2_cambi *ss2_cambi_create(int width, int height, int window, int ndiff
 
 SS2_API void ss2_cambi_destroy(ss2_cambi *ctx) { cambi_free(ctx); }
 
-static cudaError_t cambi_mark(ss2_cambi *c, int cls, bool start, cudaStream_t st) {
-  if (!c->prof) return cudaSuccess;
-  size_t idx;
-  if (start) {
-    idx = c->ev_used.size() * 2;
-    while (c->ev_pool.size() < idx + 2) {
-      cudaEvent_t e;
-      cudaError_t r = cudaEventCreate(&e);
-      if (r != cudaSuccess) return r;
-      c->ev_pool.push_back(e);
-    }
-    c->ev_used.push_back({cls, (int)idx});
-  } else {
-    idx = (size_t)c->ev_used.back().second + 1;
-  }
-  return cudaEventRecord(c->ev_pool[idx], st);
-}
-
 SS2_API int ss2_cambi_profile_begin(ss2_cambi *ctx) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  ctx->prof = true;
-  ctx->ev_used.clear();
+  ctx->timer.begin();
   return 0;
 }
 
 SS2_API int ss2_cambi_profile_end(ss2_cambi *ctx, double *ms, int *launches) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  double t[2] = {0, 0};
-  int n[2] = {0, 0};
-  for (const auto &u : ctx->ev_used) {
-    cudaError_t e = cudaEventSynchronize(ctx->ev_pool[u.second + 1]);
-    float dt = 0.0f;
-    if (e == cudaSuccess)
-      e = cudaEventElapsedTime(&dt, ctx->ev_pool[u.second], ctx->ev_pool[u.second + 1]);
-    if (e != cudaSuccess) {
-      ctx->prof = false;
-      ctx->ev_used.clear();
-      return cuda_fail(e, "cambi profile events");
-    }
-    t[u.first] += dt;
-    n[u.first] += 1;
-  }
-  ctx->prof = false;
-  ctx->ev_used.clear();
-  for (int i = 0; i < 2; ++i) {
-    if (ms) ms[i] = t[i];
-    if (launches) launches[i] = n[i];
-  }
-  return 0;
+  const cudaError_t e = ctx->timer.finish(2, ms, launches);
+  return e == cudaSuccess ? 0 : cuda_fail(e, "cambi profile events");
 }
 
 static cudaError_t cambi_cv_launch(ss2_cambi *c, const uint16_t *levels, const uint8_t *mask,
                                    float *out, int nb, cudaStream_t st) {
   const CGeom &g = c->g;
-  cudaError_t e = cambi_mark(c, 0, true, st);
+  cudaError_t e = c->timer.mark(0, true, st);
   if (e != cudaSuccess) return e;
   k_cambi_cvalues<<<dim3((g.w + 31) / 32, nb), 32, kCvSmem, st>>>(g, levels, mask, out, c->d_err);
   e = cudaGetLastError();
-  if (e == cudaSuccess) e = cambi_mark(c, 0, false, st);
+  if (e == cudaSuccess) e = c->timer.mark(0, false, st);
   return e;
 }
 
 static cudaError_t cambi_pool_launch(ss2_cambi *c, const float *cv, int nb, long long k,
                                      cudaStream_t st) {
   const CGeom &g = c->g;
-  cudaError_t e = cambi_mark(c, 1, true, st);
+  cudaError_t e = c->timer.mark(1, true, st);
   if (e == cudaSuccess) {
     k_cambi_init<<<1, nb, 0, st>>>(c->d_st, k);
     e = cudaGetLastError();
@@ -522,7 +480,7 @@ static cudaError_t cambi_pool_launch(ss2_cambi *c, const float *cv, int nb, long
     k_cambi_final<<<nb, 32, 0, st>>>(g, c->d_st, c->d_part, k, c->d_sums, c->d_thr, c->d_means);
     e = cudaGetLastError();
   }
-  if (e == cudaSuccess) e = cambi_mark(c, 1, false, st);
+  if (e == cudaSuccess) e = c->timer.mark(1, false, st);
   return e;
 }
 

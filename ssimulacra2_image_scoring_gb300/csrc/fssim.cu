@@ -609,15 +609,11 @@ struct ss2_fssim {
   double *d_part = nullptr, *d_scores = nullptr, *h_scores = nullptr;
   size_t h_cap = 0;
   int *d_err = nullptr, *h_err = nullptr;   // error bits raised by kernels (bounded waits)
-  // per-kernel event timing (ss2_fssim_profile_begin / _end)
-  bool prof = false;
-  std::vector<cudaEvent_t> ev_pool;
-  std::vector<std::pair<int, int>> ev_used;   // (kernel class, index of start event)
+  KernelTimer timer;                         // per-kernel event timing
 };
 
 static void fssim_free(ss2_fssim *c) {
   if (!c) return;
-  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   cudaFree(c->d_dec);
   cudaFree(c->d_part);
   cudaFree(c->d_scores);
@@ -769,57 +765,16 @@ SS2_API void ss2_fssim_destroy(ss2_fssim *ctx) { fssim_free(ctx); }
 
 SS2_API int ss2_fssim_scale(const ss2_fssim *ctx) { return ctx ? ctx->g.scale : 0; }
 
-// Records the start (start = true) or end event of one launch of kernel
-// class cls while profiling.
-static cudaError_t fssim_mark(ss2_fssim *c, int cls, bool start, cudaStream_t st) {
-  if (!c->prof) return cudaSuccess;
-  size_t idx;
-  if (start) {
-    idx = c->ev_used.size() * 2;
-    while (c->ev_pool.size() < idx + 2) {
-      cudaEvent_t e;
-      cudaError_t r = cudaEventCreate(&e);
-      if (r != cudaSuccess) return r;
-      c->ev_pool.push_back(e);
-    }
-    c->ev_used.push_back({cls, (int)idx});
-  } else {
-    idx = (size_t)c->ev_used.back().second + 1;
-  }
-  return cudaEventRecord(c->ev_pool[idx], st);
-}
-
 SS2_API int ss2_fssim_profile_begin(ss2_fssim *ctx) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  ctx->prof = true;
-  ctx->ev_used.clear();
+  ctx->timer.begin();
   return 0;
 }
 
 SS2_API int ss2_fssim_profile_end(ss2_fssim *ctx, double *ms, int *launches) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  double t[3] = {0, 0, 0};
-  int n[3] = {0, 0, 0};
-  for (const auto &u : ctx->ev_used) {
-    cudaError_t e = cudaEventSynchronize(ctx->ev_pool[u.second + 1]);
-    float dt = 0.0f;
-    if (e == cudaSuccess) e = cudaEventElapsedTime(&dt, ctx->ev_pool[u.second],
-                                                   ctx->ev_pool[u.second + 1]);
-    if (e != cudaSuccess) {
-      ctx->prof = false;
-      ctx->ev_used.clear();
-      return cuda_fail(e, "float_ssim profile events");
-    }
-    t[u.first] += dt;
-    n[u.first] += 1;
-  }
-  ctx->prof = false;
-  ctx->ev_used.clear();
-  for (int i = 0; i < 3; ++i) {
-    if (ms) ms[i] = t[i];
-    if (launches) launches[i] = n[i];
-  }
-  return 0;
+  const cudaError_t e = ctx->timer.finish(3, ms, launches);
+  return e == cudaSuccess ? 0 : cuda_fail(e, "float_ssim profile events");
 }
 
 static size_t fssim_decimate_smem(const FGeom &g) {
@@ -915,23 +870,23 @@ SS2_API int ss2_fssim_score(ss2_fssim *ctx, const void *ref, const void *dis, in
   const uint8_t *r8 = (const uint8_t *)ref, *d8 = (const uint8_t *)dis;
   for (int f0 = 0; f0 < n_frames; f0 += ctx->batch) {
     const int nb = std::min(ctx->batch, n_frames - f0);
-    cudaError_t e = fssim_mark(ctx, 0, true, st);
+    cudaError_t e = ctx->timer.mark(0, true, st);
     if (e == cudaSuccess)
       e = fssim_launch_decimate(g, r8 + f0 * g.frame_bytes, d8 + f0 * g.frame_bytes, ctx->d_dec,
                                 nb, ctx->d_err, st);
-    if (e == cudaSuccess) e = fssim_mark(ctx, 0, false, st);
-    if (e == cudaSuccess) e = fssim_mark(ctx, 1, true, st);
+    if (e == cudaSuccess) e = ctx->timer.mark(0, false, st);
+    if (e == cudaSuccess) e = ctx->timer.mark(1, true, st);
     if (e == cudaSuccess) {
       k_fssim_map<<<dim3(g.tiles_x, g.tiles_y, nb), 256, 0, st>>>(g, ctx->d_dec, ctx->d_part);
       e = cudaGetLastError();
     }
-    if (e == cudaSuccess) e = fssim_mark(ctx, 1, false, st);
-    if (e == cudaSuccess) e = fssim_mark(ctx, 2, true, st);
+    if (e == cudaSuccess) e = ctx->timer.mark(1, false, st);
+    if (e == cudaSuccess) e = ctx->timer.mark(2, true, st);
     if (e == cudaSuccess) {
       k_fssim_final<<<nb, 32, 0, st>>>(g, ctx->d_part, ctx->d_scores);
       e = cudaGetLastError();
     }
-    if (e == cudaSuccess) e = fssim_mark(ctx, 2, false, st);
+    if (e == cudaSuccess) e = ctx->timer.mark(2, false, st);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(ctx->h_scores + f0, ctx->d_scores, nb * sizeof(double),
                           cudaMemcpyDeviceToHost, st);

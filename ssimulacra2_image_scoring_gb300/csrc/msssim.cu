@@ -308,14 +308,11 @@ struct ss2_msssim {
   double *d_part = nullptr, *d_scores = nullptr, *d_values = nullptr;
   double *h_scores = nullptr, *h_values = nullptr;
   size_t h_cap = 0;
-  bool prof = false;
-  std::vector<cudaEvent_t> ev_pool;
-  std::vector<std::pair<int, int>> ev_used;  // (kernel class, index of start event)
+  KernelTimer timer;                         // per-kernel event timing
 };
 
 static void msssim_free(ss2_msssim *c) {
   if (!c) return;
-  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   cudaFree(c->d_pyr);
   cudaFree(c->d_part);
   cudaFree(c->d_scores);
@@ -404,57 +401,16 @@ SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int c
 
 SS2_API void ss2_msssim_destroy(ss2_msssim *ctx) { msssim_free(ctx); }
 
-// Records the start (start = true) or end event of one launch of kernel
-// class cls while profiling.
-static cudaError_t msssim_mark(ss2_msssim *c, int cls, bool start, cudaStream_t st) {
-  if (!c->prof) return cudaSuccess;
-  size_t idx;
-  if (start) {
-    idx = c->ev_used.size() * 2;
-    while (c->ev_pool.size() < idx + 2) {
-      cudaEvent_t e;
-      cudaError_t r = cudaEventCreate(&e);
-      if (r != cudaSuccess) return r;
-      c->ev_pool.push_back(e);
-    }
-    c->ev_used.push_back({cls, (int)idx});
-  } else {
-    idx = (size_t)c->ev_used.back().second + 1;
-  }
-  return cudaEventRecord(c->ev_pool[idx], st);
-}
-
 SS2_API int ss2_msssim_profile_begin(ss2_msssim *ctx) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  ctx->prof = true;
-  ctx->ev_used.clear();
+  ctx->timer.begin();
   return 0;
 }
 
 SS2_API int ss2_msssim_profile_end(ss2_msssim *ctx, double *ms, int *launches) {
   if (!ctx) return fail(SS2_EINVAL, "NULL context");
-  double t[2] = {0, 0};
-  int n[2] = {0, 0};
-  for (const auto &u : ctx->ev_used) {
-    cudaError_t e = cudaEventSynchronize(ctx->ev_pool[u.second + 1]);
-    float dt = 0.0f;
-    if (e == cudaSuccess)
-      e = cudaEventElapsedTime(&dt, ctx->ev_pool[u.second], ctx->ev_pool[u.second + 1]);
-    if (e != cudaSuccess) {
-      ctx->prof = false;
-      ctx->ev_used.clear();
-      return cuda_fail(e, "MS-SSIM profile events");
-    }
-    t[u.first] += dt;
-    n[u.first] += 1;
-  }
-  ctx->prof = false;
-  ctx->ev_used.clear();
-  for (int i = 0; i < 2; ++i) {
-    if (ms) ms[i] = t[i];
-    if (launches) launches[i] = n[i];
-  }
-  return 0;
+  const cudaError_t e = ctx->timer.finish(2, ms, launches);
+  return e == cudaSuccess ? 0 : cuda_fail(e, "MS-SSIM profile events");
 }
 
 // The five scale launches and the final one for nb frames.
@@ -463,7 +419,7 @@ static cudaError_t msssim_batch(ss2_msssim *c, const uint8_t *ref, const uint8_t
   const MGeom &g = c->g;
   cudaError_t e = cudaSuccess;
   for (int j = 0; j < kScales && e == cudaSuccess; ++j) {
-    e = msssim_mark(c, 0, true, st);
+    e = c->timer.mark(0, true, st);
     if (e != cudaSuccess) break;
     const dim3 grid(g.tx[j], g.ty[j], nb);
     if (j > 0)
@@ -473,14 +429,14 @@ static cudaError_t msssim_batch(ss2_msssim *c, const uint8_t *ref, const uint8_t
     else
       k_msssim_level<1><<<grid, 256, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
     e = cudaGetLastError();
-    if (e == cudaSuccess) e = msssim_mark(c, 0, false, st);
+    if (e == cudaSuccess) e = c->timer.mark(0, false, st);
   }
-  if (e == cudaSuccess) e = msssim_mark(c, 1, true, st);
+  if (e == cudaSuccess) e = c->timer.mark(1, true, st);
   if (e == cudaSuccess) {
     k_msssim_final<<<nb, kScales * kQ * 32, 0, st>>>(g, c->d_part, c->d_scores, c->d_values);
     e = cudaGetLastError();
   }
-  if (e == cudaSuccess) e = msssim_mark(c, 1, false, st);
+  if (e == cudaSuccess) e = c->timer.mark(1, false, st);
   return e;
 }
 

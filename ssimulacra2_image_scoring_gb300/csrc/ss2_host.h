@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <cstddef>
+#include <utility>
+#include <vector>
 
 #include "ss2_impl.h"
 
@@ -30,5 +32,75 @@ void build_eotf(float *table);                            // kEotfN + 1 floats
 void build_eotf_pairs(float *pairs);                      // 2 * kEotfN floats
 int norm_entries(int depth);                              // 256 or 65536
 void build_norm(int depth, float *ynorm, float *cnorm);   // norm_entries(depth) each
+
+// Per-kernel CUDA-event timing of one context (the ss2*_profile_begin /
+// _end entry points): while on, each launch is bracketed by a pair of events
+// recorded on its own stream; finish() waits for them and adds the elapsed
+// times per kernel class.  The events are created on first use and reused.
+class KernelTimer {
+ public:
+  KernelTimer() = default;
+  KernelTimer(const KernelTimer &) = delete;
+  KernelTimer &operator=(const KernelTimer &) = delete;
+  ~KernelTimer() {
+    for (cudaEvent_t e : pool_) cudaEventDestroy(e);
+  }
+
+  void begin() {
+    on_ = true;
+    used_.clear();
+  }
+
+  // Records the start (start = true) or end event of one launch of class cls.
+  cudaError_t mark(int cls, bool start, cudaStream_t st) {
+    if (!on_) return cudaSuccess;
+    size_t idx;
+    if (start) {
+      idx = used_.size() * 2;
+      while (pool_.size() < idx + 2) {
+        cudaEvent_t e;
+        const cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) return r;
+        pool_.push_back(e);
+      }
+      used_.push_back({cls, idx});
+    } else {
+      if (used_.empty()) return cudaErrorInvalidValue;
+      idx = used_.back().second + 1;
+    }
+    return cudaEventRecord(pool_[idx], st);
+  }
+
+  // Sums per class into ms[0..ncls) and launches[0..ncls) (either may be
+  // NULL) and stops timing, also on failure.
+  cudaError_t finish(int ncls, double *ms, int *launches) {
+    std::vector<double> t((size_t)ncls, 0.0);
+    std::vector<int> n((size_t)ncls, 0);
+    cudaError_t e = cudaSuccess;
+    for (const auto &u : used_) {
+      e = cudaEventSynchronize(pool_[u.second + 1]);
+      float dt = 0.0f;
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&dt, pool_[u.second], pool_[u.second + 1]);
+      if (e != cudaSuccess) break;
+      if (u.first >= 0 && u.first < ncls) {
+        t[(size_t)u.first] += dt;
+        n[(size_t)u.first] += 1;
+      }
+    }
+    on_ = false;
+    used_.clear();
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < ncls; ++i) {
+      if (ms) ms[i] = t[(size_t)i];
+      if (launches) launches[i] = n[(size_t)i];
+    }
+    return cudaSuccess;
+  }
+
+ private:
+  bool on_ = false;
+  std::vector<cudaEvent_t> pool_;
+  std::vector<std::pair<int, size_t>> used_;  // (kernel class, index of the start event)
+};
 
 }  // namespace ss2

@@ -193,8 +193,49 @@ def _stream_handle(stream) -> int | None:
     return stream.cuda_stream
 
 
-class FloatSSIM:
+class _Context:
+    """Lifetime and per-kernel profiling shared by the context classes: the
+    C entry points are <prefix>_destroy, <prefix>_profile_begin and
+    <prefix>_profile_end."""
+
+    _PREFIX = ""
+    KERNELS: tuple = ()
+    _h = None
+
+    def profile_begin(self) -> None:
+        """Starts per-kernel CUDA-event timing of this context's launches."""
+        _check(getattr(lib(), self._PREFIX + "_profile_begin")(self._h))
+
+    def profile_end(self) -> dict:
+        """Stops timing; returns {kernel: (total ms, launches)}."""
+        ms = np.zeros(len(self.KERNELS), np.float64)
+        n = np.zeros(len(self.KERNELS), np.int32)
+        _check(getattr(lib(), self._PREFIX + "_profile_end")(self._h, ms.ctypes.data,
+                                                             n.ctypes.data))
+        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
+
+    def close(self) -> None:
+        if self._h:
+            getattr(lib(), self._PREFIX + "_destroy")(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+class FloatSSIM(_Context):
     """float_ssim with device decimation for one frame geometry (ss2_fssim_create)."""
+
+    _PREFIX = "ss2_fssim"
+    KERNELS = ("k_fssim_decimate", "k_fssim_map", "k_fssim_final")
 
     def __init__(self, width: int, height: int, bitdepth: int, chroma: int, batch: int = 0):
         h = lib().ss2_fssim_create(width, height, bitdepth, chroma, batch)
@@ -225,40 +266,11 @@ class FloatSSIM:
                                                out.ctypes.data, _stream_handle(stream)))
         return out
 
-    KERNELS = ("k_fssim_decimate", "k_fssim_map", "k_fssim_final")
 
-    def profile_begin(self) -> None:
-        """Starts per-kernel CUDA-event timing of this context's launches."""
-        _check(lib().ss2_fssim_profile_begin(self._h))
-
-    def profile_end(self) -> dict:
-        """Stops timing; returns {kernel: (total ms, launches)}."""
-        ms = np.zeros(3, np.float64)
-        n = np.zeros(3, np.int32)
-        _check(lib().ss2_fssim_profile_end(self._h, ms.ctypes.data, n.ctypes.data))
-        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
-
-    def close(self) -> None:
-        if self._h:
-            lib().ss2_fssim_destroy(self._h)
-            self._h = None
-
-    def __enter__(self):
-        return self
-
-    def __exit__(self, *exc):
-        self.close()
-
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
-
-
-class Cambi:
+class Cambi(_Context):
     """CAMBI c-values and top-K pooling for one plane size (ss2_cambi_create)."""
 
+    _PREFIX = "ss2_cambi"
     KERNELS = ("k_cambi_cvalues", "k_cambi_topk")
 
     def __init__(self, width: int, height: int, window: int, diffs, weights, batch: int = 0):
@@ -319,38 +331,14 @@ class Cambi:
                                     _stream_handle(stream)))
         return self._result(s, t, m)
 
-    def profile_begin(self) -> None:
-        _check(lib().ss2_cambi_profile_begin(self._h))
 
-    def profile_end(self) -> dict:
-        ms = np.zeros(2, np.float64)
-        n = np.zeros(2, np.int32)
-        _check(lib().ss2_cambi_profile_end(self._h, ms.ctypes.data, n.ctypes.data))
-        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
-
-    def close(self) -> None:
-        if self._h:
-            lib().ss2_cambi_destroy(self._h)
-            self._h = None
-
-    def __enter__(self):
-        return self
-
-    def __exit__(self, *exc):
-        self.close()
-
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
-
-
-class MSSSIM:
+class MSSSIM(_Context):
     """MS-SSIM of the luma plane for one frame geometry (ss2_msssim_create)."""
 
-    SCALES = 5
+    _PREFIX = "ss2_msssim"
     KERNELS = ("k_msssim_level", "k_msssim_final")
+
+    SCALES = 5
 
     def __init__(self, width: int, height: int, bitdepth: int, chroma: int, batch: int = 0):
         h = lib().ss2_msssim_create(width, height, bitdepth, chroma, batch)
@@ -397,35 +385,12 @@ class MSSSIM:
             out.append(planes)
         return out[0], out[1]
 
-    def profile_begin(self) -> None:
-        _check(lib().ss2_msssim_profile_begin(self._h))
 
-    def profile_end(self) -> dict:
-        ms = np.zeros(2, np.float64)
-        n = np.zeros(2, np.int32)
-        _check(lib().ss2_msssim_profile_end(self._h, ms.ctypes.data, n.ctypes.data))
-        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
-
-    def close(self) -> None:
-        if self._h:
-            lib().ss2_msssim_destroy(self._h)
-            self._h = None
-
-    def __enter__(self):
-        return self
-
-    def __exit__(self, *exc):
-        self.close()
-
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
-
-
-class Scorer:
+class Scorer(_Context):
     """A scoring context for one frame geometry (ss2_create)."""
+
+    _PREFIX = "ss2"
+    KERNELS = ("k_pyramid", "k_hblur", "k_vblur", "k_finalize")
 
     def __init__(self, width: int, height: int, bitdepth: int, chroma: int,
                  batch: int | None = None, params: np.ndarray | None = None):
@@ -532,32 +497,4 @@ class Scorer:
                                       xyb.ctypes.data, hb.ctypes.data, _stream_handle(stream)))
         return xyb, hb
 
-    KERNELS = ("k_pyramid", "k_hblur", "k_vblur", "k_finalize")
 
-    def profile_begin(self) -> None:
-        """Starts per-kernel CUDA-event timing of this context's launches."""
-        _check(lib().ss2_profile_begin(self.handle))
-
-    def profile_end(self) -> dict:
-        """Stops timing; returns {kernel: (total ms, launches)}."""
-        ms = np.zeros(4, np.float64)
-        n = np.zeros(4, np.int32)
-        _check(lib().ss2_profile_end(self.handle, ms.ctypes.data, n.ctypes.data))
-        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.KERNELS)}
-
-    def close(self) -> None:
-        if self._h:
-            lib().ss2_destroy(self._h)
-            self._h = None
-
-    def __enter__(self):
-        return self
-
-    def __exit__(self, *exc):
-        self.close()
-
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
