@@ -21,8 +21,8 @@ L2.  Per-kernel CUDA events inside the library give the dominant kernel's
 average launch time for the roofline; nvidia-smi samples the clocks during
 the timed region; e2e repeats the measurement through the host-input entry
 point with pinned host buffers (upload and 8-byte-per-frame read-back
-inside the timed region).  The oracle, timed on the host cores over a
-bounded sample, is the CPU baseline.
+inside the timed region; the median of three windows of K steps).  The
+oracle, timed on the host cores over a bounded sample, is the CPU baseline.
 
 --impl reference: the oracle (plain single-threaded C, one thread per frame
 across the host cores) on a bounded sample per step; the same metric.
@@ -380,13 +380,18 @@ def run_ours(args, ws, rank, local):
     pr = torch.from_numpy(wl.ref).pin_memory()
     pd = torch.from_numpy(wl.dis).pin_memory()
     sc.score_host(pr, pd, stream)  # allocates the upload slots once
-    barrier(ws)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(max(1, args.steps)):
-        sc.score_host(pr, pd, stream)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, ws)
+    # the host's memory is shared with other jobs on the machine: the median
+    # of three timed windows of K calls each
+    windows = []
+    for _ in range(3):
+        barrier(ws)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(max(1, args.steps)):
+            sc.score_host(pr, pd, stream)
+        torch.cuda.synchronize()
+        windows.append(max_over_ranks(time.perf_counter() - t0, ws))
+    e2e_s = statistics.median(windows)
     e2e_fps = n * ws * max(1, args.steps) / e2e_s
 
     cpu = None
@@ -422,7 +427,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clk,
         "e2e": {"value": e2e_fps, "unit": "frames/s",
                 "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
-                "d2h_bytes_per_step": 8 * n},
+                "d2h_bytes_per_step": 8 * n, "windows_s": windows},
         "gpu_launches": gpu_launches,
         "cpu_baseline": cpu,
         "scores_head": [float(x) for x in scores[:3]],
