@@ -323,9 +323,9 @@ void ss2_msssim_destroy(ss2_msssim *ctx);
  *     S = sum(v > T) + (k - #(v > T)) T in units of 2^-24 (128 bits), the
  *     mean S 2^-24 / k in fp64.
  *   ss2_cambi_create: window odd with window^2 <= 4225 (at most 65), 1..4
- *     (diff, weight) pairs (diff 1..1023, weight 1..9), max_batch 0 = 16
- *     planes per pass (at most 1024).  NULL with -EINVAL for bad arguments,
- *     -ENOMEM.
+ *     (diff, weight) pairs (diff 1..1023, weight 1..9), max_batch 0 = as
+ *     many planes per pass as 2 GB of c-values hold, 1 to 64 (at most 1024
+ *     when given).  NULL with -EINVAL for bad arguments, -ENOMEM.
  *   ss2_cambi_cvalues: levels (and mask, or NULL) DEVICE, n_planes planes;
  *     cvalues DEVICE floats, n_planes planes.  -EINVAL for a level >= 1024.
  *   ss2_cambi_topk: cvalues DEVICE (values 0 or on the 2^-24 grid below

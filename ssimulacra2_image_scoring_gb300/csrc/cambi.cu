@@ -12,13 +12,18 @@
 // (d, w) pairs with the largest term taken, the reciprocal 1/n rounded to
 // nearest (__frcp_rn), the pool the mean of the exact sum.
 //
+//   k_cambi_present  the levels that occur in each plane (1024-bit maps).
 //   k_cambi_cvalues  one warp per 32 columns of a plane; lane = column.  Each
 //                    step the warp stages the leaving and entering row
 //                    segments in shared memory (fetched one step ahead); the
-//                    lane's window histogram (1024 bins of 16 bits,
-//                    interleaved by lane so each lane owns its elements) is
-//                    updated with plain loads and stores, a column whose
-//                    leaving and entering pixels agree being skipped.
+//                    lane's window histogram (16-bit bins interleaved by lane
+//                    so each lane owns its elements) is updated with plain
+//                    loads and stores, a column whose leaving and entering
+//                    pixels agree being skipped.  Planes with at most 256
+//                    distinct levels (8-bit video as 10-bit levels) index
+//                    bins by the level's rank among those present: 16 KB
+//                    per warp instead of 64 KB, four times the warps per
+//                    SM.
 //   k_cambi_hist     radix histogram of one 11/11/10-bit digit of the values
 //                    that match the digits chosen so far.
 //   k_cambi_select   one block per plane: the digit holding the k-th largest
@@ -47,6 +52,7 @@ using namespace ss2;
 constexpr int kLevels = 1024;
 constexpr int kMaxWin2 = 4225;
 constexpr int kCvSmem = kLevels * 32 * 2;          // 64 KB: 1024 bins x 32 lanes x 16 bits
+constexpr int kCvSmemCompact = 256 * 32 * 2;      // 16 KB: the compact histogram
 constexpr int kErrLevel = 2;                       // a level >= 1024 was seen
 constexpr int kErrValue = 4;                       // a value off the 2^-24 grid or >= 2^14
 constexpr int kSumThreads = 256;
@@ -59,37 +65,84 @@ struct CGeom {
   int sum_blocks;           // per plane
 };
 
-// Histogram bin of level v for lane l: the 16-bit element v * 32 + l, which
-// only that lane touches (plain loads and stores; shared-memory order within
-// a thread keeps successive updates of one bin correct).  A count stays in
-// 0..4225.
-__device__ __forceinline__ unsigned hist_get(const uint16_t *hist, int v, int lane) {
-  return hist[v * 32 + lane];
-}
-
 constexpr int kSeg = 32 + 64;                      // a row's window columns for 32 lanes
 constexpr unsigned kSkip = 0xFFFFu;                // outside the plane or not counted
 constexpr int kBatch = 16;                         // columns whose levels are read ahead
+constexpr int kCompactBins = 256;                  // the compact histogram's bins
 
+// Which of the 1024 levels occur in each plane (a 1024-bit map per plane,
+// levels >= 1024 ignored: the c-value kernel reports them).
+__global__ void __launch_bounds__(256)
+    k_cambi_present(CGeom g, const uint16_t *__restrict__ levels, unsigned *__restrict__ present) {
+  __shared__ unsigned bits[kLevels / 32];
+  const int t = threadIdx.x;
+  if (t < kLevels / 32) bits[t] = 0u;
+  __syncthreads();
+  const uint16_t *L = levels + (long long)blockIdx.y * g.plane;
+  for (long long i = (long long)blockIdx.x * blockDim.x + t; i < g.plane;
+       i += (long long)gridDim.x * blockDim.x) {
+    const unsigned v = __ldg(L + i);
+    if (v < kLevels) atomicOr(&bits[v >> 5], 1u << (v & 31));
+  }
+  __syncthreads();
+  if (t < kLevels / 32 && bits[t]) atomicOr(&present[blockIdx.y * (kLevels / 32) + t], bits[t]);
+}
+
+// k_cambi_cvalues<BINS>: one warp per 32 output columns of a plane; lane =
+// column.  Each lane owns a window histogram of BINS 16-bit bins (element
+// bin * 32 + lane, plain loads and stores; a count stays in 0..4225).  With
+// BINS = 256 a level is replaced by its rank among the levels present in the
+// plane (8-bit video as 10-bit levels has at most 256), which cuts the
+// histogram to 16 KB per warp; planes with more levels run the BINS = 1024
+// variant, which uses the levels themselves.  Both variants are launched;
+// a block whose plane belongs to the other one returns at once.  Each step
+// the warp stages the leaving and entering row segments in shared memory
+// (fetched one step ahead); a column whose two pixels agree is skipped.
+template <int BINS>
 __global__ void __launch_bounds__(32)
     k_cambi_cvalues(CGeom g, const uint16_t *__restrict__ levels, const uint8_t *__restrict__ mask,
-                    float *__restrict__ out, int *__restrict__ err) {
-  extern __shared__ uint16_t cv_hist[];            // kLevels x 32 lanes
-  // the leaving and entering row segments of the current step: columns
-  // x0 - r .. x0 + 31 + r (kSkip where outside the plane or not counted)
+                    const unsigned *__restrict__ present, float *__restrict__ out,
+                    int *__restrict__ err) {
+  extern __shared__ uint16_t cv_hist[];            // BINS x 32 lanes
   __shared__ uint16_t seg[2][kSeg];
+  __shared__ unsigned pbits[kLevels / 32];         // levels present in the plane
+  __shared__ unsigned prank[kLevels / 32];         // present levels below each word
   const int lane = threadIdx.x;
+  const unsigned *pp = present + blockIdx.y * (kLevels / 32);
+  {
+    const unsigned b = pp[lane];
+    unsigned r = __popc(b);
+    // exclusive prefix of the popcounts over the 32 words, in lane order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned u = __shfl_up_sync(0xffffffffu, r, o);
+      if (lane >= o) r += u;
+    }
+    pbits[lane] = b;
+    prank[lane] = r - __popc(b);
+    const unsigned total = __shfl_sync(0xffffffffu, r, 31);
+    if ((BINS == kCompactBins) != (total <= (unsigned)kCompactBins)) return;   // the other variant's
+  }
+  __syncwarp();
+  // histogram index of level v (v < 1024): its rank among the present
+  // levels (BINS = 256) or v itself; kSkip when v does not occur
+  auto bin = [&](unsigned v) -> unsigned {
+    if (BINS == kLevels) return v;
+    const unsigned w = pbits[v >> 5], m = 1u << (v & 31);
+    return (w & m) ? prank[v >> 5] + __popc(w & (m - 1u)) : kSkip;
+  };
   const int x0 = blockIdx.x * 32, x = x0 + lane;
   const long long base = (long long)blockIdx.y * g.plane;
   const uint16_t *L = levels + base;
   const uint8_t *M = mask ? mask + base : nullptr;
-  for (int i = lane; i < kLevels * 32; i += 32) cv_hist[i] = 0u;
+  for (int i = lane; i < BINS * 32; i += 32) cv_hist[i] = 0u;
   const int r = g.window / 2;
   const int nseg = 32 + 2 * r;
   const bool col = x < g.w;
   bool bad = false;
-  // the segment values of row yy (kSkip for rows outside the plane): three
-  // per lane, loaded together
+  // the histogram indices of row yy's segment (kSkip for rows outside the
+  // plane, pixels not counted, levels >= 1024): three per lane, loaded
+  // together
   auto fetch = [&](int yy, unsigned (&v)[3]) {
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
@@ -98,12 +151,9 @@ __global__ void __launch_bounds__(32)
       if (i < nseg && yy >= 0 && yy < g.h && xx >= 0 && xx < g.w) {
         const long long at = (long long)yy * g.w + xx;
         if (!M || __ldg(M + at)) {
-          unsigned lv = __ldg(L + at);
-          if (lv >= kLevels) {
-            bad = true;
-            lv = kLevels - 1;              // stays in bounds; the call reports -EINVAL
-          }
-          v[j] = lv;
+          const unsigned lv = __ldg(L + at);
+          if (lv >= kLevels) bad = true;        // skipped; the call reports -EINVAL
+          else v[j] = bin(lv);
         }
       }
     }
@@ -114,7 +164,7 @@ __global__ void __launch_bounds__(32)
       if (lane + 32 * j < kSeg) seg[s_][lane + 32 * j] = (uint16_t)v[j];
   };
   // the lane's window columns lane .. lane + 2r: remove seg[0], add seg[1]
-  // (a column whose two pixels agree is skipped); the levels of kBatch
+  // (a column whose two pixels agree is skipped); the indices of kBatch
   // columns are read before their updates
   auto apply = [&](bool remove) {
     for (int i0 = 0; i0 <= 2 * r; i0 += kBatch) {
@@ -164,20 +214,22 @@ __global__ void __launch_bounds__(32)
       const long long at = (long long)y * g.w + x;
       float best = 0.0f;
       if (!M || __ldg(M + at)) {
-        int lv = __ldg(L + at);
+        const unsigned lv = __ldg(L + at);
         if (lv >= kLevels) {
           bad = true;
-          lv = kLevels - 1;
-        }
-        const unsigned p0 = hist_get(cv_hist, lv, lane);
+        } else {
+          const unsigned p0 = cv_hist[bin(lv) * 32 + lane];   // the pixel's own level occurs
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (i >= g.ndiff || lv + g.diffs[i] >= kLevels) continue;
-          const unsigned pm = hist_get(cv_hist, lv + g.diffs[i], lane);
-          if (pm == 0u) continue;
-          const float c = __fmul_rn((float)((unsigned)g.weights[i] * p0 * pm),
-                                    __frcp_rn((float)(p0 + pm)));
-          best = fmaxf(best, c);
+          for (int i = 0; i < 4; ++i) {
+            if (i >= g.ndiff || lv + g.diffs[i] >= kLevels) continue;
+            const unsigned bm = bin(lv + g.diffs[i]);
+            if (bm == kSkip) continue;
+            const unsigned pm = cv_hist[bm * 32 + lane];
+            if (pm == 0u) continue;
+            const float c = __fmul_rn((float)((unsigned)g.weights[i] * p0 * pm),
+                                      __frcp_rn((float)(p0 + pm)));
+            best = fmaxf(best, c);
+          }
         }
       }
       out[base + at] = best;
@@ -342,6 +394,7 @@ struct ss2_cambi {
   float *d_thr = nullptr;
   double *d_means = nullptr;
   int *d_err = nullptr, *h_err = nullptr;
+  unsigned *d_present = nullptr;            // levels present, a 1024-bit map per plane
   unsigned long long *h_sums = nullptr;
   float *h_thr = nullptr;
   double *h_means = nullptr;
@@ -359,6 +412,7 @@ static void cambi_free(ss2_cambi *c) {
   cudaFree(c->d_thr);
   cudaFree(c->d_means);
   cudaFree(c->d_err);
+  cudaFree(c->d_present);
   if (c->h_err) cudaFreeHost(c->h_err);
   if (c->h_sums) cudaFreeHost(c->h_sums);
   if (c->h_thr) cudaFreeHost(c->h_thr);
@@ -406,10 +460,13 @@ SS2_API ss2_cambi *ss2_cambi_create(int width, int height, int window, int ndiff
   }
   c->g = g;
   c->device = dev;
-  c->batch = max_batch ? max_batch : 16;
+  // default: as many planes as 2 GB of c-values hold, 1 to 64
+  c->batch = max_batch ? max_batch
+                       : (int)std::max<long long>(1, std::min<long long>(64, (2LL << 30) / (g.plane * 4)));
   const size_t B = (size_t)c->batch;
-  if (cudaFuncSetAttribute(k_cambi_cvalues, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kCvSmem) != cudaSuccess ||
+  if (cudaFuncSetAttribute(k_cambi_cvalues<kLevels>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kCvSmem) != cudaSuccess ||
+      cudaMalloc(&c->d_present, B * (kLevels / 32) * sizeof(unsigned)) != cudaSuccess ||
       cudaMalloc(&c->d_c, B * g.plane * sizeof(float)) != cudaSuccess ||
       cudaMalloc(&c->d_st, B * sizeof(RState)) != cudaSuccess ||
       cudaMalloc(&c->d_hist, B * 2048 * sizeof(unsigned)) != cudaSuccess ||
@@ -449,8 +506,25 @@ static cudaError_t cambi_cv_launch(ss2_cambi *c, const uint16_t *levels, const u
   const CGeom &g = c->g;
   cudaError_t e = c->timer.mark(0, true, st);
   if (e != cudaSuccess) return e;
-  k_cambi_cvalues<<<dim3((g.w + 31) / 32, nb), 32, kCvSmem, st>>>(g, levels, mask, out, c->d_err);
-  e = cudaGetLastError();
+  // which levels occur, then both histogram variants (each block keeps or
+  // leaves its plane by the count of levels present)
+  e = cudaMemsetAsync(c->d_present, 0, (size_t)nb * (kLevels / 32) * sizeof(unsigned), st);
+  if (e == cudaSuccess) {
+    const int pblocks = std::max(1, std::min(64, (int)((g.plane + 8191) / 8192)));
+    k_cambi_present<<<dim3(pblocks, nb), 256, 0, st>>>(g, levels, c->d_present);
+    e = cudaGetLastError();
+  }
+  const dim3 grid((g.w + 31) / 32, nb);
+  if (e == cudaSuccess) {
+    k_cambi_cvalues<kCompactBins><<<grid, 32, kCvSmemCompact, st>>>(g, levels, mask, c->d_present,
+                                                                   out, c->d_err);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    k_cambi_cvalues<kLevels><<<grid, 32, kCvSmem, st>>>(g, levels, mask, c->d_present, out,
+                                                       c->d_err);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) e = c->timer.mark(0, false, st);
   return e;
 }

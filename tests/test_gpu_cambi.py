@@ -108,3 +108,22 @@ def test_errors(cuda):
         ok = torch.from_numpy(np.zeros((1, 48, 64), np.uint16)).cuda()
         sums, thr, means = cb.pool(ok, 10)                 # the context stays usable
         assert sums == [0] and thr[0] == 0.0 and means[0] == 0.0
+
+
+def test_wide_and_narrow_level_sets_in_one_call(cuda):
+    """Planes with more than 256 distinct levels take the 1024-bin kernel and
+    the others the compact one; one call may hold both."""
+    import torch
+
+    from ssimulacra2_image_scoring_gb300 import Cambi
+    h, w, win, d, wt = 90, 150, 17, [1, 2], [1, 3]
+    wide = _levels(h, w, 1, base=512, spread=120)
+    narrow = _levels(h, w, 2)
+    assert len(np.unique(wide)) > 256 and len(np.unique(narrow)) <= 256
+    lv = np.ascontiguousarray(np.stack([wide, narrow, wide]))
+    with Cambi(w, h, win, d, wt) as cb:
+        cv = cb.cvalues(torch.from_numpy(lv).cuda()).cpu().numpy()
+    for f in range(3):
+        want = oracle.cambi_cvalues(lv[f], win, d, wt)
+        assert np.array_equal(cv[f].view(np.uint32), want.view(np.uint32)), f
+        assert np.any(want > 0)
