@@ -485,24 +485,27 @@ __global__ void __launch_bounds__(256)
   const int t = threadIdx.x;
   // per-tile offset: the reference sample at the tile origin (same for both)
   const float off = pa[(long long)oy0 * g.pitch + ox0];
-  // every load of a thread is issued before the first is used
-  constexpr int kPer = (kInY * kInX + 255) / 256;
+  // every load of a thread is issued before the first is used; thread
+  // t < 252 takes column t % 42 and rows t / 42, + 6, + 12, ...
+  constexpr int kRowStep = 256 / kInX;                   // 6
+  constexpr int kPer = (kInY + kRowStep - 1) / kRowStep;   // 5
+  const int c = t % kInX, r0 = t / kInX;
+  const bool loader = t < kRowStep * kInX;
+  const int xc = min(ox0 + c, g.wd - 1);
   float va[kPer], vb[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int i = t + 256 * k;
-    if (i < kInY * kInX) {
-      const int r = i / kInX, c = i % kInX;
-      const int y = min(oy0 + r, g.hd - 1), x = min(ox0 + c, g.wd - 1);
-      va[k] = pa[(long long)y * g.pitch + x];
-      vb[k] = pb[(long long)y * g.pitch + x];
+    const int r = r0 + kRowStep * k;
+    if (loader && r < kInY) {
+      const long long at = (long long)min(oy0 + r, g.hd - 1) * g.pitch + xc;
+      va[k] = pa[at];
+      vb[k] = pb[at];
     }
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int i = t + 256 * k;
-    if (i < kInY * kInX) {
-      const int r = i / kInX, c = i % kInX;
+    const int r = r0 + kRowStep * k;
+    if (loader && r < kInY) {
       const float p = __fsub_rn(va[k], off);
       const float q = __fsub_rn(vb[k], off);
       PP[0][r][c] = f2_pack(p, q);

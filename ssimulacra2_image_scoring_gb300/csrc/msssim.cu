@@ -127,23 +127,26 @@ __global__ void __launch_bounds__(256)
   // input tile (clamped to the plane), shifted by the tile's first reference
   // sample; every load of a thread is issued before the first is used
   const float off = sample<MODE>(g, j, ra, pa, ox0, oy0);
-  constexpr int kPer = (kIY * kIX + 255) / 256;
+  // thread t < 252 takes column t % 42 and rows t / 42, + 6, + 12, ...
+  constexpr int kRowStep = 256 / kIX;                  // 6
+  constexpr int kPer = (kIY + kRowStep - 1) / kRowStep;  // 5
+  const int c = t % kIX, r0 = t / kIX;
+  const bool loader = t < kRowStep * kIX;
+  const int xc = min(ox0 + c, W - 1);
   float va[kPer], vb[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int i = t + 256 * k;
-    if (i < kIY * kIX) {
-      const int r = i / kIX, c = i % kIX;
-      const int y = min(oy0 + r, Hh - 1), x = min(ox0 + c, W - 1);
-      va[k] = sample<MODE>(g, j, ra, pa, x, y);
-      vb[k] = sample<MODE>(g, j, rb, pb, x, y);
+    const int r = r0 + kRowStep * k;
+    if (loader && r < kIY) {
+      const int y = min(oy0 + r, Hh - 1);
+      va[k] = sample<MODE>(g, j, ra, pa, xc, y);
+      vb[k] = sample<MODE>(g, j, rb, pb, xc, y);
     }
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int i = t + 256 * k;
-    if (i < kIY * kIX) {
-      const int r = i / kIX, c = i % kIX;
+    const int r = r0 + kRowStep * k;
+    if (loader && r < kIY) {
       const float p = __fsub_rn(va[k], off);     // exact: both lie on the same grid below 256
       const float q = __fsub_rn(vb[k], off);
       PP[0][r][c] = f2_pack(p, q);
