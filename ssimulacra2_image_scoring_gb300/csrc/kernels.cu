@@ -38,13 +38,18 @@ constexpr int kPyrThreads = 256;
 __host__ __device__ constexpr int lvl_off(int s) { return (4096 - (4096 >> (2 * s))) / 3; }
 constexpr int kLvlTotal = lvl_off(kMaxScales);
 
-__device__ __forceinline__ int read_sample(const uint8_t *__restrict__ p, long long i,
-                                           int bps) {
-  if (bps == 1) return p[i];
-  const uint16_t *q = reinterpret_cast<const uint16_t *>(p);
-  return q[i];
+// One sample of BPS bytes (8-bit, or 16-bit little-endian words) at index i.
+template <int BPS>
+__device__ __forceinline__ int read_sample(const uint8_t *__restrict__ p, int i) {
+  if (BPS == 1) return p[i];
+  return reinterpret_cast<const uint16_t *>(p)[i];
 }
 
+// Index arithmetic is 32-bit inside a frame: a plane holds at most
+// 16384 x 16384 samples and the byte offset of a V sample stays below
+// 2 x 1.5 x 2^28; each scale's XYB block is reached from a 64-bit base and
+// its six planes lie within 6 x 2^28 floats of it.
+template <int BPS>
 __global__ void __launch_bounds__(kPyrThreads)
     k_pyramid(Geom g, Pix px, PyrTabs tabs, const uint8_t *__restrict__ ref,
               const uint8_t *__restrict__ dis, float *__restrict__ X) {
@@ -67,7 +72,9 @@ __global__ void __launch_bounds__(kPyrThreads)
                                 dis + (long long)frame * g.frame_bytes};
     const int k = 1 << (g.depth - 8);
     const float dy = (float)(219 * k), dc = (float)(224 * k);
-    const long long ysz = (long long)g.w * g.h, csz = (long long)g.cw * g.ch;
+    const int ysz = g.w * g.h, csz = g.cw * g.ch;
+    float *P0 = Xf + g.xoff[0];
+    const int plane0 = (int)g.plane[0], pitch0 = g.pitch[0];
     for (int p = threadIdx.x; p < kTile * kTile; p += kPyrThreads) {
       const int lx = p & (kTile - 1), ly = p / kTile;
       const int x = tx0 + lx, y = ty0 + ly;
@@ -76,13 +83,15 @@ __global__ void __launch_bounds__(kPyrThreads)
         for (int c = 0; c < 6; ++c) L[c][p] = 0.0f;
         continue;
       }
-      const long long ci = (long long)(y >> g.sy) * g.cw + (x >> g.sx);
+      const int yi = y * g.w + x;
+      const int ci = (y >> g.sy) * g.cw + (x >> g.sx);
+      float *P = P0 + (y * pitch0 + x);
 #pragma unroll
       for (int img = 0; img < 2; ++img) {
         const uint8_t *f = frames[img];
-        const int Ys = read_sample(f, (long long)y * g.w + x, g.bps);
-        const int Us = read_sample(f + ysz * g.bps, ci, g.bps);
-        const int Vs = read_sample(f + (ysz + csz) * g.bps, ci, g.bps);
+        const int Ys = read_sample<BPS>(f, yi);
+        const int Us = read_sample<BPS>(f, ysz + ci);
+        const int Vs = read_sample<BPS>(f, ysz + csz + ci);
         float yn, cbv, crv;
         if (tabs.ynorm) {
           yn = __ldg(tabs.ynorm + Ys);
@@ -104,10 +113,9 @@ __global__ void __launch_bounds__(kPyrThreads)
         L[3 * img + 2][p] = B;
         float xo, yo, bo;
         pixel_xyb(px, cb, R, G, B, xo, yo, bo);
-        float *P = Xf + g.xoff[0] + (long long)y * g.pitch[0] + x;
-        P[(3 * img + 0) * g.plane[0]] = xo;
-        P[(3 * img + 1) * g.plane[0]] = yo;
-        P[(3 * img + 2) * g.plane[0]] = bo;
+        P[(3 * img + 0) * plane0] = xo;
+        P[(3 * img + 1) * plane0] = yo;
+        P[(3 * img + 2) * plane0] = bo;
       }
     }
   }
@@ -115,13 +123,16 @@ __global__ void __launch_bounds__(kPyrThreads)
 
   // ---- scales 1..: downsample linear RGB inside the tile, then XYB ----
   for (int s = 1; s < g.nscales; ++s) {
-    const int tw = kTile >> s;
+    const int lw = 5 - s;                               // log2 of the tile edge at scale s
+    const int tw = 1 << lw;
     const int ox = tx0 >> s, oy = ty0 >> s;            // tile origin at scale s
     const int pox = tx0 >> (s - 1), poy = ty0 >> (s - 1);  // at scale s-1
-    const int pw = kTile >> (s - 1);
+    const int pw = 2 * tw;
     const int ww = g.ws[s - 1], hh = g.hs[s - 1];
+    float *Ps = Xf + g.xoff[s];
+    const int planes = (int)g.plane[s], pitchs = g.pitch[s];
     for (int p = threadIdx.x; p < tw * tw; p += kPyrThreads) {
-      const int lx = p % tw, ly = p / tw;
+      const int lx = p & (tw - 1), ly = p >> lw;
       const int x = ox + lx, y = oy + ly;
       if (x >= g.ws[s] || y >= g.hs[s]) continue;
       const int x0 = 2 * x, x1 = min(2 * x + 1, ww - 1);
@@ -138,14 +149,14 @@ __global__ void __launch_bounds__(kPyrThreads)
         v[c] = __fmul_rn(t, 0.25f);
         L[c][lvl_off(s) + p] = v[c];
       }
+      float *P = Ps + (y * pitchs + x);
 #pragma unroll
       for (int img = 0; img < 2; ++img) {
         float xo, yo, bo;
         pixel_xyb(px, cb, v[3 * img], v[3 * img + 1], v[3 * img + 2], xo, yo, bo);
-        float *P = Xf + g.xoff[s] + (long long)y * g.pitch[s] + x;
-        P[(3 * img + 0) * g.plane[s]] = xo;
-        P[(3 * img + 1) * g.plane[s]] = yo;
-        P[(3 * img + 2) * g.plane[s]] = bo;
+        P[(3 * img + 0) * planes] = xo;
+        P[(3 * img + 1) * planes] = yo;
+        P[(3 * img + 2) * planes] = bo;
       }
     }
     __syncthreads();
@@ -381,8 +392,8 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
   const ff nd = two_sum(den_s, -p.hi);
   ff d = ff_div_f(quick_two_sum(nd.hi, __fsub_rn(nd.lo, p.lo)), den_s);
   if (!(d.hi > 0.0f)) d = {0.0f, 0.0f};
-  const ff d2 = ff_mul(d, d);
-  const ff d4 = ff_mul(d2, d2);
+  const ff d2 = ff_sqr_lazy(d);
+  const ff d4 = ff_sqr_lazy(d2);
   acc.v[0] = acc_add(acc.v[0], d);
   acc.v[1] = acc_add(acc.v[1], d4);
   // edge_diff_map: r = (1 + a2) / (1 + a1) - 1 = (a2 - a1) / (1 + a1), with
@@ -390,8 +401,8 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
   const float a2 = fabsf(__fsub_rn(x2, mu2));
   const float a1 = fabsf(__fsub_rn(x1, mu1));
   const ff r = ff_div(two_sum(a2, -a1), two_sum(1.0f, a1));
-  const ff r2 = ff_mul(r, r);
-  const ff r4 = ff_mul(r2, r2);
+  const ff r2 = ff_sqr_lazy(r);
+  const ff r4 = ff_sqr_lazy(r2);
   // artifact (r > 0) and detail lost (r < 0) are exclusive: one addition each
   // into the sum that the sign selects (r = 0 adds zero to detail lost)
   const bool pos = r.hi > 0.0f;
@@ -660,7 +671,10 @@ cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st) 
 cudaError_t launch_pyramid(const Geom &g, const Pix &px, const PyrTabs &tabs, const uint8_t *ref,
                            const uint8_t *dis, float *X, int nframes, cudaStream_t st) {
   dim3 grid((g.w + kTile - 1) / kTile, (g.h + kTile - 1) / kTile, nframes);
-  k_pyramid<<<grid, kPyrThreads, 0, st>>>(g, px, tabs, ref, dis, X);
+  if (g.bps == 1)
+    k_pyramid<1><<<grid, kPyrThreads, 0, st>>>(g, px, tabs, ref, dis, X);
+  else
+    k_pyramid<2><<<grid, kPyrThreads, 0, st>>>(g, px, tabs, ref, dis, X);
   return cudaGetLastError();
 }
 

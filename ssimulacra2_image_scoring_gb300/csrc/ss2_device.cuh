@@ -59,10 +59,27 @@ __device__ __forceinline__ ff ff_mul(ff a, ff b) {
   return quick_two_sum(p.hi, __fadd_rn(p.lo, c));
 }
 
-// Approximate reciprocal (one MUFU operation, relative error near 2^-23).
+// a^2 as a pair without the final renormalisation: hi = fl(a.hi^2) and lo
+// gathers that product's exact error and 2 a.hi a.lo in one rounding (a.lo^2,
+// below 2^-46 a^2, is dropped).  If |a.lo| <= e |a.hi| then |lo| <= (2^-24 +
+// 2.01 e) |hi|: from a quotient pair (e = 2^-23) the low word stays below
+// 2^-20 |hi| after the two squarings of a fourth power, and each squaring
+// adds about 2^-45 relative error.  The pair can be squared again or added
+// to a sum (acc_add needs no normalised operand) without the three
+// instructions of quick_two_sum.
+__device__ __forceinline__ ff ff_sqr_lazy(ff a) {
+  const ff p = two_prod(a.hi, a.hi);
+  const float c = __fmul_rn(__fadd_rn(a.hi, a.hi), a.lo);
+  return {p.hi, __fadd_rn(p.lo, c)};
+}
+
+// Approximate reciprocal (relative error near 2^-23).  The .ftz form: every
+// caller passes a normal operand whose reciprocal is normal (a variance sum
+// plus C2 > 0, 1 + |x - mu| >= 1, 3 y^2 >= 2^-67), and for those the flush
+// changes nothing while sparing the subnormal handling.
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
@@ -102,8 +119,9 @@ __device__ __forceinline__ ff ff_div(ff a, ff b) {
 
 // ---------------------------------------------------------------------------
 // Correctly rounded cube root (Finding 2 asks for the CPU's cube root exactly;
-// the plain reading is cbrt rounded to nearest).  First guess: CUDA's cbrtf.
-// Then an exact decision between the guess and its neighbours: the rounded
+// the plain reading is cbrt rounded to nearest).  The exact decision below
+// settles a guess that may be an ulp or two off, between it and its
+// neighbours: the rounded
 // result y satisfies (y - u/2)^3 < x < (y + u/2)^3 for the float spacing u
 // around y, and each midpoint cube is compared with x in 128-bit integers.
 // ---------------------------------------------------------------------------
@@ -159,15 +177,18 @@ __device__ __noinline__ float cbrt_round_exact(float x, float y) {
   return y;
 }
 
+// log2 and 2^x approximations in the .ftz form: the cube root's fast path
+// calls them only for x >= 2^-100, where neither operand nor result is
+// subnormal.
 __device__ __forceinline__ float lg2_approx(float x) {
   float r;
-  asm("lg2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float r;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
