@@ -85,15 +85,19 @@ __device__ __forceinline__ float sample(const MGeom &g, int j, const uint8_t *__
 // the approximate reciprocal (MUFU) and one Newton step on the residual
 // (Markstein, IBM J. Res. Dev. 34(1), 1990), faithful to about an ulp; the
 // square root from the approximate MUFU root (relative error near 2^-22).
+// Both in the .ftz form, which spares the subnormal handling: every
+// reciprocal is of a sum holding C1, C2 or C3 (normal, with a normal
+// reciprocal), and a subnormal v1 v2 under the root would give s1 s2 below
+// 2^-63, which vanishes beside C2 and C3 in every term that uses it.
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
 __device__ __forceinline__ float sqrt_approx(float x) {
   float r;
-  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
