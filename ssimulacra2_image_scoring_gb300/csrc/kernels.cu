@@ -192,35 +192,43 @@ __device__ __forceinline__ void res_zero(Res3 &r) {
 // k_hblur: one warp per 32 rows of one (frame, scale, channel); lane = row.
 //
 // The rows are walked left to right in chunks of 8 columns.  TMA brings each
-// chunk of the two XYB planes (x1, x2) into a 4-slot shared-memory ring
+// chunk of the two XYB planes (x1, x2) into a kHSlots-slot shared-memory ring
 // (8 x 32 floats per plane, zero-filled outside the image, which is exactly
-// the recursion's zero extension), up to three chunks ahead of the walk.
+// the recursion's zero extension), up to kHSlots - 1 chunks ahead of the walk.
 // Each lane reads its row with 16-byte loads; the recursion needs the
 // samples 5 ahead and 5 behind the step (the window of radius R = 4 has
 // taps at +-(R+1)), kept in rolling registers.  The five quantities
 // (x1, x2, x1^2, x2^2, x1 x2) are formed in registers.  The chunk's 5 x 8
-// outputs per lane go to a double-buffered shared tile and leave with TMA
-// stores (clipped to the image), so global traffic is whole boxes both ways.
-// Every mbarrier wait is bounded; a timeout raises kErrTmaTimeout.
+// outputs per lane go to a ring of kHOutBufs shared tiles and leave with TMA
+// stores (clipped to the image), so global traffic is whole boxes both ways;
+// a tile is rewritten once the store issued from it kHOutBufs chunks earlier
+// has read it.  Every mbarrier wait is bounded; a timeout raises
+// kErrTmaTimeout.
 // ---------------------------------------------------------------------------
 
-constexpr int kHWarps = 4;
+// Two-warp blocks of 46 KB (23 KB per warp): four per SM.  Measured at 4K
+// against four-warp blocks with two output tiles (three per SM), the third
+// tile takes the stall on the previous stores' reads out of the walk (2.69
+// -> 2.50 ms per 7-frame launch inside the pipeline); one-warp blocks, six
+// or eight input slots and two output tiles all measured slower.
+constexpr int kHWarps = 2;
 constexpr int kHSlots = 4;
+constexpr int kHOutBufs = 3;
 constexpr int kHBox = kBoxRows * kBoxCols;  // floats in one plane box (1 KB)
 
 struct HWarpSmem {
   float in[kHSlots][2][kHBox];   // [slot][x1 | x2][row * 8 + col]
-  float out[2][kNq][kHBox];      // [buffer][quantity][row * 8 + col]
+  float out[kHOutBufs][kNq][kHBox];  // [buffer][quantity][row * 8 + col]
 };
-static_assert(sizeof(HWarpSmem) == 18432, "per-warp tile");
-// warp tiles, then the mbarriers; +1024 to align the base to 1 KB
-constexpr int kHSmemBytes = kHWarps * (int)sizeof(HWarpSmem) + kHWarps * kHSlots * 8 + 1024;
+static_assert(sizeof(HWarpSmem) % 128 == 0, "every TMA box starts on 128 bytes");
+// warp tiles, then the mbarriers; +128 to align the base for TMA
+constexpr int kHSmemBytes = kHWarps * (int)sizeof(HWarpSmem) + kHWarps * kHSlots * 8 + 128;
 
 __global__ void __launch_bounds__(kHWarps * 32)
     k_hblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, int *__restrict__ err) {
   extern __shared__ __align__(16) unsigned char hsm_raw[];
   unsigned char *hsm = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(hsm_raw) + 1023) & ~uintptr_t(1023));
+      (reinterpret_cast<uintptr_t>(hsm_raw) + 127) & ~uintptr_t(127));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int frame = blockIdx.y;
   const int unit = blockIdx.x * kHWarps + warp;
@@ -241,9 +249,9 @@ __global__ void __launch_bounds__(kHWarps * 32)
     fence_barrier_init();
   }
   __syncwarp();
-  // chunk m (columns 8m .. 8m+7) of both planes -> slot m % 4
+  // chunk m (columns 8m .. 8m+7) of both planes -> slot m % kHSlots
   auto issue = [&](int m) {
-    const int slot = m & (kHSlots - 1);
+    const int slot = m % kHSlots;
     mbar_arrive_expect_tx(&bar[slot], 2 * kHBox * (int)sizeof(float));
     tma_load_4d(sm.in[slot][0], mx, &bar[slot], m * kBoxCols, row0, c, frame);
     tma_load_4d(sm.in[slot][1], mx, &bar[slot], m * kBoxCols, row0, 3 + c, frame);
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(kHWarps * 32)
   if (lane == 0)
     for (int m = 0; m < kHSlots && m <= nchunk; ++m) issue(m);
   auto wait_chunk = [&](int m) -> bool {
-    const bool ok = mbar_wait(&bar[m & (kHSlots - 1)], (uint32_t)(m >> 2) & 1u);
+    const bool ok = mbar_wait(&bar[m % kHSlots], (uint32_t)(m / kHSlots) & 1u);
     return __all_sync(0xffffffffu, ok);
   };
   auto bail = [&]() {
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kHWarps * 32)
 
   for (int k = 0; k < nchunk; ++k) {
     if (!wait_chunk(k + 1)) { bail(); return; }
-    const int sk = k & (kHSlots - 1), sk1 = (k + 1) & (kHSlots - 1);
+    const int sk = k % kHSlots, sk1 = (k + 1) % kHSlots;
     float4 g1[2], gn[2];  // cols 8k+4..8k+7 and 8k+8..8k+11
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
@@ -328,10 +336,10 @@ __global__ void __launch_bounds__(kHWarps * 32)
       gm1[p] = g1[p];
       g0[p] = gn[p];
     }
-    // the store issued from this buffer two chunks ago must have read it
-    if (lane == 0) bulk_wait_read<1>();
+    // the store issued from this buffer kHOutBufs chunks ago must have read it
+    if (lane == 0) bulk_wait_read<kHOutBufs - 1>();
     __syncwarp();
-    const int ob = k & 1;
+    const int ob = k % kHOutBufs;
 #pragma unroll
     for (int q = 0; q < kNq; ++q) {
       float4 *d = reinterpret_cast<float4 *>(&sm.out[ob][q][lane * kBoxCols]);
