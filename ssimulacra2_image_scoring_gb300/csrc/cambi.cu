@@ -10,20 +10,27 @@
 // Readings where the page is silent (as the oracle takes them): centred
 // windows clipped to the plane, an optional mask, a table of up to four
 // (d, w) pairs with the largest term taken, the reciprocal 1/n rounded to
-// nearest (__frcp_rn), the pool the mean of the exact sum.
+// nearest (a table of 1.0f / n built by the host's IEEE division), the pool
+// the mean of the exact sum.
 //
 //   k_cambi_present  the levels that occur in each plane (1024-bit maps).
 //   k_cambi_cvalues  one warp per 32 columns of a plane; lane = column.  Each
 //                    step the warp stages the leaving and entering row
-//                    segments in shared memory (fetched one step ahead); the
-//                    lane's window histogram (16-bit bins interleaved by lane
-//                    so each lane owns its elements) is updated with plain
-//                    loads and stores, a column whose leaving and entering
-//                    pixels agree being skipped.  Planes with at most 256
+//                    segments in shared memory (fetched one step ahead).  A
+//                    window's count is split in two: the columns that all
+//                    eight lanes of a lane group share go to the group's
+//                    core histogram (32-bit bins, shared-memory atomics,
+//                    the columns dealt out among the eight lanes; two 16-bit
+//                    bins to a 32-bit word); the seven columns left to each
+//                    lane go to its own histogram (16-bit bins interleaved
+//                    by lane so each lane owns its elements, plain loads and
+//                    stores).  A column whose leaving and entering pixels
+//                    agree is skipped.  At 65 x 65 a pixel costs about 29
+//                    bin updates instead of 130.  Planes with at most 256
 //                    distinct levels (8-bit video as 10-bit levels) index
-//                    bins by the level's rank among those present: 16 KB
-//                    per warp instead of 64 KB, four times the warps per
-//                    SM.
+//                    bins by the level's rank among those present (a 2 KB
+//                    table per warp): 18 KB of bins per warp instead of
+//                    72 KB.
 //   k_cambi_hist     radix histogram of one 11/11/10-bit digit of the values
 //                    that match the digits chosen so far.
 //   k_cambi_select   one block per plane: the digit holding the k-th largest
@@ -51,8 +58,15 @@ using namespace ss2;
 
 constexpr int kLevels = 1024;
 constexpr int kMaxWin2 = 4225;
-constexpr int kCvSmem = kLevels * 32 * 2;          // 64 KB: 1024 bins x 32 lanes x 16 bits
-constexpr int kCvSmemCompact = 256 * 32 * 2;      // 16 KB: the compact histogram
+constexpr int kGroup = 8;                          // lanes sharing a core histogram
+constexpr int kGroups = 32 / kGroup;
+constexpr int kOwnMax = kGroup - 1;                // columns a lane counts alone (at most)
+// per warp: 32 lanes' own 16-bit bins, then the groups' core bins (16-bit,
+// two to a 32-bit word)
+constexpr int cv_smem(int bins) { return bins * 32 * 2 + kGroups * bins * 2; }
+constexpr int kCvSmem = cv_smem(1024);             // 72 KB
+constexpr int kCvSmemCompact = cv_smem(256);       // 18 KB: the compact histograms
+constexpr int kMaxCount = 2 * kMaxWin2;            // p0 + pm <= 8450: the reciprocal table's range
 constexpr int kErrLevel = 2;                       // a level >= 1024 was seen
 constexpr int kErrValue = 4;                       // a value off the 2^-24 grid or >= 2^14
 constexpr int kSumThreads = 256;
@@ -67,7 +81,6 @@ struct CGeom {
 
 constexpr int kSeg = 32 + 64;                      // a row's window columns for 32 lanes
 constexpr unsigned kSkip = 0xFFFFu;                // outside the plane or not counted
-constexpr int kBatch = 16;                         // columns whose levels are read ahead
 constexpr int kCompactBins = 256;                  // the compact histogram's bins
 
 // Which of the 1024 levels occur in each plane (a 1024-bit map per plane,
@@ -89,24 +102,35 @@ __global__ void __launch_bounds__(256)
 }
 
 // k_cambi_cvalues<BINS>: one warp per 32 output columns of a plane; lane =
-// column.  Each lane owns a window histogram of BINS 16-bit bins (element
-// bin * 32 + lane, plain loads and stores; a count stays in 0..4225).  With
-// BINS = 256 a level is replaced by its rank among the levels present in the
-// plane (8-bit video as 10-bit levels has at most 256), which cuts the
-// histogram to 16 KB per warp; planes with more levels run the BINS = 1024
-// variant, which uses the levels themselves.  Both variants are launched;
-// a block whose plane belongs to the other one returns at once.  Each step
-// the warp stages the leaving and entering row segments in shared memory
-// (fetched one step ahead); a column whose two pixels agree is skipped.
+// column.  Lane l's window covers segment columns l .. l + 2r.  The eight
+// lanes of group q (lanes 8q .. 8q+7) all cover columns 8q+7 .. 8q+2r: the
+// group's core, counted once in a histogram of BINS 16-bit bins packed two
+// to a 32-bit word, which the group's lanes update with 32-bit shared-memory
+// atomics (+-1 or +-2^16), each taking every eighth core column.  The steps'
+// updates commute and every final count lies in 0..3770, so the packed word
+// holds both counts exactly once a step's updates are all in, whatever the
+// borrows and carries between the halves along the way.  The rest of a lane's window (8q+7-1-j columns on the left
+// and j on the right for lane 8q+j, seven in all) goes to the lane's own
+// histogram of BINS 16-bit bins (element bin * 32 + lane, plain loads and
+// stores; a count stays in 0..455).  A window narrower than a group has no
+// core: each lane counts its whole window alone.  A count is the core bin
+// plus the own bin.  With BINS = 256 a level is replaced by its rank among
+// the levels present in the plane (8-bit video as 10-bit levels has at most
+// 256); planes with more levels run the BINS = 1024 variant, which uses the
+// levels themselves.  Both variants are launched; a block whose plane belongs
+// to the other one returns at once.  Each step the warp stages the leaving
+// and entering row segments in shared memory (fetched one step ahead); a
+// column whose two pixels agree is skipped.
 template <int BINS>
 __global__ void __launch_bounds__(32)
     k_cambi_cvalues(CGeom g, const uint16_t *__restrict__ levels, const uint8_t *__restrict__ mask,
-                    const unsigned *__restrict__ present, float *__restrict__ out,
-                    int *__restrict__ err) {
-  extern __shared__ uint16_t cv_hist[];            // BINS x 32 lanes
+                    const unsigned *__restrict__ present, const float *__restrict__ recip,
+                    float *__restrict__ out, int *__restrict__ err) {
+  extern __shared__ uint16_t cv_hist[];            // own bins (BINS x 32 lanes), then the cores
   __shared__ uint16_t seg[2][kSeg];
   __shared__ unsigned pbits[kLevels / 32];         // levels present in the plane
   __shared__ unsigned prank[kLevels / 32];         // present levels below each word
+  __shared__ uint16_t rank_of[BINS == kLevels ? 1 : kLevels];   // compact bin of each level
   const int lane = threadIdx.x;
   const unsigned *pp = present + blockIdx.y * (kLevels / 32);
   {
@@ -124,25 +148,41 @@ __global__ void __launch_bounds__(32)
     if ((BINS == kCompactBins) != (total <= (unsigned)kCompactBins)) return;   // the other variant's
   }
   __syncwarp();
+  if (BINS != kLevels) {
+    for (int v = lane; v < kLevels; v += 32) {
+      const unsigned w = pbits[v >> 5], m = 1u << (v & 31);
+      rank_of[v] = (uint16_t)((w & m) ? prank[v >> 5] + __popc(w & (m - 1u)) : kSkip);
+    }
+    __syncwarp();
+  }
   // histogram index of level v (v < 1024): its rank among the present
   // levels (BINS = 256) or v itself; kSkip when v does not occur
   auto bin = [&](unsigned v) -> unsigned {
     if (BINS == kLevels) return v;
-    const unsigned w = pbits[v >> 5], m = 1u << (v & 31);
-    return (w & m) ? prank[v >> 5] + __popc(w & (m - 1u)) : kSkip;
+    return rank_of[v];
   };
   const int x0 = blockIdx.x * 32, x = x0 + lane;
   const long long base = (long long)blockIdx.y * g.plane;
   const uint16_t *L = levels + base;
   const uint8_t *M = mask ? mask + base : nullptr;
+  unsigned *cores = reinterpret_cast<unsigned *>(cv_hist + BINS * 32);
   for (int i = lane; i < BINS * 32; i += 32) cv_hist[i] = 0u;
+  for (int i = lane; i < kGroups * BINS / 2; i += 32) cores[i] = 0u;
   const int r = g.window / 2;
   const int nseg = 32 + 2 * r;
   const bool col = x < g.w;
   bool bad = false;
-  // the histogram indices of row yy's segment (kSkip for rows outside the
-  // plane, pixels not counted, levels >= 1024): three per lane, loaded
-  // together
+  // the lane's group, its core columns [ca, cz] and the lane's own columns:
+  // own column t is lane + t for t < nleft, then cz + 1 + (t - nleft)
+  const int jl = lane % kGroup;
+  unsigned *core = cores + (lane / kGroup) * (BINS / 2);
+  // the core count of bin b: half b & 1 of word b >> 1
+  auto core_count = [&](unsigned b) -> unsigned { return (core[b >> 1] >> ((b & 1u) * 16)) & 0xFFFFu; };
+  const bool has_core = g.window >= kGroup;           // the same for every lane
+  const int ca = lane - jl + kGroup - 1, cz = lane - jl + 2 * r;
+  const int nown = has_core ? kGroup - 1 : 2 * r + 1;
+  const int nleft = has_core ? kGroup - 1 - jl : 2 * r + 1;
+  const int ncore = has_core ? (cz - ca) / kGroup + 1 : 0;   // the first lane's count
   auto fetch = [&](int yy, unsigned (&v)[3]) {
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
@@ -163,27 +203,34 @@ __global__ void __launch_bounds__(32)
     for (int j = 0; j < 3; ++j)
       if (lane + 32 * j < kSeg) seg[s_][lane + 32 * j] = (uint16_t)v[j];
   };
-  // the lane's window columns lane .. lane + 2r: remove seg[0], add seg[1]
-  // (a column whose two pixels agree is skipped); the indices of kBatch
-  // columns are read before their updates
+  // remove seg[0] and add seg[1] over the lane's own columns (indices read
+  // before the updates) and the lane's share of its group's core columns
   auto apply = [&](bool remove) {
-    for (int i0 = 0; i0 <= 2 * r; i0 += kBatch) {
-      unsigned a[kBatch], b[kBatch];
+    unsigned a[kOwnMax], b[kOwnMax];
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int i = i0 + k;
-        a[k] = (remove && i <= 2 * r) ? seg[0][lane + i] : kSkip;
-        b[k] = i <= 2 * r ? seg[1][lane + i] : kSkip;
-      }
+    for (int t = 0; t < kOwnMax; ++t) {
+      const int i = t < nleft ? lane + t : cz + 1 + (t - nleft);
+      a[t] = (remove && t < nown) ? seg[0][i] : kSkip;
+      b[t] = t < nown ? seg[1][i] : kSkip;
+    }
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        if (a[k] == b[k]) continue;                 // the column's count does not change
-        // a != b: two different bins, both read before either is written
-        const unsigned ca = a[k] != kSkip ? cv_hist[a[k] * 32 + lane] : 0u;
-        const unsigned cb = b[k] != kSkip ? cv_hist[b[k] * 32 + lane] : 0u;
-        if (a[k] != kSkip) cv_hist[a[k] * 32 + lane] = (uint16_t)(ca - 1u);
-        if (b[k] != kSkip) cv_hist[b[k] * 32 + lane] = (uint16_t)(cb + 1u);
-      }
+    for (int t = 0; t < kOwnMax; ++t) {
+      if (a[t] == b[t]) continue;                   // the column's count does not change
+      // a != b: two different bins, both read before either is written
+      const unsigned ca_ = a[t] != kSkip ? cv_hist[a[t] * 32 + lane] : 0u;
+      const unsigned cb_ = b[t] != kSkip ? cv_hist[b[t] * 32 + lane] : 0u;
+      if (a[t] != kSkip) cv_hist[a[t] * 32 + lane] = (uint16_t)(ca_ - 1u);
+      if (b[t] != kSkip) cv_hist[b[t] * 32 + lane] = (uint16_t)(cb_ + 1u);
+    }
+    for (int t = 0; t < ncore; ++t) {
+      const int i = ca + jl + t * kGroup;
+      if (i > cz) break;
+      const unsigned av = remove ? seg[0][i] : kSkip, bv = seg[1][i];
+      if (av == bv) continue;
+      // commuting +-1 on a packed bin: both halves are exact once the
+      // step's updates are all in
+      if (av != kSkip) atomicAdd(&core[av >> 1], 0u - (1u << ((av & 1u) * 16)));
+      if (bv != kSkip) atomicAdd(&core[bv >> 1], 1u << ((bv & 1u) * 16));
     }
   };
   __syncwarp();
@@ -193,7 +240,7 @@ __global__ void __launch_bounds__(32)
     fetch(yy, v);
     put(1, v);
     __syncwarp();
-    if (col) apply(false);
+    apply(false);                                   // every lane: the cores are shared
     __syncwarp();
   }
   // step y moves the window from rows y-1-r .. y-1+r to y-r .. y+r; the
@@ -208,7 +255,8 @@ __global__ void __launch_bounds__(32)
       __syncwarp();
       fetch(y - r, nout);                           // rows of step y + 1
       fetch(y + 1 + r, nin);
-      if (col) apply(true);
+      apply(true);
+      __syncwarp();                                 // the cores are complete
     }
     if (col) {
       const long long at = (long long)y * g.w + x;
@@ -218,16 +266,17 @@ __global__ void __launch_bounds__(32)
         if (lv >= kLevels) {
           bad = true;
         } else {
-          const unsigned p0 = cv_hist[bin(lv) * 32 + lane];   // the pixel's own level occurs
+          const unsigned b0 = bin(lv);               // the pixel's own level occurs
+          const unsigned p0 = cv_hist[b0 * 32 + lane] + (has_core ? core_count(b0) : 0u);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             if (i >= g.ndiff || lv + g.diffs[i] >= kLevels) continue;
             const unsigned bm = bin(lv + g.diffs[i]);
             if (bm == kSkip) continue;
-            const unsigned pm = cv_hist[bm * 32 + lane];
+            const unsigned pm = cv_hist[bm * 32 + lane] + (has_core ? core_count(bm) : 0u);
             if (pm == 0u) continue;
             const float c = __fmul_rn((float)((unsigned)g.weights[i] * p0 * pm),
-                                      __frcp_rn((float)(p0 + pm)));
+                                      __ldg(recip + p0 + pm));
             best = fmaxf(best, c);
           }
         }
@@ -395,6 +444,7 @@ struct ss2_cambi {
   double *d_means = nullptr;
   int *d_err = nullptr, *h_err = nullptr;
   unsigned *d_present = nullptr;            // levels present, a 1024-bit map per plane
+  float *d_recip = nullptr;                 // 1.0f / n for n = 0 .. kMaxCount (entry 0 unused)
   unsigned long long *h_sums = nullptr;
   float *h_thr = nullptr;
   double *h_means = nullptr;
@@ -413,6 +463,7 @@ static void cambi_free(ss2_cambi *c) {
   cudaFree(c->d_means);
   cudaFree(c->d_err);
   cudaFree(c->d_present);
+  cudaFree(c->d_recip);
   if (c->h_err) cudaFreeHost(c->h_err);
   if (c->h_sums) cudaFreeHost(c->h_sums);
   if (c->h_thr) cudaFreeHost(c->h_thr);
@@ -467,6 +518,7 @@ SS2_API ss2_cambi *ss2_cambi_create(int width, int height, int window, int ndiff
   if (cudaFuncSetAttribute(k_cambi_cvalues<kLevels>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kCvSmem) != cudaSuccess ||
       cudaMalloc(&c->d_present, B * (kLevels / 32) * sizeof(unsigned)) != cudaSuccess ||
+      cudaMalloc(&c->d_recip, (kMaxCount + 1) * sizeof(float)) != cudaSuccess ||
       cudaMalloc(&c->d_c, B * g.plane * sizeof(float)) != cudaSuccess ||
       cudaMalloc(&c->d_st, B * sizeof(RState)) != cudaSuccess ||
       cudaMalloc(&c->d_hist, B * 2048 * sizeof(unsigned)) != cudaSuccess ||
@@ -484,6 +536,19 @@ SS2_API ss2_cambi *ss2_cambi_create(int width, int height, int window, int ndiff
     return nullptr;
   }
   *c->h_err = 0;
+  {
+    // the reciprocal table: IEEE single division on the host rounds to
+    // nearest, so entry n is 1/n correctly rounded
+    std::vector<float> r(kMaxCount + 1, 0.0f);
+    for (int n = 1; n <= kMaxCount; ++n) r[n] = 1.0f / (float)n;
+    if (cudaMemcpy(c->d_recip, r.data(), r.size() * sizeof(float), cudaMemcpyHostToDevice) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      fail(SS2_EIO, "cambi reciprocal table upload failed");
+      cambi_free(c);
+      return nullptr;
+    }
+  }
   return c;
 }
 
@@ -516,13 +581,13 @@ static cudaError_t cambi_cv_launch(ss2_cambi *c, const uint16_t *levels, const u
   }
   const dim3 grid((g.w + 31) / 32, nb);
   if (e == cudaSuccess) {
-    k_cambi_cvalues<kCompactBins><<<grid, 32, kCvSmemCompact, st>>>(g, levels, mask, c->d_present,
-                                                                   out, c->d_err);
+    k_cambi_cvalues<kCompactBins><<<grid, 32, kCvSmemCompact, st>>>(
+        g, levels, mask, c->d_present, c->d_recip, out, c->d_err);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    k_cambi_cvalues<kLevels><<<grid, 32, kCvSmem, st>>>(g, levels, mask, c->d_present, out,
-                                                       c->d_err);
+    k_cambi_cvalues<kLevels><<<grid, 32, kCvSmem, st>>>(g, levels, mask, c->d_present,
+                                                       c->d_recip, out, c->d_err);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = c->timer.mark(0, false, st);
