@@ -193,28 +193,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Correctly rounded cbrt for x >= 0 finite.
-//   1. y0 = 2^(log2(x) / 3) from the hardware approximations (a few ulps).
-//   2. The residual R = x - y0^3 to about 2^-43 x: y0^2 = p + e and
-//      y0 p = q + f exactly (fma), x - q exact by Sterbenz.
+//   1. y0 = 2^(log2(x) / 3) from the hardware approximations (within about
+//      2^-20 relative).
+//   2. The residual R = x - y0^3 to about 2^-46 x: y0^2 = p + e and
+//      y0 p = q + f exactly (fma), x - q exact by Sterbenz, then f and y0 e
+//      taken off (the latter in one fma).
 //   3. One Newton step y0 + R / (3 y0^2), whose error is about 2^-41 y0,
 //      with the rounding error of the final addition kept exactly
-//      (two_sum): the root lies at that error (plus 2^-41 y0) from the
-//      float y, so y is the nearest float unless the error is within
-//      2^-14 ulp of half an ulp.
+//      (quick_two_sum: the correction is below 2^-19 y0): the root lies at
+//      that error (plus 2^-41 y0) from the float y, so y is the nearest
+//      float unless the error is within 2^-14 ulp of half an ulp.
 //   4. Those near-ties, powers of two (where the spacing below halves) and
 //      x < 2^-100 (where the products' error terms underflow) take the exact
-//      128-bit integer decision.
+//      128-bit integer decision; +-0 return themselves.
 __device__ __forceinline__ float cbrt_cr(float x) {
-  if (x == 0.0f) return 0.0f;
-  if (__float_as_uint(x) < 0x0d800000u) return cbrt_round_exact(x, cbrtf(x));
+  // magnitude below 2^-100, zeros included (the sign bit shifted out)
+  if ((__float_as_uint(x) << 1) < (0x0d800000u << 1))
+    return x == 0.0f ? x : cbrt_round_exact(x, cbrtf(x));
   const float y0 = ex2_approx(__fmul_rn(lg2_approx(x), 0.333333343f));
   const ff p = two_prod(y0, y0);
   const ff q = two_prod(y0, p.hi);
   float r = __fsub_rn(x, q.hi);
   r = __fsub_rn(r, q.lo);
-  r = __fsub_rn(r, __fmul_rn(y0, p.lo));
+  r = __fmaf_rn(-y0, p.lo, r);
   const float d = __fmul_rn(r, rcp_approx(__fmul_rn(3.0f, p.hi)));
-  const ff y = two_sum(y0, d);
+  const ff y = quick_two_sum(y0, d);
   const uint32_t yb = __float_as_uint(y.hi);
   const float half_u = __uint_as_float((yb & 0x7f800000u) - (24u << 23));
   if ((yb & 0x7fffffu) != 0u && fabsf(y.lo) < __fmul_rn(half_u, 0.99993896484375f)) return y.hi;

@@ -132,13 +132,15 @@ def test_random_params(cuda):
 
 def test_cbrt_matches_oracle_on_reachable_domain(cuda):
     """Every float in [2^-9, 2) (the opsin outputs of [0,1] RGB lie in
-    [bias, 1 + bias]) plus a stride through the rest of the positive floats,
-    bitwise against the oracle's correctly rounded cube root."""
+    [bias, 1 + bias]) plus a stride through the rest of the positive floats
+    and both zeros, bitwise against the oracle's correctly rounded cube
+    root."""
     import torch
     from ssimulacra2_image_scoring_gb300 import ss2
     lo = np.float32(2.0 ** -9).view(np.uint32)
     hi = np.float32(2.0).view(np.uint32)
-    bits = np.concatenate([np.arange(lo, hi, dtype=np.uint32),
+    bits = np.concatenate([np.array([0, 0x80000000], dtype=np.uint32),
+                           np.arange(lo, hi, dtype=np.uint32),
                            np.arange(1, 0x7f800000, 9973, dtype=np.uint32)])
     x = bits.view(np.float32)
     got = ss2.debug_cbrt(torch.from_numpy(x).cuda()).cpu().numpy()
