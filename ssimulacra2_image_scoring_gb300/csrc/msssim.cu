@@ -13,20 +13,25 @@
 // score prod_{j<5} mean(cs_j)^beta_j * mean(l cs)_5^beta_5 with the
 // published exponents.
 //
-//   k_msssim_level  one launch per scale over the batch; a block takes a
-//                   32x16 tile of window positions: the 42x26 input tile
-//                   (raw luma at scale 1, fp32 planes after), shifted by
-//                   the tile's first reference sample (variances and
-//                   covariance do not change, cancellation does); the five
-//                   Gaussian means in fp32 as three packed pairs (separable,
-//                   fma.rn.f32x2, products formed once per pixel); l, c, s,
-//                   cs, l cs per position (approximate reciprocals and root
-//                   refined to about an ulp); sums in fp32 per warp (fixed
-//                   tree) and fp64 over the block's warps into the (frame,
-//                   scale, tile) span (fp64 is slow on this part).  It
-//                   also writes its share of the next scale: 2x2 means,
-//                   exact in fp32 (a level-5 value is at most 2^24 units of
-//                   2^-16, so every partial sum is representable).
+//   k_msssim_level  one launch per scale over the batch; a block walks a
+//                   strip of 32 window positions across, down a band of up
+//                   to 128 rows, 16 rows at a time: each step loads the 16
+//                   new input rows of the 42-column strip (raw luma at
+//                   scale 1, fp32 planes after), shifted by the band's
+//                   first reference sample (variances and covariance do not
+//                   change, cancellation does), and forms their horizontal
+//                   Gaussian sums once into a 32-row ring, from which the
+//                   vertical sums of the step's 16 output rows are read;
+//                   the five Gaussian means in fp32 as three packed pairs
+//                   (fma.rn.f32x2, products formed once per pixel); l, c,
+//                   s, cs, l cs per position (approximate reciprocals and
+//                   root refined to about an ulp); per step fp32 sums per
+//                   warp (fixed tree), then fp64 over the steps and the
+//                   block's warps into the (frame, scale, block) span (fp64
+//                   is slow on this part).  It also writes its share of the
+//                   next scale: 2x2 means, exact in fp32 (a level-5 value is
+//                   at most 2^24 units of 2^-16, so every partial sum is
+//                   representable).
 //   k_msssim_final  per frame: each span summed in a fixed warp order, the
 //                   means, and the product of powers (fp64).
 #include <cuda_runtime.h>
@@ -50,9 +55,13 @@ using namespace ss2;
 constexpr int kScales = 5;
 constexpr int kQ = 5;                      // l, c, s, cs, l cs
 constexpr int kWin = 11;
-constexpr int kTX = 32, kTY = 16;          // window positions per block
-constexpr int kIX = kTX + kWin - 1;        // input tile 42 x 26
-constexpr int kIY = kTY + kWin - 1;
+constexpr int kTX = 32;                    // window positions across a strip
+constexpr int kIX = kTX + kWin - 1;        // input columns of a strip: 42
+constexpr int kCH = 16;                    // output rows per step
+constexpr int kBH = 128;                   // output rows per band (8 steps)
+constexpr int kRing = 32;                  // rows of horizontal sums kept (>= kCH + kWin - 1)
+constexpr int kHalo = kWin - 1;            // input rows ahead of a band's first step
+static_assert(kCH % 2 == 0 && kHalo % 2 == 0 && kBH % kCH == 0, "row pairs stay in one step");
 
 struct MGeom {
   int w, h, depth, bps;
@@ -114,69 +123,100 @@ __global__ void __launch_bounds__(256)
     k_msssim_level(MGeom g, int j, const uint8_t *__restrict__ ref, const uint8_t *__restrict__ dis,
                    float *__restrict__ pyr, double *__restrict__ part) {
   // the five quantities as three fp32 pairs (p, q), (p p, q q), (p q, 0):
-  // PP for the input tile, HH for the horizontal sums of every input row
-  // (rows padded by one pair: the horizontal pass runs row-fastest)
-  __shared__ __align__(16) f2 PP[3][kIY][kIX + 1];
-  __shared__ __align__(16) f2 HH[3][kIY][kTX + 1];
-  __shared__ float wsum[8][kQ];
-  const int frame = blockIdx.z, t = threadIdx.x;
+  // PP for a step's new input rows, HH the ring of horizontal sums (rows
+  // padded by one pair: the horizontal pass runs row-fastest)
+  __shared__ __align__(16) f2 PP[3][kCH][kIX + 1];
+  __shared__ __align__(16) f2 HH[3][kRing][kTX + 1];
+  __shared__ double wsum[8][kQ];
+  const int frame = blockIdx.z, t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int W = g.ws[j], Hh = g.hs[j];
-  const int ox0 = blockIdx.x * kTX, oy0 = blockIdx.y * kTY;
+  const int ox0 = blockIdx.x * kTX, oy0 = blockIdx.y * kBH;
   const int ow = W - kWin + 1, oh = Hh - kWin + 1;
+  const int nsteps = (min(kBH, oh - oy0) + kCH - 1) / kCH;
   const uint8_t *ra = ref + (long long)frame * g.frame_bytes;
   const uint8_t *rb = dis + (long long)frame * g.frame_bytes;
   const float *pa = pyr + (long long)(2 * frame) * g.img_floats + g.lvl_off[j];
   const float *pb = pa + g.img_floats;
-
-  // input tile (clamped to the plane), shifted by the tile's first reference
-  // sample; every load of a thread is issued before the first is used
   const float off = sample<MODE>(g, j, ra, pa, ox0, oy0);
-  // thread t < 252 takes column t % 42 and rows t / 42, + 6, + 12, ...
-  constexpr int kRowStep = 256 / kIX;                  // 6
-  constexpr int kPer = (kIY + kRowStep - 1) / kRowStep;  // 5
-  const int c = t % kIX, r0 = t / kIX;
-  const bool loader = t < kRowStep * kIX;
-  const int xc = min(ox0 + c, W - 1);
-  float va[kPer], vb[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int r = r0 + kRowStep * k;
-    if (loader && r < kIY) {
-      const int y = min(oy0 + r, Hh - 1);
-      va[k] = sample<MODE>(g, j, ra, pa, xc, y);
-      vb[k] = sample<MODE>(g, j, rb, pb, xc, y);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int r = r0 + kRowStep * k;
-    if (loader && r < kIY) {
-      const float p = __fsub_rn(va[k], off);     // exact: both lie on the same grid below 256
-      const float q = __fsub_rn(vb[k], off);
-      PP[0][r][c] = f2_pack(p, q);
-      PP[1][r][c] = f2_pack(__fmul_rn(p, p), __fmul_rn(q, q));
-      PP[2][r][c] = f2_pack(__fmul_rn(p, q), 0.0f);
-    }
-  }
   f2 gk[kWin];
 #pragma unroll
   for (int k = 0; k < kWin; ++k) gk[k] = f2_pack(g.gauss[k], g.gauss[k]);
-  __syncthreads();
 
-  // the 2x2 means of this block's share of the next scale, from the tile
-  // (p + off restores each sample exactly; clamping matches the tile's)
-  if (j + 1 < kScales) {
-    const int Wn = g.ws[j + 1], Hn = g.hs[j + 1];
-    const int X0 = blockIdx.x * (kTX / 2), Y0 = blockIdx.y * (kTY / 2);
-    const int X1 = blockIdx.x + 1 == gridDim.x ? Wn : X0 + kTX / 2;
-    const int Y1 = blockIdx.y + 1 == gridDim.y ? Hn : Y0 + kTY / 2;
-    const int nx = X1 - X0, n = nx * (Y1 - Y0);
+  // input rows row0 .. row0 + n - 1 of the band (clamped to the plane) into
+  // PP rows 0 .. n - 1; thread t < 252 takes column t % 42 and rows t / 42,
+  // + 6, + 12, every load issued before the first is used
+  constexpr int kRowStep = 256 / kIX;                    // 6
+  constexpr int kPer = (kCH + kRowStep - 1) / kRowStep;  // 3
+  const int lc = t % kIX, lr0 = t / kIX;
+  const bool loader = t < kRowStep * kIX;
+  const int xc = min(ox0 + lc, W - 1);
+  // the loads (issue) and the PP stores (commit) are separate so that a
+  // step's loads are in flight during the previous step's vertical pass
+  auto load_issue = [&](int row0, int n, float (&va)[kPer], float (&vb)[kPer]) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int r = lr0 + kRowStep * k;
+      if (loader && r < n) {
+        const int y = min(oy0 + row0 + r, Hh - 1);
+        va[k] = sample<MODE>(g, j, ra, pa, xc, y);
+        vb[k] = sample<MODE>(g, j, rb, pb, xc, y);
+      }
+    }
+  };
+  auto load_commit = [&](int n, const float (&va)[kPer], const float (&vb)[kPer]) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int r = lr0 + kRowStep * k;
+      if (loader && r < n) {
+        const float p = __fsub_rn(va[k], off);     // exact: both lie on the same grid below 256
+        const float q = __fsub_rn(vb[k], off);
+        PP[0][r][lc] = f2_pack(p, q);
+        PP[1][r][lc] = f2_pack(__fmul_rn(p, p), __fmul_rn(q, q));
+        PP[2][r][lc] = f2_pack(__fmul_rn(p, q), 0.0f);
+      }
+    }
+  };
+  // horizontal sums of PP rows 0 .. n - 1 into ring rows (row0 + r) % 32: a
+  // thread takes 2 adjacent positions of one row, rows fastest across threads
+  auto hpass = [&](int row0, int n) {
+    if (t < n * (kTX / 2)) {
+      const int r = t % n, c0 = 2 * (t / n);
+      const int hr = (row0 + r) & (kRing - 1);
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        f2 v[kWin + 1];
+#pragma unroll
+        for (int k = 0; k < kWin + 1; ++k) v[k] = PP[q][r][c0 + k];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          f2 acc = 0ull;                                 // (+0, +0)
+#pragma unroll
+          for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[i + k], acc);
+          HH[q][hr][c0 + i] = acc;
+        }
+      }
+    }
+  };
+  // the block's share of the next scale whose source rows are PP rows 0 ..
+  // n - 1 (p + off restores each sample exactly; clamping matches the
+  // loads').  A block owns next-scale columns 16 bx .. and rows 64 by ..,
+  // the last strip and band up to the plane's edge; row pairs never
+  // straddle two steps (even band origin, step and halo).
+  const bool next = j + 1 < kScales;
+  const int Wn = next ? g.ws[j + 1] : 0, Hn = next ? g.hs[j + 1] : 0;
+  const int X0 = blockIdx.x * (kTX / 2), Y0 = blockIdx.y * (kBH / 2);
+  const int X1 = blockIdx.x + 1 == gridDim.x ? Wn : X0 + kTX / 2;
+  const int Y1 = blockIdx.y + 1 == gridDim.y ? Hn : Y0 + kBH / 2;
+  auto next_scale = [&](int row0, int n) {
+    if (!next) return;
+    const int ya = max(Y0, (oy0 + row0) / 2), yb = min(Y1, (oy0 + row0 + n) / 2);
+    const int nx = X1 - X0, cnt = nx * (yb - ya);
     float *na = pyr + (long long)(2 * frame) * g.img_floats + g.lvl_off[j + 1];
     float *nb = na + g.img_floats;
-    for (int i = t; i < n; i += 256) {
-      const int X = X0 + i % nx, Y = Y0 + i / nx;
+    for (int i = t; i < cnt; i += 256) {
+      const int X = X0 + i % nx, Y = ya + i / nx;
       const int c0 = 2 * X - ox0, c1 = min(2 * X + 1, W - 1) - ox0;
-      const int r0 = 2 * Y - oy0, r1 = min(2 * Y + 1, Hh - 1) - oy0;
+      const int r0 = 2 * Y - oy0 - row0, r1 = min(2 * Y + 1, Hh - 1) - oy0 - row0;
       float a00, b00, a01, b01, a10, b10, a11, b11;
       f2_unpack(PP[0][r0][c0], a00, b00);
       f2_unpack(PP[0][r0][c1], a01, b01);
@@ -189,89 +229,91 @@ __global__ void __launch_bounds__(256)
       na[(long long)Y * g.pitch[j + 1] + X] = __fmul_rn(a, 0.25f);
       nb[(long long)Y * g.pitch[j + 1] + X] = __fmul_rn(b, 0.25f);
     }
-  }
+  };
 
-  // horizontal sums: a thread takes 4 adjacent positions of one input row,
-  // rows fastest across threads (conflict-free 64-bit shared accesses)
-  if (t < kIY * (kTX / 4)) {
-    const int r = t % kIY, c0 = 4 * (t / kIY);
+  double dsum[kQ] = {0.0, 0.0, 0.0, 0.0, 0.0};        // lane 0: the warp's steps in order
+  float va[kPer], vb[kPer];
+  // the halo rows ahead of the first step
+  load_issue(0, kHalo, va, vb);
+  load_commit(kHalo, va, vb);
+  __syncthreads();
+  hpass(0, kHalo);
+  next_scale(0, kHalo);
+  load_issue(kHalo, kCH, va, vb);                       // the first step's rows
+  __syncthreads();                                      // PP is free
+  for (int st = 0; st < nsteps; ++st) {
+    const int row0 = kHalo + st * kCH;                  // the step's new input rows
+    load_commit(kCH, va, vb);
+    __syncthreads();                                    // PP complete; the last vertical pass is done
+    hpass(row0, kCH);
+    next_scale(row0, kCH);
+    __syncthreads();                                    // the ring is complete; PP is free
+    if (st + 1 < nsteps) load_issue(row0 + kCH, kCH, va, vb);
+    // vertical sums and the terms of two positions (output rows 2 w, 2 w + 1
+    // of the step, w = thread / 32)
+    const int oc = t % kTX, orow = st * kCH + 2 * (t / kTX);
+    const int ox = ox0 + oc;
+    f2 m[2][3];
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
-      f2 v[kWin + 3];
+      f2 v[kWin + 1];
 #pragma unroll
-      for (int k = 0; k < kWin + 3; ++k) v[k] = PP[q][r][c0 + k];
+      for (int k = 0; k < kWin + 1; ++k) v[k] = HH[q][(orow + k) & (kRing - 1)][oc];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f2 acc = 0ull;                                   // (+0, +0)
+      for (int i = 0; i < 2; ++i) {
+        f2 acc = 0ull;
 #pragma unroll
         for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[i + k], acc);
-        HH[q][r][c0 + i] = acc;
+        m[i][q] = acc;
       }
     }
-  }
-  __syncthreads();
-  // vertical sums and the terms of two positions (rows 2 oy, 2 oy + 1)
-  const int oc = t % kTX, orow = 2 * (t / kTX);
-  const int ox = ox0 + oc;
-  f2 m[2][3];
-#pragma unroll
-  for (int q = 0; q < 3; ++q) {
-    f2 v[kWin + 1];
-#pragma unroll
-    for (int k = 0; k < kWin + 1; ++k) v[k] = HH[q][orow + k][oc];
+    float sum[kQ] = {0, 0, 0, 0, 0};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      f2 acc = 0ull;
+      const int oy = oy0 + orow + i;
+      if (ox < ow && oy < oh) {
+        float m1, m2, e11, e22, e12, unused;
+        f2_unpack(m[i][0], m1, m2);
+        f2_unpack(m[i][1], e11, e22);
+        f2_unpack(m[i][2], e12, unused);
+        const float v1 = fmaxf(__fsub_rn(e11, __fmul_rn(m1, m1)), 0.0f);
+        const float v2 = fmaxf(__fsub_rn(e22, __fmul_rn(m2, m2)), 0.0f);
+        const float cv = __fsub_rn(e12, __fmul_rn(m1, m2));
+        const float mu1 = __fadd_rn(m1, off), mu2 = __fadd_rn(m2, off);
+        // s1 s2 = sqrt(v1 v2) (0 for a flat window); c and cs share 1 / vden
+        const float sd12 = sqrt_approx(__fmul_rn(v1, v2));
+        const float vden = __fadd_rn(__fadd_rn(v1, v2), g.C2);
+        const float rv = rcp_approx(vden);
+        const float l = div_fast(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(mu1, mu2)), g.C1),
+                                 __fadd_rn(__fadd_rn(__fmul_rn(mu1, mu1), __fmul_rn(mu2, mu2)), g.C1));
+        const float c = div_by(__fadd_rn(__fmul_rn(2.0f, sd12), g.C2), vden, rv);
+        const float s = div_fast(__fadd_rn(cv, g.C3), __fadd_rn(sd12, g.C3));
+        const float cs = div_by(__fadd_rn(__fmul_rn(2.0f, cv), g.C2), vden, rv);
+        sum[0] = __fadd_rn(sum[0], l);
+        sum[1] = __fadd_rn(sum[1], c);
+        sum[2] = __fadd_rn(sum[2], s);
+        sum[3] = __fadd_rn(sum[3], cs);
+        sum[4] = __fadd_rn(sum[4], __fmul_rn(l, cs));
+      }
+    }
+    // the step's warp sums in fp32 (a fixed xor tree), added in fp64 by lane 0
 #pragma unroll
-      for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[i + k], acc);
-      m[i][q] = acc;
+    for (int q = 0; q < kQ; ++q) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum[q] = __fadd_rn(sum[q], __shfl_xor_sync(0xffffffffu, sum[q], o));
+      if (lane == 0) dsum[q] = __dadd_rn(dsum[q], (double)sum[q]);
     }
   }
-  float sum[kQ] = {0, 0, 0, 0, 0};
+  // the block's eight warp sums in fp64 in warp order
+  if (lane == 0) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int oy = oy0 + orow + i;
-    if (ox < ow && oy < oh) {
-      float m1, m2, e11, e22, e12, unused;
-      f2_unpack(m[i][0], m1, m2);
-      f2_unpack(m[i][1], e11, e22);
-      f2_unpack(m[i][2], e12, unused);
-      const float v1 = fmaxf(__fsub_rn(e11, __fmul_rn(m1, m1)), 0.0f);
-      const float v2 = fmaxf(__fsub_rn(e22, __fmul_rn(m2, m2)), 0.0f);
-      const float cv = __fsub_rn(e12, __fmul_rn(m1, m2));
-      const float mu1 = __fadd_rn(m1, off), mu2 = __fadd_rn(m2, off);
-      // s1 s2 = sqrt(v1 v2) (0 for a flat window); c and cs share 1 / vden
-      const float sd12 = sqrt_approx(__fmul_rn(v1, v2));
-      const float vden = __fadd_rn(__fadd_rn(v1, v2), g.C2);
-      const float rv = rcp_approx(vden);
-      const float l = div_fast(__fadd_rn(__fmul_rn(2.0f, __fmul_rn(mu1, mu2)), g.C1),
-                               __fadd_rn(__fadd_rn(__fmul_rn(mu1, mu1), __fmul_rn(mu2, mu2)), g.C1));
-      const float c = div_by(__fadd_rn(__fmul_rn(2.0f, sd12), g.C2), vden, rv);
-      const float s = div_fast(__fadd_rn(cv, g.C3), __fadd_rn(sd12, g.C3));
-      const float cs = div_by(__fadd_rn(__fmul_rn(2.0f, cv), g.C2), vden, rv);
-      sum[0] = __fadd_rn(sum[0], l);
-      sum[1] = __fadd_rn(sum[1], c);
-      sum[2] = __fadd_rn(sum[2], s);
-      sum[3] = __fadd_rn(sum[3], cs);
-      sum[4] = __fadd_rn(sum[4], __fmul_rn(l, cs));
-    }
-  }
-  // warp sums in fp32 (a fixed xor tree; lane 0's order is fixed), then the
-  // block's eight warp sums in fp64 in warp order
-#pragma unroll
-  for (int q = 0; q < kQ; ++q) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum[q] = __fadd_rn(sum[q], __shfl_xor_sync(0xffffffffu, sum[q], o));
-  }
-  if ((t & 31) == 0) {
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) wsum[t >> 5][q] = sum[q];
+    for (int q = 0; q < kQ; ++q) wsum[warp][q] = dsum[q];
   }
   __syncthreads();
   if (t < kQ) {
     double acc = 0.0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) acc = __dadd_rn(acc, (double)wsum[w][t]);
+    for (int w = 0; w < 8; ++w) acc = __dadd_rn(acc, wsum[w][t]);
     const long long tile = g.tile_off[j] + blockIdx.y * g.tx[j] + blockIdx.x;
     part[((long long)frame * g.tiles_total + tile) * kQ + t] = acc;
   }
@@ -365,7 +407,7 @@ SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int c
   int tiles = 0;
   for (int j = 0; j < kScales; ++j) {
     g.tx[j] = (g.ws[j] - kWin + 1 + kTX - 1) / kTX;
-    g.ty[j] = (g.hs[j] - kWin + 1 + kTY - 1) / kTY;
+    g.ty[j] = (g.hs[j] - kWin + 1 + kBH - 1) / kBH;
     g.tile_off[j] = tiles;
     tiles += g.tx[j] * g.ty[j];
   }
