@@ -25,10 +25,12 @@
 //                   the five Gaussian means in fp32 as three packed pairs
 //                   (fma.rn.f32x2, products formed once per pixel); l, c,
 //                   s, cs, l cs per position (approximate reciprocals and
-//                   root refined to about an ulp); per step fp32 sums per
-//                   warp (fixed tree), then fp64 over the steps and the
-//                   block's warps into the (frame, scale, block) span (fp64
-//                   is slow on this part).  It also writes its share of the
+//                   root refined to about an ulp); a thread takes four
+//                   adjacent positions of a row (horizontal pass) and of a
+//                   column (vertical pass); per step fp32 sums per warp
+//                   (fixed tree), then fp64 over the steps and the block's
+//                   four warps into the (frame, scale, block) span (fp64 is
+//                   slow on this part).  It also writes its share of the
 //                   next scale: 2x2 means, exact in fp32 (a level-5 value is
 //                   at most 2^24 units of 2^-16, so every partial sum is
 //                   representable).
@@ -61,6 +63,7 @@ constexpr int kCH = 16;                    // output rows per step
 constexpr int kBH = 128;                   // output rows per band (8 steps)
 constexpr int kRing = 32;                  // rows of horizontal sums kept (>= kCH + kWin - 1)
 constexpr int kHalo = kWin - 1;            // input rows ahead of a band's first step
+constexpr int kLevelThreads = 128;         // 4 warps: 4 positions per thread in both passes
 static_assert(kCH % 2 == 0 && kHalo % 2 == 0 && kBH % kCH == 0, "row pairs stay in one step");
 
 struct MGeom {
@@ -119,7 +122,7 @@ __device__ __forceinline__ float div_by(float a, float b, float rb) {
 __device__ __forceinline__ float div_fast(float a, float b) { return div_by(a, b, rcp_approx(b)); }
 
 template <int MODE>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kLevelThreads)
     k_msssim_level(MGeom g, int j, const uint8_t *__restrict__ ref, const uint8_t *__restrict__ dis,
                    float *__restrict__ pyr, double *__restrict__ part) {
   // the five quantities as three fp32 pairs (p, q), (p p, q q), (p q, 0):
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(256)
   // padded by one pair: the horizontal pass runs row-fastest)
   __shared__ __align__(16) f2 PP[3][kCH][kIX + 1];
   __shared__ __align__(16) f2 HH[3][kRing][kTX + 1];
-  __shared__ double wsum[8][kQ];
+  __shared__ double wsum[kLevelThreads / 32][kQ];
   const int frame = blockIdx.z, t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int W = g.ws[j], Hh = g.hs[j];
   const int ox0 = blockIdx.x * kTX, oy0 = blockIdx.y * kBH;
@@ -143,10 +146,10 @@ __global__ void __launch_bounds__(256)
   for (int k = 0; k < kWin; ++k) gk[k] = f2_pack(g.gauss[k], g.gauss[k]);
 
   // input rows row0 .. row0 + n - 1 of the band (clamped to the plane) into
-  // PP rows 0 .. n - 1; thread t < 252 takes column t % 42 and rows t / 42,
-  // + 6, + 12, every load issued before the first is used
-  constexpr int kRowStep = 256 / kIX;                    // 6
-  constexpr int kPer = (kCH + kRowStep - 1) / kRowStep;  // 3
+  // PP rows 0 .. n - 1; thread t < 126 takes column t % 42 and rows t / 42,
+  // + 3, + 6, ..., every load issued before the first is used
+  constexpr int kRowStep = kLevelThreads / kIX;          // 3
+  constexpr int kPer = (kCH + kRowStep - 1) / kRowStep;  // 6
   const int lc = t % kIX, lr0 = t / kIX;
   const bool loader = t < kRowStep * kIX;
   const int xc = min(ox0 + lc, W - 1);
@@ -177,18 +180,18 @@ __global__ void __launch_bounds__(256)
     }
   };
   // horizontal sums of PP rows 0 .. n - 1 into ring rows (row0 + r) % 32: a
-  // thread takes 2 adjacent positions of one row, rows fastest across threads
+  // thread takes 4 adjacent positions of one row, rows fastest across threads
   auto hpass = [&](int row0, int n) {
-    if (t < n * (kTX / 2)) {
-      const int r = t % n, c0 = 2 * (t / n);
+    if (t < n * (kTX / 4)) {
+      const int r = t % n, c0 = 4 * (t / n);
       const int hr = (row0 + r) & (kRing - 1);
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
-        f2 v[kWin + 1];
+        f2 v[kWin + 3];
 #pragma unroll
-        for (int k = 0; k < kWin + 1; ++k) v[k] = PP[q][r][c0 + k];
+        for (int k = 0; k < kWin + 3; ++k) v[k] = PP[q][r][c0 + k];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
           f2 acc = 0ull;                                 // (+0, +0)
 #pragma unroll
           for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[i + k], acc);
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(256)
     const int nx = X1 - X0, cnt = nx * (yb - ya);
     float *na = pyr + (long long)(2 * frame) * g.img_floats + g.lvl_off[j + 1];
     float *nb = na + g.img_floats;
-    for (int i = t; i < cnt; i += 256) {
+    for (int i = t; i < cnt; i += kLevelThreads) {
       const int X = X0 + i % nx, Y = ya + i / nx;
       const int c0 = 2 * X - ox0, c1 = min(2 * X + 1, W - 1) - ox0;
       const int r0 = 2 * Y - oy0 - row0, r1 = min(2 * Y + 1, Hh - 1) - oy0 - row0;
@@ -249,18 +252,18 @@ __global__ void __launch_bounds__(256)
     next_scale(row0, kCH);
     __syncthreads();                                    // the ring is complete; PP is free
     if (st + 1 < nsteps) load_issue(row0 + kCH, kCH, va, vb);
-    // vertical sums and the terms of two positions (output rows 2 w, 2 w + 1
-    // of the step, w = thread / 32)
-    const int oc = t % kTX, orow = st * kCH + 2 * (t / kTX);
+    // vertical sums and the terms of four positions (output rows 4 w .. 4 w
+    // + 3 of the step, w = thread / 32)
+    const int oc = t % kTX, orow = st * kCH + 4 * (t / kTX);
     const int ox = ox0 + oc;
-    f2 m[2][3];
+    f2 m[4][3];
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
-      f2 v[kWin + 1];
+      f2 v[kWin + 3];
 #pragma unroll
-      for (int k = 0; k < kWin + 1; ++k) v[k] = HH[q][(orow + k) & (kRing - 1)][oc];
+      for (int k = 0; k < kWin + 3; ++k) v[k] = HH[q][(orow + k) & (kRing - 1)][oc];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < 4; ++i) {
         f2 acc = 0ull;
 #pragma unroll
         for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[i + k], acc);
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(256)
     }
     float sum[kQ] = {0, 0, 0, 0, 0};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const int oy = oy0 + orow + i;
       if (ox < ow && oy < oh) {
         float m1, m2, e11, e22, e12, unused;
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(256)
       if (lane == 0) dsum[q] = __dadd_rn(dsum[q], (double)sum[q]);
     }
   }
-  // the block's eight warp sums in fp64 in warp order
+  // the block's warp sums in fp64 in warp order
   if (lane == 0) {
 #pragma unroll
     for (int q = 0; q < kQ; ++q) wsum[warp][q] = dsum[q];
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(256)
   if (t < kQ) {
     double acc = 0.0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) acc = __dadd_rn(acc, wsum[w][t]);
+    for (int w = 0; w < kLevelThreads / 32; ++w) acc = __dadd_rn(acc, wsum[w][t]);
     const long long tile = g.tile_off[j] + blockIdx.y * g.tx[j] + blockIdx.x;
     part[((long long)frame * g.tiles_total + tile) * kQ + t] = acc;
   }
@@ -472,11 +475,11 @@ static cudaError_t msssim_batch(ss2_msssim *c, const uint8_t *ref, const uint8_t
     if (e != cudaSuccess) break;
     const dim3 grid(g.tx[j], g.ty[j], nb);
     if (j > 0)
-      k_msssim_level<2><<<grid, 256, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
+      k_msssim_level<2><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
     else if (g.bps == 1)
-      k_msssim_level<0><<<grid, 256, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
+      k_msssim_level<0><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
     else
-      k_msssim_level<1><<<grid, 256, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
+      k_msssim_level<1><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = c->timer.mark(0, false, st);
   }
