@@ -25,8 +25,10 @@
 //                     x1, x2, x1^2, x2^2, x1 x2 in fp32 as three packed pairs
 //                     (fma.rn.f32x2) on samples shifted by a per-tile offset
 //                     (variances and covariance do not change, cancellation
-//                     does), SSIM per pixel, fp32 warp sums in a fixed tree
-//                     and an fp64 sum of the block's warps.
+//                     does), SSIM per pixel (four vertical outputs per
+//                     thread, so one column's 14 loads serve four), fp32
+//                     warp sums in a fixed tree and an fp64 sum of the
+//                     block's four warps.
 //   k_fssim_final     per frame: block sums in a fixed warp order (fp64), mean.
 #include <cuda_runtime.h>
 
@@ -53,6 +55,7 @@ constexpr int kWin = 11;                   // Gaussian window
 constexpr int kTileX = 32, kTileY = 16;    // map outputs per block
 constexpr int kInX = kTileX + kWin - 1;    // input tile (42 x 26)
 constexpr int kInY = kTileY + kWin - 1;
+constexpr int kMapThreads = 128;           // 4 warps: 4 vertical outputs per thread
 
 struct FGeom {
   int w, h, depth, bps, scale, wd, hd, pitch;
@@ -470,14 +473,14 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMapThreads)
     k_fssim_map(FGeom g, const float *__restrict__ D, double *__restrict__ part) {
   // the five quantities as three fp32 pairs (a, b), (a a, b b), (a b, 0):
   // PP for the input tile, HH for the horizontal sums of every input row
   // (rows padded by one pair: the horizontal pass runs row-fastest)
   __shared__ __align__(16) f2 PP[3][kInY][kInX + 1];
   __shared__ __align__(16) f2 HH[3][kInY][kTileX + 1];
-  __shared__ float wsum[8];
+  __shared__ float wsum[kMapThreads / 32];
   const int frame = blockIdx.z;
   const int ox0 = blockIdx.x * kTileX, oy0 = blockIdx.y * kTileY;
   const float *pa = D + (long long)frame * 2 * g.plane;
@@ -486,9 +489,9 @@ __global__ void __launch_bounds__(256)
   // per-tile offset: the reference sample at the tile origin (same for both)
   const float off = pa[(long long)oy0 * g.pitch + ox0];
   // every load of a thread is issued before the first is used; thread
-  // t < 252 takes column t % 42 and rows t / 42, + 6, + 12, ...
-  constexpr int kRowStep = 256 / kInX;                   // 6
-  constexpr int kPer = (kInY + kRowStep - 1) / kRowStep;   // 5
+  // t < 126 takes column t % 42 and rows t / 42, + 3, + 6, ...
+  constexpr int kRowStep = kMapThreads / kInX;             // 3
+  constexpr int kPer = (kInY + kRowStep - 1) / kRowStep;   // 9
   const int c = t % kInX, r0 = t / kInX;
   const bool loader = t < kRowStep * kInX;
   const int xc = min(ox0 + c, g.wd - 1);
@@ -517,10 +520,10 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int k = 0; k < kWin; ++k) gk[k] = f2_pack(g.gauss[k], g.gauss[k]);
   __syncthreads();
-  // horizontal sums: a thread takes 4 adjacent outputs of one input row,
-  // rows fastest across threads (conflict-free 64-bit shared accesses)
-  if (t < kInY * (kTileX / 4)) {
-    const int r = t % kInY, c0 = 4 * (t / kInY);
+  // horizontal sums: a task is 4 adjacent outputs of one input row, rows
+  // fastest across threads (conflict-free 64-bit shared accesses)
+  for (int task = t; task < kInY * (kTileX / 4); task += kMapThreads) {
+    const int r = task % kInY, c0 = 4 * (task / kInY);
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       f2 v[kWin + 3];
@@ -536,17 +539,18 @@ __global__ void __launch_bounds__(256)
     }
   }
   __syncthreads();
-  // vertical sums and the SSIM terms of two outputs (rows 2 oy, 2 oy + 1)
-  const int oc = t % kTileX, orow = 2 * (t / kTileX);
+  // vertical sums and the SSIM terms of four outputs (rows 4 w .. 4 w + 3,
+  // w = thread / 32): 14 loads of a column serve four outputs
+  const int oc = t % kTileX, orow = 4 * (t / kTileX);
   const int ox = ox0 + oc;
-  f2 m[2][3];
+  f2 m[4][3];
 #pragma unroll
   for (int q = 0; q < 3; ++q) {
-    f2 v[kWin + 1];
+    f2 v[kWin + 3];
 #pragma unroll
-    for (int k = 0; k < kWin + 1; ++k) v[k] = HH[q][orow + k][oc];
+    for (int k = 0; k < kWin + 3; ++k) v[k] = HH[q][orow + k][oc];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < 4; ++j) {
       f2 acc = 0ull;
 #pragma unroll
       for (int k = 0; k < kWin; ++k) acc = f2_fma(gk[k], v[j + k], acc);
@@ -555,7 +559,7 @@ __global__ void __launch_bounds__(256)
   }
   float tile = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
+  for (int j = 0; j < 4; ++j) {
     const int oy = oy0 + orow + j;
     if (ox < g.ow && oy < g.oh) {
       float m1, m2, e11, e22, e12, unused;
@@ -575,7 +579,7 @@ __global__ void __launch_bounds__(256)
     }
   }
   // warp sums in fp32 (a fixed xor tree; lane 0's order is fixed), then the
-  // block's eight warp sums in fp64 in warp order (fp64 is slow on this part)
+  // block's four warp sums in fp64 in warp order (fp64 is slow on this part)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tile = __fadd_rn(tile, __shfl_xor_sync(0xffffffffu, tile, o));
   if ((t & 31) == 0) wsum[t >> 5] = tile;
@@ -583,7 +587,7 @@ __global__ void __launch_bounds__(256)
   if (t == 0) {
     double acc = 0.0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) acc = __dadd_rn(acc, (double)wsum[w]);
+    for (int w = 0; w < kMapThreads / 32; ++w) acc = __dadd_rn(acc, (double)wsum[w]);
     part[(long long)frame * g.tiles_x * g.tiles_y + blockIdx.y * g.tiles_x + blockIdx.x] = acc;
   }
 }
@@ -880,7 +884,7 @@ SS2_API int ss2_fssim_score(ss2_fssim *ctx, const void *ref, const void *dis, in
     if (e == cudaSuccess) e = ctx->timer.mark(0, false, st);
     if (e == cudaSuccess) e = ctx->timer.mark(1, true, st);
     if (e == cudaSuccess) {
-      k_fssim_map<<<dim3(g.tiles_x, g.tiles_y, nb), 256, 0, st>>>(g, ctx->d_dec, ctx->d_part);
+      k_fssim_map<<<dim3(g.tiles_x, g.tiles_y, nb), kMapThreads, 0, st>>>(g, ctx->d_dec, ctx->d_part);
       e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = ctx->timer.mark(1, false, st);
