@@ -15,7 +15,7 @@
 //
 //   k_msssim_level  one launch per scale over the batch; a block walks a
 //                   strip of 32 window positions across, down a band of up
-//                   to 128 rows, 16 rows at a time: each step loads the 16
+//                   to 512 rows, 16 rows at a time: each step loads the 16
 //                   new input rows of the 42-column strip (raw luma at
 //                   scale 1, fp32 planes after), shifted by the band's
 //                   first reference sample (variances and covariance do not
@@ -60,7 +60,7 @@ constexpr int kWin = 11;
 constexpr int kTX = 32;                    // window positions across a strip
 constexpr int kIX = kTX + kWin - 1;        // input columns of a strip: 42
 constexpr int kCH = 16;                    // output rows per step
-constexpr int kBH = 128;                   // output rows per band (8 steps)
+constexpr int kBH = 512;                   // output rows per band (32 steps)
 constexpr int kRing = 32;                  // rows of horizontal sums kept (>= kCH + kWin - 1)
 constexpr int kHalo = kWin - 1;            // input rows ahead of a band's first step
 constexpr int kLevelThreads = 128;         // 4 warps: 4 positions per thread in both passes
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kLevelThreads)
   };
   // the block's share of the next scale whose source rows are PP rows 0 ..
   // n - 1 (p + off restores each sample exactly; clamping matches the
-  // loads').  A block owns next-scale columns 16 bx .. and rows 64 by ..,
+  // loads').  A block owns next-scale columns 16 bx .. and rows 256 by ..,
   // the last strip and band up to the plane's edge; row pairs never
   // straddle two steps (even band origin, step and halo).
   const bool next = j + 1 < kScales;
