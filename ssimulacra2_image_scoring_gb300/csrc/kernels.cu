@@ -225,17 +225,21 @@ static_assert(sizeof(HWarpSmem) % 128 == 0, "every TMA box starts on 128 bytes")
 constexpr int kHSmemBytes = kHWarps * (int)sizeof(HWarpSmem) + kHWarps * kHSlots * 8 + 128;
 
 __global__ void __launch_bounds__(kHWarps * 32)
-    k_hblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, int *__restrict__ err) {
+    k_hblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, int nframes,
+            int *__restrict__ err) {
   extern __shared__ __align__(16) unsigned char hsm_raw[];
   unsigned char *hsm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(hsm_raw) + 127) & ~uintptr_t(127));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int frame = blockIdx.y;
-  const int unit = blockIdx.x * kHWarps + warp;
-  if (unit >= g.hunit_off[g.nscales]) return;  // whole warp
+  // units in scale-major order over the batch (every frame's scale-0 rows
+  // first): the longest walks start first and the shortest fill the tail
+  const int gu = blockIdx.x * kHWarps + warp;
+  if (gu >= g.hunit_off[g.nscales] * nframes) return;  // whole warp
   int s = 0;
-  while (unit >= g.hunit_off[s + 1]) ++s;
-  const int local = unit - g.hunit_off[s];
+  while (gu >= g.hunit_off[s + 1] * nframes) ++s;
+  const int ns = g.hunit_off[s + 1] - g.hunit_off[s];
+  const int frame = (gu - g.hunit_off[s] * nframes) / ns;
+  const int local = (gu - g.hunit_off[s] * nframes) % ns;
   const int nrb = (g.hs[s] + kBoxRows - 1) / kBoxRows;
   const int c = local / nrb, row0 = (local % nrb) * kBoxRows;
   const int nchunk = (g.ws[s] + kBoxCols - 1) / kBoxCols;
@@ -450,17 +454,20 @@ constexpr int kVSmemBytes = kVWarps * (int)sizeof(VWarpSmem) + kVWarps * 4 * 8 +
 
 __global__ void __launch_bounds__(kVWarps * 32)
     k_vblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, const float *__restrict__ X,
-            float2 *__restrict__ part, int *__restrict__ err) {
+            int nframes, float2 *__restrict__ part, int *__restrict__ err) {
   extern __shared__ __align__(16) unsigned char vsm_raw[];
   unsigned char *vsm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(vsm_raw) + 1023) & ~uintptr_t(1023));
-  const int frame = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wid = blockIdx.x * kVWarps + warp;
-  if (wid >= g.vwarp_off[g.nscales]) return;  // whole warp exits together
+  // column walkers in scale-major order over the batch (every frame's
+  // scale-0 columns first): the longest walks start first
+  const int gw = blockIdx.x * kVWarps + warp;
+  if (gw >= g.vwarp_off[g.nscales] * nframes) return;  // whole warp exits together
   int s = 0;
-  while (wid >= g.vwarp_off[s + 1]) ++s;
-  const int local = wid - g.vwarp_off[s];
+  while (gw >= g.vwarp_off[s + 1] * nframes) ++s;
+  const int ns = g.vwarp_off[s + 1] - g.vwarp_off[s];
+  const int frame = (gw - g.vwarp_off[s] * nframes) / ns;
+  const int local = (gw - g.vwarp_off[s] * nframes) % ns;
   const int c = local % 3, cb = local / 3;
   const int col0 = cb * kVCols;
   const bool active = col0 + lane < g.ws[s];
@@ -698,8 +705,8 @@ cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, in
     configured[dev] = true;
   }
   const int units = g.hunit_off[g.nscales];
-  dim3 grid((units + kHWarps - 1) / kHWarps, nframes);
-  k_hblur<<<grid, kHWarps * 32, kHSmemBytes, st>>>(g, px, maps, err);
+  const dim3 grid((units * nframes + kHWarps - 1) / kHWarps);
+  k_hblur<<<grid, kHWarps * 32, kHSmemBytes, st>>>(g, px, maps, nframes, err);
   return cudaGetLastError();
 }
 
@@ -715,8 +722,8 @@ cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, co
     configured[dev] = true;
   }
   const int warps = g.vwarp_off[g.nscales];
-  dim3 grid((warps + kVWarps - 1) / kVWarps, nframes);
-  k_vblur<<<grid, kVWarps * 32, kVSmemBytes, st>>>(g, px, maps, X, part, err);
+  const dim3 grid((warps * nframes + kVWarps - 1) / kVWarps);
+  k_vblur<<<grid, kVWarps * 32, kVSmemBytes, st>>>(g, px, maps, X, nframes, part, err);
   return cudaGetLastError();
 }
 
