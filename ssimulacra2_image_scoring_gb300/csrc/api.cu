@@ -749,11 +749,14 @@ SS2_API int ss2_score_frames_host(ss2_ctx *ctx, const void *ref_host, const void
   const long long fb = ctx->g.frame_bytes;
   const size_t half = (size_t)ctx->batch * (size_t)fb;
   const uint8_t *r8 = (const uint8_t *)ref_host, *d8 = (const uint8_t *)dis_host;
-  int nbat, base, extra;
-  batch_plan(n_frames, ctx->batch, &nbat, &base, &extra);
+  // Nothing overlaps the first batch's upload, so the first batch is a
+  // quarter of a full one (rounded up); the rest are planned as usual.
+  const int first = std::min(n_frames, (ctx->batch + 3) / 4);
+  int nbat = 0, base = 0, extra = 0;
+  if (n_frames > first) batch_plan(n_frames - first, ctx->batch, &nbat, &base, &extra);
   if (fork_lanes(ctx, st)) return t_err;
-  for (int b = 0, f0 = 0; b < nbat; ++b) {
-    const int nb = base + (b < extra ? 1 : 0);
+  for (int b = 0, f0 = 0; b <= nbat; ++b) {
+    const int nb = b == 0 ? first : base + (b - 1 < extra ? 1 : 0);
     Lane &L = ctx->lane[b % kLanes];
     uint8_t *dref = L.in, *ddis = L.in + half;
     // slot fence: the upload waits for the kernel that last read this lane's slot

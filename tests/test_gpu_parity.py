@@ -169,7 +169,11 @@ def test_host_input_path_matches_device_path(cuda):
         pd = torch.from_numpy(wl.dis).pin_memory()
         s_host = sc.score_host(pr, pd)
         s_page = sc.score_host(wl.ref, wl.dis)
+        # calls no longer than the host path's short first batch
+        s_one = sc.score_host(pr[:1], pd[:1])
+        s_two = sc.score_host(pr[:2], pd[:2])
     assert np.array_equal(s_dev, s_host) and np.array_equal(s_dev, s_page)
+    assert np.array_equal(s_dev[:1], s_one) and np.array_equal(s_dev[:2], s_two)
 
 
 def test_context_reuse_two_geometries(cuda):
