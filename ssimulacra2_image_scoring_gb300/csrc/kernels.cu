@@ -55,12 +55,20 @@ __global__ void __launch_bounds__(kPyrThreads)
               const uint8_t *__restrict__ dis, float *__restrict__ X) {
   __shared__ float L[6][kLvlTotal];
   __shared__ float cb_s[3];
+  // 8-bit samples: the two normalisation tables in shared memory
+  __shared__ float ntab[BPS == 1 ? 512 : 1];
   const int frame = blockIdx.z;
   const int tx0 = blockIdx.x * kTile, ty0 = blockIdx.y * kTile;
   float *Xf = X + (long long)frame * g.x_fs;
 
   // cbrt(bias_i), once per block
   if (threadIdx.x < 3) cb_s[threadIdx.x] = cbrt_cr(px.bias[threadIdx.x]);
+  if (BPS == 1 && tabs.ynorm) {
+    for (int i = threadIdx.x; i < 256; i += kPyrThreads) {
+      ntab[i] = __ldg(tabs.ynorm + i);
+      ntab[256 + i] = __ldg(tabs.cnorm + i);
+    }
+  }
   __syncthreads();
   float cb[3];
 #pragma unroll
@@ -93,7 +101,11 @@ __global__ void __launch_bounds__(kPyrThreads)
         const int Us = read_sample<BPS>(f, ysz + ci);
         const int Vs = read_sample<BPS>(f, ysz + csz + ci);
         float yn, cbv, crv;
-        if (tabs.ynorm) {
+        if (BPS == 1 && tabs.ynorm) {
+          yn = ntab[Ys];
+          cbv = ntab[256 + Us];
+          crv = ntab[256 + Vs];
+        } else if (tabs.ynorm) {
           yn = __ldg(tabs.ynorm + Ys);
           cbv = __ldg(tabs.cnorm + Us);
           crv = __ldg(tabs.cnorm + Vs);
