@@ -739,10 +739,29 @@ cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, co
   return cudaGetLastError();
 }
 
+// k_finalize is launched at the device's highest priority: its few blocks
+// then take the next free SM slots ahead of the other lane's pending blocks,
+// and the lane's stream moves on to its next batch sooner.
 cudaError_t launch_finalize(const Geom &g, const float2 *part, const double *params,
                             double *values, double *scores, int nframes, cudaStream_t st) {
-  k_finalize<<<nframes, 128, 0, st>>>(g, part, params, values, scores);
-  return cudaGetLastError();
+  static int greatest = 1;   // numerically lowest priority value; 1 = not yet read
+  if (greatest == 1) {
+    int least = 0, hi = 0;
+    const cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &hi);
+    if (e != cudaSuccess) return e;
+    greatest = hi;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nframes);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributePriority;
+  attr[0].val.priority = greatest;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_finalize, g, part, params, values, scores);
 }
 
 }  // namespace ss2
