@@ -317,9 +317,7 @@ int ss2::encode_maps(const Geom &g, float *X, float *H, int batch, PlaneMaps &m)
         encode_stack(&m.h[s], hb, ws, hs, 3 * kNq, batch, g.pitch[s], g.plane[s], g.h_fs,
                      kBoxCols, kBoxRows, 1) ||
         encode_stack(&m.hv[s], hb, ws, hs, 3 * kNq, batch, g.pitch[s], g.plane[s], g.h_fs,
-                     kVCols, kVRows, kNq) ||
-        encode_stack(&m.xv[s], xb, ws, hs, 6, batch, g.pitch[s], g.plane[s], g.x_fs, kVCols,
-                     kVRows, 1))
+                     kVCols, kVRows, kNq))
       return t_err;
   }
   return 0;

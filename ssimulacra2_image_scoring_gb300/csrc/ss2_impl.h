@@ -44,17 +44,15 @@ struct Geom {
   int vwarp_off[kMaxScales + 1];   // prefix of 3 * nw[s]            (vertical warps)
 };
 
-// TMA descriptors of the plane stacks, one per scale.  x[s] / xv[s] view the
-// XYB block as a 4-D tensor (column, row, plane 0..5, frame), h[s] / hv[s]
-// the horizontally blurred block (column, row, plane 0..14, frame).
+// TMA descriptors of the plane stacks, one per scale.  x[s] views the XYB
+// block as a 4-D tensor (column, row, plane 0..5, frame), h[s] / hv[s] the
+// horizontally blurred block (column, row, plane 0..14, frame).
 //   x, h:  8-column x 32-row boxes (row walkers of the horizontal pass)
 //   hv:    32-column x 8-row x 5-plane boxes (column walkers, one channel)
-//   xv:    32-column x 8-row boxes
 struct PlaneMaps {
   CUtensorMap x[kMaxScales];
   CUtensorMap h[kMaxScales];
   CUtensorMap hv[kMaxScales];
-  CUtensorMap xv[kMaxScales];
 };
 constexpr int kBoxCols = 8, kBoxRows = 32;      // horizontal pass box
 constexpr int kVCols = 32, kVRows = 8;          // vertical pass box
