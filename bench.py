@@ -21,7 +21,7 @@ L2.  Per-kernel CUDA events inside the library give the dominant kernel's
 average launch time for the roofline; nvidia-smi samples the clocks during
 the timed region; e2e repeats the measurement through the host-input entry
 point with pinned host buffers (upload and 8-byte-per-frame read-back
-inside the timed region; the median of three windows of K steps).  The
+inside the timed region; the median of five windows of K steps).  The
 oracle, timed on the host cores over a bounded sample, is the CPU baseline.
 
 --impl reference: the oracle (plain single-threaded C, one thread per frame
@@ -381,9 +381,9 @@ def run_ours(args, ws, rank, local):
     pd = torch.from_numpy(wl.dis).pin_memory()
     sc.score_host(pr, pd, stream)  # allocates the upload slots once
     # the host's memory is shared with other jobs on the machine: the median
-    # of three timed windows of K calls each
+    # of five timed windows of K calls each
     windows = []
-    for _ in range(3):
+    for _ in range(5):
         barrier(ws)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
