@@ -617,7 +617,7 @@ def cambi_levels(wl):
     return np.ascontiguousarray(y.reshape(-1, sp.height, sp.width))
 
 
-CAMBI_GROUP = 8   # lanes sharing a core histogram in k_cambi_cvalues
+CAMBI_GROUP = 4   # lanes sharing a core histogram in k_cambi_cvalues
 
 
 def cambi_updates(w, h, win):

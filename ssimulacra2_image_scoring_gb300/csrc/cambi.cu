@@ -18,19 +18,19 @@
 //                    step the warp stages the leaving and entering row
 //                    segments in shared memory (fetched one step ahead).  A
 //                    window's count is split in two: the columns that all
-//                    eight lanes of a lane group share go to the group's
-//                    core histogram (32-bit bins, shared-memory atomics,
-//                    the columns dealt out among the eight lanes; two 16-bit
-//                    bins to a 32-bit word); the seven columns left to each
-//                    lane go to its own histogram (16-bit bins interleaved
-//                    by lane so each lane owns its elements, plain loads and
-//                    stores).  A column whose leaving and entering pixels
-//                    agree is skipped.  At 65 x 65 a pixel costs about 29
-//                    bin updates instead of 130.  Planes with at most 256
+//                    four lanes of a lane group share go to the group's
+//                    core histogram (16-bit bins, two to a 32-bit word,
+//                    shared-memory atomics, the columns dealt out among the
+//                    four lanes); the three columns left to each lane go to
+//                    its own histogram (8-bit bins interleaved by lane so
+//                    each lane owns its elements, plain loads and stores).
+//                    A column whose leaving and entering pixels agree is
+//                    skipped.  At 65 x 65 a pixel costs about 37 bin
+//                    updates instead of 130.  Planes with at most 256
 //                    distinct levels (8-bit video as 10-bit levels) index
 //                    bins by the level's rank among those present (a 2 KB
-//                    table per warp): 18 KB of bins per warp instead of
-//                    72 KB.
+//                    table per warp): 12 KB of bins per warp instead of
+//                    48 KB.
 //   k_cambi_hist     radix histogram of one 11/11/10-bit digit of the values
 //                    that match the digits chosen so far.
 //   k_cambi_select   one block per plane: the digit holding the k-th largest
@@ -58,14 +58,14 @@ using namespace ss2;
 
 constexpr int kLevels = 1024;
 constexpr int kMaxWin2 = 4225;
-constexpr int kGroup = 8;                          // lanes sharing a core histogram
+constexpr int kGroup = 4;                          // lanes sharing a core histogram
 constexpr int kGroups = 32 / kGroup;
 constexpr int kOwnMax = kGroup - 1;                // columns a lane counts alone (at most)
 // per warp: 32 lanes' own 16-bit bins, then the groups' core bins (16-bit,
 // two to a 32-bit word)
-constexpr int cv_smem(int bins) { return bins * 32 * 2 + kGroups * bins * 2; }
-constexpr int kCvSmem = cv_smem(1024);             // 72 KB
-constexpr int kCvSmemCompact = cv_smem(256);       // 18 KB: the compact histograms
+constexpr int cv_smem(int bins) { return bins * 32 * 1 + kGroups * bins * 2; }
+constexpr int kCvSmem = cv_smem(1024);             // 48 KB
+constexpr int kCvSmemCompact = cv_smem(256);       // 12 KB: the compact histograms
 constexpr int kMaxCount = 2 * kMaxWin2;            // p0 + pm <= 8450: the reciprocal table's range
 constexpr int kErrLevel = 2;                       // a level >= 1024 was seen
 constexpr int kErrValue = 4;                       // a value off the 2^-24 grid or >= 2^14
@@ -102,31 +102,36 @@ __global__ void __launch_bounds__(256)
 }
 
 // k_cambi_cvalues<BINS>: one warp per 32 output columns of a plane; lane =
-// column.  Lane l's window covers segment columns l .. l + 2r.  The eight
-// lanes of group q (lanes 8q .. 8q+7) all cover columns 8q+7 .. 8q+2r: the
+// column.  Lane l's window covers segment columns l .. l + 2r.  The four
+// lanes of group q (lanes 4q .. 4q+3) all cover columns 4q+3 .. 4q+2r: the
 // group's core, counted once in a histogram of BINS 16-bit bins packed two
 // to a 32-bit word, which the group's lanes update with 32-bit shared-memory
-// atomics (+-1 or +-2^16), each taking every eighth core column.  The steps'
-// updates commute and every final count lies in 0..3770, so the packed word
+// atomics (+-1 or +-2^16), each taking every fourth core column.  The steps'
+// updates commute and every final count lies in 0..4030, so the packed word
 // holds both counts exactly once a step's updates are all in, whatever the
-// borrows and carries between the halves along the way.  The rest of a lane's window (8q+7-1-j columns on the left
-// and j on the right for lane 8q+j, seven in all) goes to the lane's own
-// histogram of BINS 16-bit bins (element bin * 32 + lane, plain loads and
-// stores; a count stays in 0..455).  A window narrower than a group has no
-// core: each lane counts its whole window alone.  A count is the core bin
-// plus the own bin.  With BINS = 256 a level is replaced by its rank among
-// the levels present in the plane (8-bit video as 10-bit levels has at most
-// 256); planes with more levels run the BINS = 1024 variant, which uses the
-// levels themselves.  Both variants are launched; a block whose plane belongs
-// to the other one returns at once.  Each step the warp stages the leaving
-// and entering row segments in shared memory (fetched one step ahead); a
-// column whose two pixels agree is skipped.
+// borrows and carries between the halves along the way.  The rest of a
+// lane's window (2-j columns on the left and j on the right for lane 4q+j,
+// three in all) goes to the lane's own histogram of BINS 8-bit bins
+// (element bin * 32 + lane, plain loads and stores; a count stays in
+// 0..195).  A window narrower than a group has no core: each lane counts
+// its whole window (at most 3 x 3 pixels) alone.  A count is the core bin
+// plus the own bin.  Groups of four rather than eight cost more core
+// updates per pixel (2 x 62 / 4 against 2 x 58 / 8) but let the own bins
+// be 8-bit: 14.7 KB of shared memory per warp instead of 20.7 KB, 14
+// resident warps per SM instead of 10, and the kernel waits on its step
+// chains more than it issues.  With BINS = 256 a level is replaced by its
+// rank among the levels present in the plane (8-bit video as 10-bit levels
+// has at most 256); planes with more levels run the BINS = 1024 variant,
+// which uses the levels themselves.  Both variants are launched; a block
+// whose plane belongs to the other one returns at once.  Each step the warp
+// stages the leaving and entering row segments in shared memory (fetched
+// one step ahead); a column whose two pixels agree is skipped.
 template <int BINS>
 __global__ void __launch_bounds__(32)
     k_cambi_cvalues(CGeom g, const uint16_t *__restrict__ levels, const uint8_t *__restrict__ mask,
                     const unsigned *__restrict__ present, const float *__restrict__ recip,
                     float *__restrict__ out, int *__restrict__ err) {
-  extern __shared__ uint16_t cv_hist[];            // own bins (BINS x 32 lanes), then the cores
+  extern __shared__ __align__(16) uint8_t cv_hist[];   // own 8-bit bins (BINS x 32 lanes), then the cores
   __shared__ uint16_t seg[2][kSeg];
   __shared__ unsigned pbits[kLevels / 32];         // levels present in the plane
   __shared__ unsigned prank[kLevels / 32];         // present levels below each word
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(32)
   const uint16_t *L = levels + base;
   const uint8_t *M = mask ? mask + base : nullptr;
   unsigned *cores = reinterpret_cast<unsigned *>(cv_hist + BINS * 32);
-  for (int i = lane; i < BINS * 32; i += 32) cv_hist[i] = 0u;
+  for (int i = lane; i < BINS * 8; i += 32) reinterpret_cast<unsigned *>(cv_hist)[i] = 0u;
   for (int i = lane; i < kGroups * BINS / 2; i += 32) cores[i] = 0u;
   const int r = g.window / 2;
   const int nseg = 32 + 2 * r;
@@ -219,8 +224,8 @@ __global__ void __launch_bounds__(32)
       // a != b: two different bins, both read before either is written
       const unsigned ca_ = a[t] != kSkip ? cv_hist[a[t] * 32 + lane] : 0u;
       const unsigned cb_ = b[t] != kSkip ? cv_hist[b[t] * 32 + lane] : 0u;
-      if (a[t] != kSkip) cv_hist[a[t] * 32 + lane] = (uint16_t)(ca_ - 1u);
-      if (b[t] != kSkip) cv_hist[b[t] * 32 + lane] = (uint16_t)(cb_ + 1u);
+      if (a[t] != kSkip) cv_hist[a[t] * 32 + lane] = (uint8_t)(ca_ - 1u);
+      if (b[t] != kSkip) cv_hist[b[t] * 32 + lane] = (uint8_t)(cb_ + 1u);
     }
     for (int t = 0; t < ncore; ++t) {
       const int i = ca + jl + t * kGroup;
