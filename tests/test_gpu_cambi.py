@@ -28,8 +28,12 @@ def _levels(h, w, seed, base=300, spread=6):
 CASES = [  # (h, w, window, diffs, weights, masked)
     (61, 97, 9, [1], [1], False),
     (61, 97, 1, [1, 2], [1, 2], False),
-    (50, 70, 7, [1, 2], [3, 1], True),              # narrower than a lane group: no core
-    (47, 83, 11, [1, 4], [2, 2], False),            # a core of four columns
+    # windows around the lane-group size (cores of 0, 2, 4 and 8 columns
+    # with groups of four lanes)
+    (37, 45, 3, [1], [2], False),
+    (44, 58, 5, [1, 3], [1, 1], True),
+    (50, 70, 7, [1, 2], [3, 1], True),
+    (47, 83, 11, [1, 4], [2, 2], False),
     (128, 256, 33, [1, 2, 3, 4], [1, 2, 3, 4], True),
     (270, 480, 65, [1, 3], [2, 9], False),
     (40, 33, 65, [2], [5], True),
