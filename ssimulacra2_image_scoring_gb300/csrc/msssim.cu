@@ -19,9 +19,12 @@
 //                   new input rows of the 42-column strip (raw luma at
 //                   scale 1, fp32 planes after), shifted by the band's
 //                   first reference sample (variances and covariance do not
-//                   change, cancellation does), and forms their horizontal
-//                   Gaussian sums once into a 32-row ring, from which the
-//                   vertical sums of the step's 16 output rows are read;
+//                   change, cancellation does), keeps (p, q) and (p q, 0)
+//                   per pixel, and forms the horizontal Gaussian sums of
+//                   (p, q), its squares and (p q, 0) once into a 32-row
+//                   ring, from which the vertical sums of the step's 16
+//                   output rows are read (36 KB and 76 registers: six
+//                   four-warp blocks per SM);
 //                   the five Gaussian means in fp32 as three packed pairs
 //                   (fma.rn.f32x2, products formed once per pixel); l, c,
 //                   s, cs, l cs per position (approximate reciprocals and
@@ -121,14 +124,24 @@ __device__ __forceinline__ float div_by(float a, float b, float rb) {
 
 __device__ __forceinline__ float div_fast(float a, float b) { return div_by(a, b, rcp_approx(b)); }
 
+// a * b per half, one rounding each (mul.rn.f32x2): the same bits as two
+// scalar __fmul_rn
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(kLevelThreads)
+__global__ void __launch_bounds__(kLevelThreads, 6)
     k_msssim_level(MGeom g, int j, const uint8_t *__restrict__ ref, const uint8_t *__restrict__ dis,
                    float *__restrict__ pyr, double *__restrict__ part) {
   // the five quantities as three fp32 pairs (p, q), (p p, q q), (p q, 0):
-  // PP for a step's new input rows, HH the ring of horizontal sums (rows
-  // padded by one pair: the horizontal pass runs row-fastest)
-  __shared__ __align__(16) f2 PP[3][kCH][kIX + 1];
+  // PP holds (p, q) and (p q, 0) of a step's new input rows ((p p, q q) is
+  // formed from (p, q) in the horizontal pass), HH the ring of horizontal
+  // sums of all three (rows padded by one pair: the horizontal pass runs
+  // row-fastest)
+  __shared__ __align__(16) f2 PP[2][kCH][kIX + 1];
   __shared__ __align__(16) f2 HH[3][kRing][kTX + 1];
   __shared__ double wsum[kLevelThreads / 32][kQ];
   const int frame = blockIdx.z, t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -174,8 +187,7 @@ __global__ void __launch_bounds__(kLevelThreads)
         const float p = __fsub_rn(va[k], off);     // exact: both lie on the same grid below 256
         const float q = __fsub_rn(vb[k], off);
         PP[0][r][lc] = f2_pack(p, q);
-        PP[1][r][lc] = f2_pack(__fmul_rn(p, p), __fmul_rn(q, q));
-        PP[2][r][lc] = f2_pack(__fmul_rn(p, q), 0.0f);
+        PP[1][r][lc] = f2_pack(__fmul_rn(p, q), 0.0f);
       }
     }
   };
@@ -185,11 +197,13 @@ __global__ void __launch_bounds__(kLevelThreads)
     if (t < n * (kTX / 4)) {
       const int r = t % n, c0 = 4 * (t / n);
       const int hr = (row0 + r) & (kRing - 1);
+      f2 v[kWin + 3];
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
-        f2 v[kWin + 3];
+        // q = 0: (p, q) as loaded; q = 1: its squares; q = 2: (p q, 0)
 #pragma unroll
-        for (int k = 0; k < kWin + 3; ++k) v[k] = PP[q][r][c0 + k];
+        for (int k = 0; k < kWin + 3; ++k)
+          v[k] = q == 0 ? PP[0][r][c0 + k] : (q == 1 ? f2_mul(v[k], v[k]) : PP[1][r][c0 + k]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           f2 acc = 0ull;                                 // (+0, +0)
