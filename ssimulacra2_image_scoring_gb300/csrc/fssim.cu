@@ -473,12 +473,22 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-__global__ void __launch_bounds__(kMapThreads)
+// a * b per half, one rounding each (mul.rn.f32x2): the same bits as two
+// scalar __fmul_rn
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__global__ void __launch_bounds__(kMapThreads, 5)
     k_fssim_map(FGeom g, const float *__restrict__ D, double *__restrict__ part) {
   // the five quantities as three fp32 pairs (a, b), (a a, b b), (a b, 0):
-  // PP for the input tile, HH for the horizontal sums of every input row
-  // (rows padded by one pair: the horizontal pass runs row-fastest)
-  __shared__ __align__(16) f2 PP[3][kInY][kInX + 1];
+  // PP holds (a, b) and (a b, 0) of the input tile ((a a, b b) is formed
+  // from (a, b) in the horizontal pass), HH the horizontal sums of all three
+  // for every input row (rows padded by one pair: the horizontal pass runs
+  // row-fastest)
+  __shared__ __align__(16) f2 PP[2][kInY][kInX + 1];
   __shared__ __align__(16) f2 HH[3][kInY][kTileX + 1];
   __shared__ float wsum[kMapThreads / 32];
   const int frame = blockIdx.z;
@@ -512,8 +522,7 @@ __global__ void __launch_bounds__(kMapThreads)
       const float p = __fsub_rn(va[k], off);
       const float q = __fsub_rn(vb[k], off);
       PP[0][r][c] = f2_pack(p, q);
-      PP[1][r][c] = f2_pack(__fmul_rn(p, p), __fmul_rn(q, q));
-      PP[2][r][c] = f2_pack(__fmul_rn(p, q), 0.0f);
+      PP[1][r][c] = f2_pack(__fmul_rn(p, q), 0.0f);
     }
   }
   f2 gk[kWin];
@@ -524,11 +533,13 @@ __global__ void __launch_bounds__(kMapThreads)
   // fastest across threads (conflict-free 64-bit shared accesses)
   for (int task = t; task < kInY * (kTileX / 4); task += kMapThreads) {
     const int r = task % kInY, c0 = 4 * (task / kInY);
+    f2 v[kWin + 3];
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
-      f2 v[kWin + 3];
+      // q = 0: (a, b) as loaded; q = 1: its squares; q = 2: (a b, 0)
 #pragma unroll
-      for (int k = 0; k < kWin + 3; ++k) v[k] = PP[q][r][c0 + k];
+      for (int k = 0; k < kWin + 3; ++k)
+        v[k] = q == 0 ? PP[0][r][c0 + k] : (q == 1 ? f2_mul(v[k], v[k]) : PP[1][r][c0 + k]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         f2 acc = 0ull;
