@@ -505,6 +505,11 @@ static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
     e = cudaMemcpy(c->d_params, c->params, sizeof(c->params), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMallocHost((void **)&c->h_err, sizeof(int));
+  // The copies and the memset are ordered on the legacy default stream only
+  // (a copy from pageable memory may still be in flight when cudaMemcpy
+  // returns); the scoring calls run on non-blocking streams, so they are
+  // waited for here.
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cuda_fail(e, "uploading constant tables");
     free_ctx(c);
@@ -559,6 +564,8 @@ SS2_API int ss2_set_params(ss2_ctx *ctx, const double *params, int n_params) {
   set_pix(ctx);
   CU(cudaMemcpy(ctx->d_params, ctx->params, sizeof(ctx->params), cudaMemcpyHostToDevice),
      "uploading parameters");
+  // in place before any later call on a non-blocking stream reads them
+  CU(cudaDeviceSynchronize(), "uploading parameters");
   return 0;
 }
 

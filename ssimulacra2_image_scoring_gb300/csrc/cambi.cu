@@ -546,8 +546,12 @@ SS2_API ss2_cambi *ss2_cambi_create(int width, int height, int window, int ndiff
     // nearest, so entry n is 1/n correctly rounded
     std::vector<float> r(kMaxCount + 1, 0.0f);
     for (int n = 1; n <= kMaxCount; ++n) r[n] = 1.0f / (float)n;
+    // the copy and the memsets above are ordered on the legacy stream only
+    // (a pageable copy may still be in flight when cudaMemcpy returns):
+    // wait for them before any call on a non-blocking stream
     if (cudaMemcpy(c->d_recip, r.data(), r.size() * sizeof(float), cudaMemcpyHostToDevice) !=
-        cudaSuccess) {
+            cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
       cudaGetLastError();
       fail(SS2_EIO, "cambi reciprocal table upload failed");
       cambi_free(c);

@@ -769,7 +769,9 @@ SS2_API ss2_fssim *ss2_fssim_create(int width, int height, int bitdepth, int chr
       cudaMalloc(&c->d_scores, B * sizeof(double)) != cudaSuccess ||
       cudaMalloc(&c->d_err, sizeof(int)) != cudaSuccess ||
       cudaMallocHost(&c->h_err, sizeof(int)) != cudaSuccess ||
-      cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) {
+      cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess ||
+      // the memset is ordered on the legacy stream only: wait for it
+      cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     fail(SS2_ENOMEM, "float_ssim workspace allocation failed");
     fssim_free(c);

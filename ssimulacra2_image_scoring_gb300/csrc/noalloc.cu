@@ -83,6 +83,8 @@ static int scratch_for_device(int dev, unsigned char **out) {
     if (e == cudaSuccess)
       e = cudaMemcpy(base + kParamsOff, params, sizeof(params), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(base + kErrOff, 0, sizeof(int));
+    // ordered on the legacy stream only: wait before the caller's stream runs
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "scratch set-up copy");
     g_dev_ptr[dev] = base;
   }
