@@ -120,6 +120,8 @@ def lib() -> ctypes.CDLL:
             L.ss2o_msssim_pyramid.restype = i
             L.ss2o_msssim.argtypes = [vp, vp, i, i, i, vp, vp]
             L.ss2o_msssim.restype = i
+            L.ss2o_msssim_planes.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
+            L.ss2o_msssim_planes.restype = i
             L.ss2o_blur_line.argtypes = [vp, i, vp]
             L.ss2o_downsample.argtypes = [vp, i, i, vp]
             _lib = L
@@ -393,3 +395,16 @@ def downsample(plane: np.ndarray) -> np.ndarray:
     out = np.zeros(((h + 1) // 2, (w + 1) // 2), np.float32)
     lib().ss2o_downsample(_ptr(plane), w, h, _ptr(out))
     return out
+
+
+def msssim_planes(ref: np.ndarray, dis: np.ndarray, w: int, h: int, depth: int, chroma: int,
+                  nplanes: int = 3):
+    """(scores[nplanes], values[nplanes][5][5]) of one packed frame pair: MS-SSIM
+    of the luma plane and, with nplanes = 3, of Cb and Cr at chroma resolution."""
+    sc = np.zeros(nplanes, np.float64)
+    v = np.zeros((nplanes, MSSSIM_SCALES, 5), np.float64)
+    rc = lib().ss2o_msssim_planes(_ptr(np.ascontiguousarray(ref)), _ptr(np.ascontiguousarray(dis)),
+                                  w, h, depth, chroma, nplanes, _ptr(sc), _ptr(v))
+    if rc != 0:
+        raise ValueError(f"msssim planes rejected {w}x{h} chroma {chroma}: rc={rc}")
+    return sc, v

@@ -29,6 +29,11 @@
  *     exponents; a negative mean gives NaN, as pow does).
  * Samples are taken in the 8-bit range, raw / 2^(depth - 8), with L = 255
  * (the reading the float_ssim oracle takes for the same family of features).
+ * With enable_chroma (Finding 6 lists it among float_ms_ssim's outputs and
+ * asks for a span per (plane, scale)), the Cb and Cr planes are scored too,
+ * each on its own at chroma resolution (ceil(w / 2^sx) x ceil(h / 2^sy))
+ * with the same method and constants: the page names the option only, so
+ * the plainest reading is one MS-SSIM score per plane.
  * Everything is fp64.  Frames whose scale-5 plane is below 11x11 are refused
  * (-95).
  */
@@ -184,5 +189,31 @@ int ss2o_msssim(const void *ref, const void *dis, int w, int h, int depth, doubl
     if (values) memcpy(values, m, sizeof(m));
     free(pa);
     free(pb);
+    return 0;
+}
+
+/* Per-plane scores of a packed frame pair: plane 0 is luma, 1 Cb, 2 Cr
+ * (nplanes 1 or 3).  scores[p], values[p][5][5] (values may be NULL).    */
+int ss2o_msssim_planes(const void *ref, const void *dis, int w, int h, int depth,
+                       int chroma, int nplanes, double *scores, double *values)
+{
+    int sx, sy;
+    switch (chroma) {
+    case 420: sx = 1; sy = 1; break;
+    case 422: sx = 1; sy = 0; break;
+    case 444: sx = 0; sy = 0; break;
+    default: return -22;
+    }
+    if (nplanes != 1 && nplanes != 3) return -22;
+    const size_t bps = depth > 8 ? 2 : 1;
+    const int cw = (w + sx) >> sx, ch = (h + sy) >> sy;
+    for (int p = 0; p < nplanes; ++p) {
+        const int pw = p ? cw : w, ph = p ? ch : h;
+        const size_t off = p == 0 ? 0 : (size_t)w * h + (size_t)(p - 1) * cw * ch;
+        const int rc = ss2o_msssim((const uint8_t *)ref + off * bps,
+                                   (const uint8_t *)dis + off * bps, pw, ph, depth,
+                                   scores + p, values ? values + (size_t)p * 25 : NULL);
+        if (rc) return rc;
+    }
     return 0;
 }

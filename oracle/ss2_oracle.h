@@ -131,6 +131,11 @@ int ss2o_msssim_pyramid(const void *frame, int width, int height, int bitdepth,
                         double *levels);
 int ss2o_msssim(const void *ref, const void *dis, int width, int height,
                 int bitdepth, double *score, double *values);
+/* MS-SSIM per plane of a packed frame pair (Y, then Cb and Cr at chroma
+ * resolution when nplanes = 3): scores[nplanes], values[nplanes][5][5]. */
+int ss2o_msssim_planes(const void *ref, const void *dis, int width, int height,
+                       int bitdepth, int chroma, int nplanes, double *scores,
+                       double *values);
 
 #ifdef __cplusplus
 }

@@ -13,7 +13,11 @@ results that follow from that definition by a different route:
     score is prod_{j<=k} mean(cs_j)^beta_j, with mean(cs_j) counted over the
     window phases (pins beta_1 .. beta_4, the window and the pyramid);
   - a pattern against its negative: the structure term (cov + C3) /
-    (s1 s2 + C3) with cov = -s^2 (pins C3 = C2 / 2).
+    (s1 s2 + C3) with cov = -s^2 (pins C3 = C2 / 2);
+  - with the chroma planes (enable_chroma): the block pattern placed in the
+    Cb or the Cr plane alone, at chroma resolution, gives that plane the
+    closed-form score and the other two planes exactly 1, at 4:2:0, 4:2:2
+    and 4:4:4 (pins each plane's offset, size and order).
 """
 from __future__ import annotations
 
@@ -147,3 +151,39 @@ def test_smallest_frame():
     g = _frame(np.zeros((160, 161), np.int64))
     with pytest.raises(ValueError):
         oracle.msssim(g, g, 161, 160, 8)
+
+
+@pytest.mark.parametrize("chroma", [420, 422, 444])
+@pytest.mark.parametrize("plane", [1, 2])
+def test_chroma_planes_carry_their_own_pattern(chroma, plane):
+    W, H, a, c0, k = 704, 384, 20.0, 128.0, 2
+    sx, sy = {420: (1, 1), 422: (1, 0), 444: (0, 0)}[chroma]
+    cw, ch = (W + sx) >> sx, (H + sy) >> sy
+    b = 1 << (k - 1)
+    flat_y = np.full(W * H, 100, np.uint8)
+    flat_c = np.full(cw * ch, int(c0), np.uint8)
+    pat = (c0 + a * np.outer(_pattern(ch, b), _pattern(cw, b))).astype(np.uint8).ravel()
+    ref = np.concatenate([flat_y, flat_c, flat_c])
+    dis = np.concatenate([flat_y, pat if plane == 1 else flat_c, pat if plane == 2 else flat_c])
+    sc, v = oracle.msssim_planes(ref, dis, W, H, 8, chroma)
+    want = 1.0
+    for j in range(1, k + 1):
+        mcs = _mean_cs_of_pattern(cw >> (j - 1), ch >> (j - 1), 1 << (k - j), a)
+        assert abs(v[plane, j - 1, 3] - mcs) <= 1e-12, (j, v[plane, j - 1, 3], mcs)
+        want *= mcs ** BETA[j - 1]
+    assert abs(sc[plane] - want) <= 1e-12 and want < 0.99
+    other = 3 - plane
+    assert sc[0] == 1.0 and sc[other] == 1.0
+
+
+def test_identical_chroma_scores_one_with_distorted_luma():
+    rng = np.random.default_rng(3)
+    W, H = 400, 352
+    a = rng.integers(0, 256, W * H + 2 * (W // 2) * (H // 2)).astype(np.uint8)
+    b = a.copy()
+    b[:W * H] = np.clip(a[:W * H].astype(int) + rng.integers(-20, 21, W * H), 0, 255)
+    sc, v = oracle.msssim_planes(a, b, W, H, 8, 420)
+    assert sc[0] < 0.99 and sc[1] == 1.0 and sc[2] == 1.0
+    assert np.all(v[1:] == 1.0)
+    luma, _ = oracle.msssim(a, b, W, H, 8)
+    assert sc[0] == luma

@@ -49,6 +49,9 @@ MUTATIONS = {
                         "while (n < SS2O_NSCALES && w >= 9 && h >= 9) {"),
     "norm_limited_range_219_as_220": ("const float dy = (float)(219 * k), dc = (float)(224 * k);",
                                       "const float dy = (float)(220 * k), dc = (float)(224 * k);"),
+    "default_c2_0_003": ("p[SS2O_P_C2] = 0.0009;", "p[SS2O_P_C2] = 0.003;"),
+    "default_c2_0_0005": ("p[SS2O_P_C2] = 0.0009;", "p[SS2O_P_C2] = 0.0005;"),
+    "default_c2_0_0015": ("p[SS2O_P_C2] = 0.0009;", "p[SS2O_P_C2] = 0.0015;"),
 }
 
 
@@ -93,6 +96,10 @@ MSSSIM_MUTATIONS = {
                                       "const double norm = 1.0;"),
     "msssim_product_skips_scale_4": ("for (int j = 0; j < NSCALE - 1; ++j) ms *= pow(m[j][3], kBeta[j]);",
                                      "for (int j = 0; j < NSCALE - 2; ++j) ms *= pow(m[j][3], kBeta[j]);"),
+    "msssim_cr_reads_cb": ("(size_t)w * h + (size_t)(p - 1) * cw * ch;",
+                           "(size_t)w * h + (size_t)0 * cw * ch;"),
+    "msssim_chroma_width_uses_sy": ("const int cw = (w + sx) >> sx, ch = (h + sy) >> sy;",
+                                    "const int cw = (w + sy) >> sy, ch = (h + sy) >> sy;"),
 }
 
 # Planted slips in the CAMBI oracle, caught by tests/test_cambi_pins.py.

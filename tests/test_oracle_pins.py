@@ -229,6 +229,77 @@ def test_ssim_term_on_flat_frames_is_the_squared_mean_difference():
     assert (xyb[1][inner].mean() - xyb[4][inner].mean()) ** 2 > 1e-3
 
 
+def test_ssim_and_edge_terms_around_an_impulse_pin_c2():
+    """One bright luma pixel on a gray reference against the flat gray frame,
+    with the affine set so that both frames' XYB planes are exactly zero but
+    for the reference's Y value delta at the impulse.  Blurring is linear, so
+    with h the pinned 1-D impulse response and H = h(dx) h(dy):
+        mu1 = delta H, s11 = delta^2 H, mu2 = s22 = s12 = 0,
+        d   = 1 - (1 - delta^2 H^2) C2 / (delta^2 H (1 - H) + C2),
+        det = a / (1 + a), a = |x1 - mu1|, art = 0.
+    Near the impulse delta^2 H is of the order of C2, so the SSIM term depends
+    on C2 at first order: the textbook stabiliser C2 = (K2 L)^2 with K2 = 0.03
+    and dynamic range L = 1 must be the default (a value 0.0005 or 0.0015
+    moves the terms by over 40%).  Scales 0 and 1 (where the impulse is
+    still large against the fp32 rounding of the variances)."""
+    w = h = 128
+    Yf, dY = 126, 60
+    chroma = np.full(w * h, 128, np.uint8)
+    luma = np.full((h, w), Yf, np.uint8)
+    dis = np.concatenate([luma.ravel(), chroma, chroma])
+    luma[64, 64] = Yf + dY
+    ref = np.concatenate([luma.ravel(), chroma, chroma])
+    p = oracle.default_params()
+    _, _, d0 = oracle.score(ref, dis, w, h, 8, 444, p, dump_scale=0)
+    y_flat = float(d0["xyb"][4, 0, 0])
+    # X' = 0 X + 0, Y' = Y - Y(flat gray), B' = (B - Y) 0 + 0
+    p[oracle.P_AFFINE:oracle.P_AFFINE + 5] = [0.0, 0.0, -y_flat, 0.0, 0.0]
+    c2 = 0.03 ** 2
+    n = 201
+    e = np.zeros(n, np.float32)
+    e[n // 2] = 1.0
+    hl = oracle.blur_line(e).astype(np.float64)
+    _, vals, _ = oracle.score(ref, dis, w, h, 8, 444, p)
+    vals = vals.reshape(3, 6, 2, 3)
+    for s in (0, 1):
+        _, _, dump = oracle.score(ref, dis, w, h, 8, 444, p, dump_scale=s)
+        xyb = dump["xyb"]
+        py = px = 64 >> s
+        delta = float(xyb[1, py, px])
+        assert delta > 0.05
+        rest = xyb.copy()
+        rest[1, py, px] = 0.0
+        assert not np.any(rest), "the XYB planes must vanish off the impulse"
+        sh, sw = xyb.shape[1:]
+        hy = hl[n // 2 - py:n // 2 - py + sh]
+        hx = hl[n // 2 - px:n // 2 - px + sw]
+        H = np.outer(hy, hx)
+        dd = delta * delta
+        d_want = 1.0 - (1.0 - dd * H * H) * c2 / (dd * H * (1.0 - H) + c2)
+        x1 = np.zeros_like(H)
+        x1[py, px] = delta
+        a = np.abs(x1 - delta * H)
+        det_want = a / (1.0 + a)
+        supp = (slice(py - 4, py + 5), slice(px - 4, px + 5))
+        terms = dump["terms"]
+        d_got, art_got, det_got = terms[6], terms[8], terms[10]
+        assert np.all(np.abs(d_got - d_want)[supp] <= 1e-4 * d_want[supp]), s
+        assert np.all(np.abs(det_got - det_want)[supp] <= 1e-4 * det_want[supp]), s
+        assert not np.any(art_got)
+        # off the 9x9 support only rounding residue of the recursions is left
+        off = np.ones_like(H, bool)
+        off[supp] = False
+        assert d_got[off].sum() <= 1e-3 and det_got[off].sum() <= 1e-4
+        # the pooled 1-norms and 4-norms of the Y channel at this scale
+        N = sh * sw
+        assert abs(vals[1, s, 0, 0] - d_want[supp].sum() / N) <= 1e-4 * vals[1, s, 0, 0]
+        assert abs(vals[1, s, 1, 0] - (np.sum(d_want[supp] ** 4) / N) ** 0.25) \
+            <= 1e-4 * vals[1, s, 1, 0]
+        assert abs(vals[1, s, 0, 2] - det_want.sum() / N) <= 1e-4 * vals[1, s, 0, 2]
+        assert vals[1, s, 0, 1] == 0.0 and vals[1, s, 1, 1] == 0.0
+    assert not np.any(vals[0]) and not np.any(vals[2])
+
+
 def test_edge_terms_tell_lost_detail_from_artifacts():
     """A flat distorted frame against a textured reference loses detail
     (det >> art); a textured distorted frame against a flat reference has
