@@ -280,18 +280,28 @@ void ss2_fssim_destroy(ss2_fssim *ctx);
  * 0.2856, 0.3001, 0.2363, 0.1333).  All scales of a batch are enqueued at
  * once; one stream synchronisation per call.
  *   ss2_msssim_create: geometry as ss2_create; max_batch 0 = 32 frames per
- *     pass.  NULL with -ENOTSUP when the scale-5 plane is below 11x11 (a
- *     side below 161), -EINVAL for bad geometry, -ENOMEM.
+ *     pass; the luma plane only.  NULL with -ENOTSUP when the scale-5 plane
+ *     is below 11x11 (a side below 161), -EINVAL for bad geometry, -ENOMEM.
+ *   ss2_msssim_create_ex: as ss2_msssim_create; enable_chroma != 0 also
+ *     scores the Cb and Cr planes (Finding 6 lists enable_chroma among the
+ *     outputs), each on its own at chroma resolution (ceil(w / 2^sx) x
+ *     ceil(h / 2^sy)) with the same method: NULL with -ENOTSUP when a
+ *     chroma plane's scale-5 plane is below 11x11.
+ *   ss2_msssim_planes: the planes a context scores, 1 or 3 (-EINVAL for
+ *     NULL).
  *   ss2_msssim_score: ref, dis DEVICE frames (n_frames packed frames each,
- *     owned by the caller, read only); scores HOST doubles (n_frames);
- *     values HOST doubles (n_frames x 5 scales x (l, c, s, cs, l cs)) or
- *     NULL.  0 on success; -EINVAL for a NULL context or pointer or a
- *     negative count (0 frames: no work); -ENOMEM when the pinned staging
- *     cannot grow; -EIO on a CUDA failure.  The context owns its workspace:
- *     scales 2..5 of both images (fp32, rows padded to 32 floats) and the
- *     per-(frame, scale, tile) partial sums of each frame of the batch.
- *   ss2_msssim_debug_pyramid: scales 2..5 of one frame pair (HOST floats:
- *     ref scales 2..5 then dis scales 2..5, each w_j x h_j packed).
+ *     owned by the caller, read only); scores HOST doubles (n_frames x
+ *     planes, frame-major: Y then Cb, Cr); values HOST doubles (n_frames x
+ *     planes x 5 scales x (l, c, s, cs, l cs)) or NULL.  0 on success;
+ *     -EINVAL for a NULL context or pointer or a negative count (0 frames:
+ *     no work); -ENOMEM when the pinned staging cannot grow; -EIO on a CUDA
+ *     failure.  The context owns its workspace: per plane, scales 2..5 of
+ *     both images (fp32, rows padded to 32 floats) and the per-(frame,
+ *     scale, tile) partial sums of each frame of the batch.
+ *   ss2_msssim_debug_pyramid: scales 2..5 of the luma plane of one frame
+ *     pair (HOST floats: ref scales 2..5 then dis scales 2..5, each w_j x
+ *     h_j packed); ss2_msssim_debug_pyramid_plane: the same for plane 0, 1
+ *     or 2 (-EINVAL for a plane the context does not score).
  *   ss2_msssim_profile_begin / _end: as ss2_profile_begin / _end, kernel
  *     classes 0 k_msssim_level (all scales), 1 k_msssim_final (ms: 2
  *     doubles, launches: 2 ints, either may be NULL).
@@ -299,10 +309,15 @@ void ss2_fssim_destroy(ss2_fssim *ctx);
 typedef struct ss2_msssim ss2_msssim;
 ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int chroma,
                               int max_batch);
+ss2_msssim *ss2_msssim_create_ex(int width, int height, int bitdepth, int chroma,
+                                 int max_batch, int enable_chroma);
+int ss2_msssim_planes(const ss2_msssim *ctx);
 int ss2_msssim_score(ss2_msssim *ctx, const void *ref, const void *dis,
                      int n_frames, double *scores, double *values, void *stream);
 int ss2_msssim_debug_pyramid(ss2_msssim *ctx, const void *ref, const void *dis,
                              float *planes, void *stream);
+int ss2_msssim_debug_pyramid_plane(ss2_msssim *ctx, const void *ref, const void *dis,
+                                   int plane, float *planes, void *stream);
 int ss2_msssim_profile_begin(ss2_msssim *ctx);
 int ss2_msssim_profile_end(ss2_msssim *ctx, double *ms, int *launches);
 void ss2_msssim_destroy(ss2_msssim *ctx);

@@ -1,10 +1,12 @@
-// msssim.cu — MS-SSIM of the luma plane on the device (ss2_msssim_* in
-// include/ss2.h).
+// msssim.cu — MS-SSIM on the device (ss2_msssim_* in include/ss2.h): of the
+// luma plane, and with enable_chroma of the Cb and Cr planes as well, each
+// on its own at chroma resolution.
 //
 // Source: "Research-1363: Device-resident ssimulacra2 and a single-wait
 // MS-SSIM on SYCL" (vmafx documentation), Finding 6: every scale of a frame
-// is enqueued at once, each scale's partial sums go to a span of their own,
-// and the host waits once.  The method is Wang, Simoncelli and Bovik,
+// is enqueued at once, each (plane, scale) has a span of partial sums of its
+// own, and the host waits once; the outputs are the default score, the
+// per-scale terms (enable_lcs) and the chroma planes (enable_chroma).  The method is Wang, Simoncelli and Bovik,
 // "Multi-scale structural similarity for image quality assessment" (2003):
 // five scales of a 2x2-average pyramid (edge sample repeated), the SSIM
 // statistics of an 11x11 Gaussian window (sigma 1.5) wherever it fits,
@@ -70,8 +72,9 @@ constexpr int kLevelThreads = 128;         // 4 warps: 4 positions per thread in
 static_assert(kCH % 2 == 0 && kHalo % 2 == 0 && kBH % kCH == 0, "row pairs stay in one step");
 
 struct MGeom {
-  int w, h, depth, bps;
+  int w, h, depth, bps;          // the plane's size (luma, or a chroma plane)
   long long frame_bytes;
+  long long plane_off;           // byte offset of the plane inside a frame
   float norm;                    // 2^(8 - depth)
   int ws[kScales], hs[kScales];  // plane size per scale
   int pitch[kScales];            // fp32 pitch of scales 2..5 (index 1..4)
@@ -149,8 +152,8 @@ __global__ void __launch_bounds__(kLevelThreads, 6)
   const int ox0 = blockIdx.x * kTX, oy0 = blockIdx.y * kBH;
   const int ow = W - kWin + 1, oh = Hh - kWin + 1;
   const int nsteps = (min(kBH, oh - oy0) + kCH - 1) / kCH;
-  const uint8_t *ra = ref + (long long)frame * g.frame_bytes;
-  const uint8_t *rb = dis + (long long)frame * g.frame_bytes;
+  const uint8_t *ra = ref + (long long)frame * g.frame_bytes + g.plane_off;
+  const uint8_t *rb = dis + (long long)frame * g.frame_bytes + g.plane_off;
   const float *pa = pyr + (long long)(2 * frame) * g.img_floats + g.lvl_off[j];
   const float *pb = pa + g.img_floats;
   const float off = sample<MODE>(g, j, ra, pa, ox0, oy0);
@@ -338,10 +341,11 @@ __global__ void __launch_bounds__(kLevelThreads, 6)
 
 // One block per frame, one warp per (scale, quantity): the span summed with
 // lane l taking tiles l, l + 32, ... in order and a fixed xor tree; then the
-// means and the score.
+// means and the score of one plane.  scores / values point at the plane's
+// entry of frame 0; frames are nplanes entries apart.
 __global__ void __launch_bounds__(kScales * kQ * 32)
     k_msssim_final(MGeom g, const double *__restrict__ part, double *__restrict__ scores,
-                   double *__restrict__ values) {
+                   double *__restrict__ values, int nplanes) {
   __shared__ double mean[kScales * kQ];
   const int frame = blockIdx.x, wq = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int j = wq / kQ, q = wq % kQ;
@@ -354,24 +358,26 @@ __global__ void __launch_bounds__(kScales * kQ * 32)
   if (lane == 0) {
     const double cnt = (double)(g.ws[j] - kWin + 1) * (double)(g.hs[j] - kWin + 1);
     mean[wq] = s / cnt;
-    values[(long long)frame * kScales * kQ + wq] = s / cnt;
+    values[(long long)frame * nplanes * kScales * kQ + wq] = s / cnt;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     double ms = 1.0;
     for (int k = 0; k + 1 < kScales; ++k) ms *= pow(mean[k * kQ + 3], g.beta[k]);
     ms *= pow(mean[(kScales - 1) * kQ + 4], g.beta[kScales - 1]);
-    scores[frame] = ms;
+    scores[(long long)frame * nplanes] = ms;
   }
 }
 
 }  // namespace
 
 struct ss2_msssim {
-  MGeom g;
+  int nplanes;                             // 1 (luma) or 3 (luma, Cb, Cr)
+  MGeom g[3];
   int batch, device;
-  float *d_pyr = nullptr;                  // scales 2..5 of both images, per frame
-  double *d_part = nullptr, *d_scores = nullptr, *d_values = nullptr;
+  float *d_pyr[3] = {};                    // per plane: scales 2..5 of both images, per frame
+  double *d_part[3] = {};                  // per plane: the (frame, scale, tile) spans
+  double *d_scores = nullptr, *d_values = nullptr;   // frame-major, nplanes per frame
   double *h_scores = nullptr, *h_values = nullptr;
   size_t h_cap = 0;
   KernelTimer timer;                         // per-kernel event timing
@@ -379,8 +385,10 @@ struct ss2_msssim {
 
 static void msssim_free(ss2_msssim *c) {
   if (!c) return;
-  cudaFree(c->d_pyr);
-  cudaFree(c->d_part);
+  for (int p = 0; p < 3; ++p) {
+    cudaFree(c->d_pyr[p]);
+    cudaFree(c->d_part[p]);
+  }
   cudaFree(c->d_scores);
   cudaFree(c->d_values);
   if (c->h_scores) cudaFreeHost(c->h_scores);
@@ -388,21 +396,16 @@ static void msssim_free(ss2_msssim *c) {
   delete c;
 }
 
-SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int chroma,
-                                      int max_batch) {
-  if (check_geometry(width, height, bitdepth, chroma)) return nullptr;
-  if (max_batch < 0 || max_batch > 4096) {
-    fail(SS2_EINVAL, "batch %d is outside 0..4096", max_batch);
-    return nullptr;
-  }
-  MGeom g;
+// Geometry of one plane (pw x ph samples at byte offset plane_off of each
+// frame); -ENOTSUP when its scale-5 plane is below the 11x11 window.
+static int make_mgeom(int pw, int ph, int bitdepth, long long frame_bytes, long long plane_off,
+                      const char *name, MGeom &g) {
   std::memset(&g, 0, sizeof(g));
-  g.w = width; g.h = height; g.depth = bitdepth; g.bps = bitdepth > 8 ? 2 : 1;
-  Geom full;
-  make_geom(width, height, bitdepth, chroma, full);
-  g.frame_bytes = full.frame_bytes;
+  g.w = pw; g.h = ph; g.depth = bitdepth; g.bps = bitdepth > 8 ? 2 : 1;
+  g.frame_bytes = frame_bytes;
+  g.plane_off = plane_off;
   g.norm = 1.0f / (float)(1 << (bitdepth - 8));
-  int w = width, h = height;
+  int w = pw, h = ph;
   long long off = 0;
   for (int j = 0; j < kScales; ++j) {
     g.ws[j] = w;
@@ -416,11 +419,9 @@ SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int c
     h = (h + 1) / 2;
   }
   g.img_floats = (off + 63) & ~63LL;
-  if (g.ws[kScales - 1] < kWin || g.hs[kScales - 1] < kWin) {
-    fail(SS2_ENOTSUP, "MS-SSIM: the scale-5 plane %dx%d is below the 11x11 window",
-         g.ws[kScales - 1], g.hs[kScales - 1]);
-    return nullptr;
-  }
+  if (g.ws[kScales - 1] < kWin || g.hs[kScales - 1] < kWin)
+    return fail(SS2_ENOTSUP, "MS-SSIM: the %s plane's scale-5 plane %dx%d is below the 11x11 window",
+                name, g.ws[kScales - 1], g.hs[kScales - 1]);
   int tiles = 0;
   for (int j = 0; j < kScales; ++j) {
     g.tx[j] = (g.ws[j] - kWin + 1 + kTX - 1) / kTX;
@@ -442,6 +443,28 @@ SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int c
   for (int i = 0; i < kWin; ++i) g.gauss[i] = (float)(gs[i] / tot);
   const double beta[kScales] = {0.0448, 0.2856, 0.3001, 0.2363, 0.1333};
   for (int j = 0; j < kScales; ++j) g.beta[j] = beta[j];
+  return 0;
+}
+
+SS2_API ss2_msssim *ss2_msssim_create_ex(int width, int height, int bitdepth, int chroma,
+                                         int max_batch, int enable_chroma) {
+  if (check_geometry(width, height, bitdepth, chroma)) return nullptr;
+  if (max_batch < 0 || max_batch > 4096) {
+    fail(SS2_EINVAL, "batch %d is outside 0..4096", max_batch);
+    return nullptr;
+  }
+  Geom full;
+  make_geom(width, height, bitdepth, chroma, full);
+  const int np = enable_chroma ? 3 : 1;
+  MGeom g[3];
+  const long long bps = full.bps, ysz = (long long)width * height,
+                  csz = (long long)full.cw * full.ch;
+  static const char *names[3] = {"luma", "Cb", "Cr"};
+  for (int p = 0; p < np; ++p) {
+    const int pw = p ? full.cw : width, ph = p ? full.ch : height;
+    const long long off = p == 0 ? 0 : (ysz + (p - 1) * csz) * bps;
+    if (make_mgeom(pw, ph, bitdepth, full.frame_bytes, off, names[p], g[p])) return nullptr;
+  }
   int dev = 0;
   if (check_device(&dev)) return nullptr;
   ss2_msssim *c = new (std::nothrow) ss2_msssim();
@@ -449,20 +472,34 @@ SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int c
     fail(SS2_ENOMEM, "host allocation failed");
     return nullptr;
   }
-  c->g = g;
+  c->nplanes = np;
+  for (int p = 0; p < np; ++p) c->g[p] = g[p];
   c->device = dev;
   c->batch = max_batch ? max_batch : 32;
   const size_t B = (size_t)c->batch;
-  if (cudaMalloc(&c->d_pyr, B * 2 * g.img_floats * sizeof(float)) != cudaSuccess ||
-      cudaMalloc(&c->d_part, B * g.tiles_total * kQ * sizeof(double)) != cudaSuccess ||
-      cudaMalloc(&c->d_scores, B * sizeof(double)) != cudaSuccess ||
-      cudaMalloc(&c->d_values, B * kScales * kQ * sizeof(double)) != cudaSuccess) {
+  bool ok = true;
+  for (int p = 0; p < np && ok; ++p)
+    ok = cudaMalloc(&c->d_pyr[p], B * 2 * g[p].img_floats * sizeof(float)) == cudaSuccess &&
+         cudaMalloc(&c->d_part[p], B * g[p].tiles_total * kQ * sizeof(double)) == cudaSuccess;
+  ok = ok && cudaMalloc(&c->d_scores, B * np * sizeof(double)) == cudaSuccess &&
+       cudaMalloc(&c->d_values, B * np * kScales * kQ * sizeof(double)) == cudaSuccess;
+  if (!ok) {
     cudaGetLastError();
     fail(SS2_ENOMEM, "MS-SSIM workspace allocation failed");
     msssim_free(c);
     return nullptr;
   }
   return c;
+}
+
+SS2_API ss2_msssim *ss2_msssim_create(int width, int height, int bitdepth, int chroma,
+                                      int max_batch) {
+  return ss2_msssim_create_ex(width, height, bitdepth, chroma, max_batch, 0);
+}
+
+SS2_API int ss2_msssim_planes(const ss2_msssim *ctx) {
+  if (!ctx) return fail(SS2_EINVAL, "NULL context");
+  return ctx->nplanes;
 }
 
 SS2_API void ss2_msssim_destroy(ss2_msssim *ctx) { msssim_free(ctx); }
@@ -479,30 +516,34 @@ SS2_API int ss2_msssim_profile_end(ss2_msssim *ctx, double *ms, int *launches) {
   return e == cudaSuccess ? 0 : cuda_fail(e, "MS-SSIM profile events");
 }
 
-// The five scale launches and the final one for nb frames.
+// For each plane, the five scale launches and the final one, for nb frames
+// (all enqueued; the caller waits once).
 static cudaError_t msssim_batch(ss2_msssim *c, const uint8_t *ref, const uint8_t *dis, int nb,
                                 cudaStream_t st) {
-  const MGeom &g = c->g;
   cudaError_t e = cudaSuccess;
-  for (int j = 0; j < kScales && e == cudaSuccess; ++j) {
-    e = c->timer.mark(0, true, st);
-    if (e != cudaSuccess) break;
-    const dim3 grid(g.tx[j], g.ty[j], nb);
-    if (j > 0)
-      k_msssim_level<2><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
-    else if (g.bps == 1)
-      k_msssim_level<0><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
-    else
-      k_msssim_level<1><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr, c->d_part);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) e = c->timer.mark(0, false, st);
+  for (int p = 0; p < c->nplanes && e == cudaSuccess; ++p) {
+    const MGeom &g = c->g[p];
+    for (int j = 0; j < kScales && e == cudaSuccess; ++j) {
+      e = c->timer.mark(0, true, st);
+      if (e != cudaSuccess) break;
+      const dim3 grid(g.tx[j], g.ty[j], nb);
+      if (j > 0)
+        k_msssim_level<2><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr[p], c->d_part[p]);
+      else if (g.bps == 1)
+        k_msssim_level<0><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr[p], c->d_part[p]);
+      else
+        k_msssim_level<1><<<grid, kLevelThreads, 0, st>>>(g, j, ref, dis, c->d_pyr[p], c->d_part[p]);
+      e = cudaGetLastError();
+      if (e == cudaSuccess) e = c->timer.mark(0, false, st);
+    }
+    if (e == cudaSuccess) e = c->timer.mark(1, true, st);
+    if (e == cudaSuccess) {
+      k_msssim_final<<<nb, kScales * kQ * 32, 0, st>>>(
+          g, c->d_part[p], c->d_scores + p, c->d_values + (size_t)p * kScales * kQ, c->nplanes);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = c->timer.mark(1, false, st);
   }
-  if (e == cudaSuccess) e = c->timer.mark(1, true, st);
-  if (e == cudaSuccess) {
-    k_msssim_final<<<nb, kScales * kQ * 32, 0, st>>>(g, c->d_part, c->d_scores, c->d_values);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess) e = c->timer.mark(1, false, st);
   return e;
 }
 
@@ -517,47 +558,53 @@ SS2_API int ss2_msssim_score(ss2_msssim *ctx, const void *ref, const void *dis, 
     if (ctx->h_values) cudaFreeHost(ctx->h_values);
     ctx->h_scores = ctx->h_values = nullptr;
     ctx->h_cap = 0;
-    if (cudaMallocHost(&ctx->h_scores, (size_t)n_frames * sizeof(double)) != cudaSuccess ||
-        cudaMallocHost(&ctx->h_values, (size_t)n_frames * kScales * kQ * sizeof(double)) !=
+    if (cudaMallocHost(&ctx->h_scores, (size_t)n_frames * ctx->nplanes * sizeof(double)) !=
+            cudaSuccess ||
+        cudaMallocHost(&ctx->h_values,
+                       (size_t)n_frames * ctx->nplanes * kScales * kQ * sizeof(double)) !=
             cudaSuccess) {
       cudaGetLastError();
       return fail(SS2_ENOMEM, "pinned allocation failed");
     }
     ctx->h_cap = (size_t)n_frames;
   }
-  const MGeom &g = ctx->g;
+  const long long fb = ctx->g[0].frame_bytes;
+  const size_t np = (size_t)ctx->nplanes;
   cudaStream_t st = (cudaStream_t)stream;
   const uint8_t *r8 = (const uint8_t *)ref, *d8 = (const uint8_t *)dis;
   for (int f0 = 0; f0 < n_frames; f0 += ctx->batch) {
     const int nb = std::min(ctx->batch, n_frames - f0);
-    cudaError_t e = msssim_batch(ctx, r8 + f0 * g.frame_bytes, d8 + f0 * g.frame_bytes, nb, st);
+    cudaError_t e = msssim_batch(ctx, r8 + f0 * fb, d8 + f0 * fb, nb, st);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(ctx->h_scores + f0, ctx->d_scores, nb * sizeof(double),
+      e = cudaMemcpyAsync(ctx->h_scores + f0 * np, ctx->d_scores, nb * np * sizeof(double),
                           cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && values)
-      e = cudaMemcpyAsync(ctx->h_values + (size_t)f0 * kScales * kQ, ctx->d_values,
-                          (size_t)nb * kScales * kQ * sizeof(double), cudaMemcpyDeviceToHost, st);
+      e = cudaMemcpyAsync(ctx->h_values + (size_t)f0 * np * kScales * kQ, ctx->d_values,
+                          (size_t)nb * np * kScales * kQ * sizeof(double),
+                          cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) return cuda_fail(e, "MS-SSIM launch");
   }
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  std::memcpy(scores, ctx->h_scores, (size_t)n_frames * sizeof(double));
+  std::memcpy(scores, ctx->h_scores, (size_t)n_frames * np * sizeof(double));
   if (values)
-    std::memcpy(values, ctx->h_values, (size_t)n_frames * kScales * kQ * sizeof(double));
+    std::memcpy(values, ctx->h_values, (size_t)n_frames * np * kScales * kQ * sizeof(double));
   return 0;
 }
 
-SS2_API int ss2_msssim_debug_pyramid(ss2_msssim *ctx, const void *ref, const void *dis,
-                                     float *planes, void *stream) {
+SS2_API int ss2_msssim_debug_pyramid_plane(ss2_msssim *ctx, const void *ref, const void *dis,
+                                           int plane, float *planes, void *stream) {
   if (!ctx || !ref || !dis || !planes) return fail(SS2_EINVAL, "NULL argument");
-  const MGeom &g = ctx->g;
+  if (plane < 0 || plane >= ctx->nplanes)
+    return fail(SS2_EINVAL, "plane %d is not scored by this context", plane);
+  const MGeom &g = ctx->g[plane];
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = msssim_batch(ctx, (const uint8_t *)ref, (const uint8_t *)dis, 1, st);
   size_t off = 0;
   for (int img = 0; img < 2 && e == cudaSuccess; ++img)
     for (int j = 1; j < kScales && e == cudaSuccess; ++j) {
       e = cudaMemcpy2DAsync(planes + off, g.ws[j] * sizeof(float),
-                            ctx->d_pyr + img * g.img_floats + g.lvl_off[j],
+                            ctx->d_pyr[plane] + img * g.img_floats + g.lvl_off[j],
                             g.pitch[j] * sizeof(float), g.ws[j] * sizeof(float), g.hs[j],
                             cudaMemcpyDeviceToHost, st);
       off += (size_t)g.ws[j] * g.hs[j];
@@ -565,4 +612,9 @@ SS2_API int ss2_msssim_debug_pyramid(ss2_msssim *ctx, const void *ref, const voi
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "MS-SSIM pyramid");
   return 0;
+}
+
+SS2_API int ss2_msssim_debug_pyramid(ss2_msssim *ctx, const void *ref, const void *dis,
+                                     float *planes, void *stream) {
+  return ss2_msssim_debug_pyramid_plane(ctx, ref, dis, 0, planes, stream);
 }

@@ -94,6 +94,12 @@ def lib() -> ctypes.CDLL:
             L.ss2_cambi_destroy.restype = None
             L.ss2_msssim_create.argtypes = [i, i, i, i, i]
             L.ss2_msssim_create.restype = vp
+            L.ss2_msssim_create_ex.argtypes = [i, i, i, i, i, i]
+            L.ss2_msssim_create_ex.restype = vp
+            L.ss2_msssim_planes.argtypes = [vp]
+            L.ss2_msssim_planes.restype = i
+            L.ss2_msssim_debug_pyramid_plane.argtypes = [vp, vp, vp, i, vp, vp]
+            L.ss2_msssim_debug_pyramid_plane.restype = i
             L.ss2_msssim_score.argtypes = [vp, vp, vp, i, vp, vp, vp]
             L.ss2_msssim_score.restype = i
             L.ss2_msssim_debug_pyramid.argtypes = [vp, vp, vp, vp, vp]
@@ -333,49 +339,63 @@ class Cambi(_Context):
 
 
 class MSSSIM(_Context):
-    """MS-SSIM of the luma plane for one frame geometry (ss2_msssim_create)."""
+    """MS-SSIM for one frame geometry (ss2_msssim_create_ex): of the luma
+    plane, and with enable_chroma=True of the Cb and Cr planes too."""
 
     _PREFIX = "ss2_msssim"
     KERNELS = ("k_msssim_level", "k_msssim_final")
 
     SCALES = 5
 
-    def __init__(self, width: int, height: int, bitdepth: int, chroma: int, batch: int = 0):
-        h = lib().ss2_msssim_create(width, height, bitdepth, chroma, batch)
+    def __init__(self, width: int, height: int, bitdepth: int, chroma: int, batch: int = 0,
+                 enable_chroma: bool = False):
+        h = lib().ss2_msssim_create_ex(width, height, bitdepth, chroma, batch,
+                                       1 if enable_chroma else 0)
         if not h:
             code, msg = last_error()
             raise SS2Error(code, msg)
         self._h = h
-        self.width, self.height = width, height
+        self.width, self.height, self.chroma = width, height, chroma
+        self.planes = int(lib().ss2_msssim_planes(h))
 
-    def _dims(self):
-        w, h, out = self.width, self.height, []
+    def _dims(self, plane: int = 0):
+        w, h = self.width, self.height
+        if plane:
+            sx, sy = {420: (1, 1), 422: (1, 0), 444: (0, 0)}[self.chroma]
+            w, h = (w + sx) >> sx, (h + sy) >> sy
+        out = []
         for _ in range(self.SCALES):
             out.append((w, h))
             w, h = (w + 1) // 2, (h + 1) // 2
         return out
 
     def score(self, ref, dis, stream=None, values: bool = False):
-        """Scores (n,), and with values=True also the per-scale means
-        (n, 5, 5): l, c, s, cs, l cs."""
+        """Scores (n,) for the luma plane alone, (n, 3) with the chroma planes
+        (Y, Cb, Cr); with values=True also the per-scale means (n, 5, 5) or
+        (n, 3, 5, 5): l, c, s, cs, l cs."""
         import torch
         for t in (ref, dis):
             if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
                 raise TypeError("frames must be contiguous CUDA tensors")
-        n = ref.shape[0]
-        out = np.zeros(n, np.float64)
-        v = np.zeros((n, self.SCALES, 5), np.float64) if values else None
+        n, p = ref.shape[0], self.planes
+        out = np.zeros((n, p), np.float64)
+        v = np.zeros((n, p, self.SCALES, 5), np.float64) if values else None
         _check(lib().ss2_msssim_score(self._h, ref.data_ptr(), dis.data_ptr(), n, out.ctypes.data,
                                       v.ctypes.data if values else None, _stream_handle(stream)))
+        if p == 1:
+            out = out[:, 0]
+            v = v[:, 0] if values else None
         return (out, v) if values else out
 
-    def pyramid(self, ref, dis, stream=None):
-        """Scales 2..5 of the first frame pair: ([ref planes], [dis planes])."""
-        dims = self._dims()[1:]
+    def pyramid(self, ref, dis, stream=None, plane: int = 0):
+        """Scales 2..5 of one plane of the first frame pair: ([ref planes],
+        [dis planes])."""
+        dims = self._dims(plane)[1:]
         total = sum(w * h for w, h in dims)
         buf = np.zeros(2 * total, np.float32)
-        _check(lib().ss2_msssim_debug_pyramid(self._h, ref.data_ptr(), dis.data_ptr(),
-                                              buf.ctypes.data, _stream_handle(stream)))
+        _check(lib().ss2_msssim_debug_pyramid_plane(self._h, ref.data_ptr(), dis.data_ptr(),
+                                                    plane, buf.ctypes.data,
+                                                    _stream_handle(stream)))
         out, off = [], 0
         for _ in range(2):
             planes = []

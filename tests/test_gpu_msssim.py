@@ -72,3 +72,61 @@ def test_msssim_refuses_small_frames(cuda):
     with pytest.raises(SS2Error) as e:
         MSSSIM(160, 400, 8, 444)
     assert e.value.code == -95
+
+
+# enable_chroma: odd sizes and every chroma layout (chroma planes of at least
+# 161 samples a side, so that their scale-5 planes hold the window)
+CHROMA_GEOMS = [
+    (704, 384, 8, 420), (401, 333, 10, 444), (660, 341, 8, 422), (1920, 1080, 10, 420),
+]
+
+
+@pytest.mark.parametrize("geom", CHROMA_GEOMS, ids=lambda g: "x".join(map(str, g)))
+def test_msssim_chroma_planes(cuda, geom):
+    """Per-plane scores and per-scale means of Y, Cb and Cr within 1e-6 of the
+    oracle, and the chroma pyramids bitwise; the luma results are those of a
+    luma-only context, bit for bit."""
+    import concurrent.futures as cf
+
+    import torch
+
+    from ssimulacra2_image_scoring_gb300 import MSSSIM
+    w, h, d, c = geom
+    wl = synth.custom(w, h, d, c, 3, seed=w + h, noise=4.0)
+    ref = torch.from_numpy(wl.ref).cuda()
+    dis = torch.from_numpy(wl.dis).cuda()
+    with MSSSIM(w, h, d, c, enable_chroma=True) as ms, MSSSIM(w, h, d, c) as luma:
+        assert ms.planes == 3
+        got, vals = ms.score(ref, dis, values=True)
+        only_y, only_v = luma.score(ref, dis, values=True)
+        pyr = [ms.pyramid(ref, dis, plane=p) for p in range(3)]
+    assert got.shape == (3, 3) and vals.shape == (3, 3, 5, 5)
+    assert np.array_equal(got[:, 0], only_y) and np.array_equal(vals[:, 0], only_v)
+    with cf.ThreadPoolExecutor(max_workers=3) as ex:   # ctypes releases the GIL
+        want = list(ex.map(lambda f: oracle.msssim_planes(wl.ref[f], wl.dis[f], w, h, d, c),
+                           range(3)))
+    for f, (s, v) in enumerate(want):
+        assert np.max(np.abs(got[f] - s)) <= TOL, (f, got[f], s)
+        assert np.max(np.abs(vals[f] - v)) <= TOL, (f, np.max(np.abs(vals[f] - v)))
+    # the chroma pyramids: a chroma plane scored as the luma of a frame of
+    # its size gives the oracle's levels
+    sx, sy = {420: (1, 1), 422: (1, 0), 444: (0, 0)}[c]
+    cw, ch = (w + sx) >> sx, (h + sy) >> sy
+    for p in (1, 2):
+        off = w * h + (p - 1) * cw * ch
+        for img, (frames, got_p) in enumerate(((wl.ref, pyr[p][0]), (wl.dis, pyr[p][1]))):
+            plane = np.ascontiguousarray(frames[0][off:off + cw * ch])
+            want_p = oracle.msssim_pyramid(plane, cw, ch, d)
+            for j in range(4):
+                assert np.array_equal(got_p[j].view(np.uint32),
+                                      want_p[j + 1].astype(np.float32).view(np.uint32)), (p, img, j)
+
+
+def test_msssim_chroma_refuses_small_chroma(cuda):
+    from ssimulacra2_image_scoring_gb300 import MSSSIM, SS2Error
+    # luma 200 x 200 holds the window at scale 5, its 4:2:0 chroma does not
+    with MSSSIM(200, 200, 8, 420):
+        pass
+    with pytest.raises(SS2Error) as e:
+        MSSSIM(200, 200, 8, 420, enable_chroma=True)
+    assert e.value.code == -95 and "Cb" in str(e.value)
