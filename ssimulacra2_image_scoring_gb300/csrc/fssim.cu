@@ -294,7 +294,9 @@ __global__ void __launch_bounds__(256)
     }
     // stage u & 1 read and the column sums complete; the other column buffer
     // was last read by the item before, which every thread finished before
-    // this barrier
+    // this barrier.  The stage's reads (generic proxy) are ordered before
+    // the bulk copy that refills it (async proxy) by a proxy fence.
+    fence_async_smem();
     __syncthreads();
     if (t == 0) issue(u + 2);
     if (grp == g.ng - 1) {
@@ -450,7 +452,10 @@ __global__ void __launch_bounds__(256)
     // One barrier per unit: the stage is read, this item's tails are written
     // (the other tail buffer was last read by the item before, finished
     // before this barrier), and every thread's wait agreed.  A failed wait
-    // leaves garbage sums behind and ends the kernel here.
+    // leaves garbage sums behind and ends the kernel here.  The stage's
+    // reads are ordered before the bulk copy that refills it (a proxy
+    // fence, then the barrier).
+    fence_async_smem();
     if (!__syncthreads_and(ok)) {
       if (t == 0) {
         atomicOr(err, kErrTmaTimeout);

@@ -325,8 +325,14 @@ __global__ void __launch_bounds__(kHWarps * 32)
       g1[p] = *reinterpret_cast<const float4 *>(&sm.in[sk][p][lane * kBoxCols + 4]);
       gn[p] = *reinterpret_cast<const float4 *>(&sm.in[sk1][p][lane * kBoxCols]);
     }
+    // slot k is free once every lane's reads of it are ordered before the
+    // copy that refills it: the reads are generic-proxy accesses and the
+    // copy writes through the async proxy, so a proxy fence precedes the
+    // warp barrier (without it a read still in flight under heavy
+    // shared-memory traffic could return the refilled data)
+    fence_async_smem();
     __syncwarp();
-    if (lane == 0 && k + kHSlots <= nchunk) issue(k + kHSlots);  // slot k is free
+    if (lane == 0 && k + kHSlots <= nchunk) issue(k + kHSlots);
     float o[kNq][kBoxCols];
     {
       // step producing Y[8k + j] takes x[8k + j + 4] + x[8k + j - 6]
@@ -562,6 +568,9 @@ __global__ void __launch_bounds__(kVWarps * 32)
         o[q] = res_step(r[q], px, __fadd_rn(ha[q * kVBox], hb[q * kVBox]));
       if (j == 5) {
         // chunk k - 1 is read for the last time: refill its slot with k + 2
+        // (the reads are ordered before the async-proxy refill by a proxy
+        // fence and the warp barrier)
+        fence_async_smem();
         __syncwarp();
         if (lane == 0 && k + 2 <= nchunk) issue_h(k + 2);
       }

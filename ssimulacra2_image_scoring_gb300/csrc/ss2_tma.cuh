@@ -108,8 +108,9 @@ __device__ __forceinline__ void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA) reads of them.
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses to the same memory: writes before a bulk store
+// reads them, and reads before a bulk load overwrites them.
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
