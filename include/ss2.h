@@ -135,6 +135,19 @@ int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis,
                      int scale, float *xyb, float *hblur, void *stream);
 
 /*
+ * ss2_debug_linear — runs the pyramid kernel on one frame pair (device
+ * pointers) and copies the linear RGB of one scale to host memory: the
+ * YUV -> linear RGB conversion at scale 0 (picture_to_linear_rgb), and the
+ * 2x2 downsample of linear RGB at scales 1-5 (downsample_2x2; Research-1363,
+ * "Sources" and Finding 2), which the kernel otherwise keeps on chip.
+ *   lin: HOST array of 6 planes ws*hs, packed: ref R, G, B then dis R, G, B.
+ * The device buffer for the planes is allocated and freed inside the call.
+ * Returns -EINVAL for a scale the geometry does not reach or a NULL output.
+ */
+int ss2_debug_linear(ss2_ctx *ctx, const void *ref, const void *dis, int scale,
+                     float *lin, void *stream);
+
+/*
  * ss2_debug_cbrt — applies the pipeline's correctly rounded cube root
  * (linear_rgb_to_xyb's cbrtf; Research-1363, Finding 2) to n floats.
  * x, y: DEVICE arrays of n floats (may alias).  Non-negative finite inputs

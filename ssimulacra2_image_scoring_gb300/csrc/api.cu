@@ -818,6 +818,28 @@ SS2_API int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis, int
   return check_err_word(ctx, st);
 }
 
+SS2_API int ss2_debug_linear(ss2_ctx *ctx, const void *ref, const void *dis, int scale,
+                             float *lin, void *stream) {
+  if (check_call(ctx, ref, dis, 1)) return t_err;
+  if (scale < 0 || scale >= ctx->g.nscales)
+    return fail(SS2_EINVAL, "scale %d is not computed for this geometry", scale);
+  if (!lin) return fail(SS2_EINVAL, "NULL output");
+  CU(cudaSetDevice(ctx->device), "cudaSetDevice");
+  cudaStream_t st = (cudaStream_t)stream;
+  const Geom &g = ctx->g;
+  const size_t n = (size_t)6 * g.ws[scale] * g.hs[scale];
+  float *d_lin = nullptr;
+  CU(cudaMalloc(&d_lin, n * sizeof(float)), "cudaMalloc");
+  cudaError_t e = launch_pyramid(g, ctx->px, ctx->tabs, (const uint8_t *)ref,
+                                 (const uint8_t *)dis, ctx->lane[0].X, 1, st, d_lin, scale);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(lin, d_lin, n * sizeof(float), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(d_lin);
+  if (e != cudaSuccess) return cuda_fail(e, "linear RGB read-back");
+  return 0;
+}
+
 SS2_API int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream) {
   if (n < 0 || (n > 0 && (!x || !y))) return fail(SS2_EINVAL, "bad cbrt arguments");
   int dev = 0;

@@ -19,6 +19,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <utility>
 
 #include "ss2_device.cuh"
 #include "ss2_tma.cuh"
@@ -28,21 +30,86 @@
 namespace ss2 {
 
 // ---------------------------------------------------------------------------
-// k_pyramid
+// k_pyramid: one 64x64 scale-0 tile of one frame pair per block.
+//
+// Scale 0 and 1.  Warp w takes the tile's row pairs w, w + 8, w + 16, w + 24;
+// lane l takes the 2x2 quad at tile columns 2l, 2l + 1 of the row pair.  The
+// row pair's samples (two luma rows and their chroma rows, both frames) are
+// staged in a per-warp shared-memory buffer: 16-byte asynchronous copies
+// when the geometry keeps every row start on 16 bytes, else sample by
+// sample.  The next row pair's copies are in flight while the current one is
+// computed (two buffers per warp).  Each thread converts its quad's four
+// pixels (YUV -> R'G'B' -> linear RGB -> XYB, stored two columns at a time),
+// averages the quad's linear RGB into the scale-1 pixel, forms that pixel's
+// XYB at once and keeps its linear RGB in shared memory: no barrier sits
+// between scale 0 and scale 1.
+//
+// Scales 2-5 are halved from the shared scale-1 tile (16x16, 8x8, 4x4, 2x2
+// pixels): one block barrier before scale 2, then scale 3 on two warps (a
+// named barrier) and scales 4-5 on one warp; the other warps leave.
+//
+// Only XYB reaches HBM; linear RGB never does (lin_dbg, when set, receives
+// the linear RGB of scale dbg_scale for the parity tests).
 // ---------------------------------------------------------------------------
 
-constexpr int kTile = 32;  // scale-0 tile edge; 32 = 2^5 keeps 5 halvings inside the tile
+constexpr int kPT = 64;  // scale-0 tile edge; 64 = 2^6 keeps 5 halvings inside the tile
 constexpr int kPyrThreads = 256;
-// shared-memory offset of the level-s tile inside each plane's region:
-// sum_{k<s} (32 >> k)^2 = (4096 - (4096 >> 2s)) / 3
-__host__ __device__ constexpr int lvl_off(int s) { return (4096 - (4096 >> (2 * s))) / 3; }
-constexpr int kLvlTotal = lvl_off(kMaxScales);
+constexpr int kPyrWarps = kPyrThreads / 32;
+constexpr int kPyrIters = kPT / 2 / kPyrWarps;  // row pairs per warp
+// shared-memory offset of the level-s tile (s >= 1) inside each plane's
+// region: sum_{k=1}^{s-1} (64 >> k)^2 = (4096 - (4096 >> 2(s-1))) / 3
+__host__ __device__ constexpr int lvl_off(int s) { return (4096 - (4096 >> (2 * (s - 1)))) / 3; }
+constexpr int kLvlTotal = lvl_off(kMaxScales);  // 1364 floats per plane
 
-// One sample of BPS bytes (8-bit, or 16-bit little-endian words) at index i.
+// Staging geometry of one launch.
+struct PyrStage {
+  int ybytes;     // one staged luma row: 64 samples
+  int cbytes;     // one staged chroma row: 64 >> sx samples
+  int crows;      // chroma rows per luma row pair: 1 (4:2:0) or 2
+  int img_bytes;  // one frame's rows: 2 ybytes + 2 crows cbytes (a multiple of 16)
+  int vec;        // 1: 16-byte copies (every staged row starts on 16 bytes)
+  int dbg_scale;  // scale whose linear RGB is written to lin_dbg, or -1
+};
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Source of byte `off` of one frame's staged rows for the row pair starting
+// at luma row r0 (layout: luma row r0, luma row r0 + 1, the U rows, the V
+// rows), and whether that byte lies inside the frame.
+__device__ __forceinline__ const uint8_t *stage_src(const Geom &g, const PyrStage &ps,
+                                                    const uint8_t *f, int tx0, int r0, int off,
+                                                    int bps, bool &ok) {
+  if (off < 2 * ps.ybytes) {
+    const int r = off >= ps.ybytes;
+    const int col = off - (r ? ps.ybytes : 0);
+    const int y = r0 + r;
+    ok = y < g.h && tx0 * bps + col < g.w * bps;
+    return f + (y * g.w + tx0) * bps + col;
+  }
+  off -= 2 * ps.ybytes;
+  const int plane = off >= ps.crows * ps.cbytes;
+  off -= plane ? ps.crows * ps.cbytes : 0;
+  const int r = off >= ps.cbytes;  // 0 when there is one chroma row
+  const int col = off - (r ? ps.cbytes : 0);
+  const int cy = (r0 >> g.sy) + r, cx0 = tx0 >> g.sx;
+  ok = cy < g.ch && cx0 * bps + col < g.cw * bps;
+  return f + (g.w * g.h + plane * g.cw * g.ch + cy * g.cw + cx0) * bps + col;
+}
+
 template <int BPS>
-__device__ __forceinline__ int read_sample(const uint8_t *__restrict__ p, int i) {
-  if (BPS == 1) return p[i];
-  return reinterpret_cast<const uint16_t *>(p)[i];
+__device__ __forceinline__ int stage_sample(const unsigned char *p) {
+  if (BPS == 1) return *p;
+  return *reinterpret_cast<const uint16_t *>(p);
 }
 
 // Index arithmetic is 32-bit inside a frame: a plane holds at most
@@ -50,18 +117,59 @@ __device__ __forceinline__ int read_sample(const uint8_t *__restrict__ p, int i)
 // 2 x 1.5 x 2^28; each scale's XYB block is reached from a 64-bit base and
 // its six planes lie within 6 x 2^28 floats of it.
 template <int BPS>
-__global__ void __launch_bounds__(kPyrThreads)
-    k_pyramid(Geom g, Pix px, PyrTabs tabs, const uint8_t *__restrict__ ref,
-              const uint8_t *__restrict__ dis, float *__restrict__ X) {
-  __shared__ float L[6][kLvlTotal];
-  __shared__ float cb_s[3];
-  // 8-bit samples: the two normalisation tables in shared memory
-  __shared__ float ntab[BPS == 1 ? 512 : 1];
+__global__ void __launch_bounds__(kPyrThreads, 4)
+    k_pyramid(Geom g, Pix px, PyrTabs tabs, PyrStage ps, const uint8_t *__restrict__ ref,
+              const uint8_t *__restrict__ dis, float *__restrict__ X,
+              float *__restrict__ lin_dbg) {
+  extern __shared__ __align__(16) unsigned char psm[];
+  float(*L)[kLvlTotal] = reinterpret_cast<float(*)[kLvlTotal]>(psm);
+  float *ntab = reinterpret_cast<float *>(psm + sizeof(float) * 6 * kLvlTotal);
+  float *cb_s = ntab + (BPS == 1 ? 512 : 0);
+  unsigned char *stage = reinterpret_cast<unsigned char *>(cb_s + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int frame = blockIdx.z;
-  const int tx0 = blockIdx.x * kTile, ty0 = blockIdx.y * kTile;
+  const int tx0 = blockIdx.x * kPT, ty0 = blockIdx.y * kPT;
   float *Xf = X + (long long)frame * g.x_fs;
+  const uint8_t *fref = ref + (long long)frame * g.frame_bytes;
+  const uint8_t *fdis = dis + (long long)frame * g.frame_bytes;
+  const int buf_bytes = 2 * ps.img_bytes;
+  unsigned char *wst = stage + warp * 2 * buf_bytes;  // this warp's two buffers
 
-  // cbrt(bias_i), once per block
+  // row pair i of this warp -> buffer i & 1 (vec: one copy group per row pair)
+  auto stage_rows = [&](int i) {
+    const int r0 = ty0 + 2 * (warp + kPyrWarps * i);
+    unsigned char *dst = wst + (i & 1) * buf_bytes;
+    if (ps.vec) {
+      if (r0 < g.h) {
+        for (int c = lane; c < (buf_bytes >> 4); c += 32) {
+          int off = c << 4;
+          const int img = off >= ps.img_bytes;
+          off -= img ? ps.img_bytes : 0;
+          bool ok;
+          const uint8_t *src = stage_src(g, ps, img ? fdis : fref, tx0, r0, off, BPS, ok);
+          if (ok) cp_async16(dst + (c << 4), src);
+        }
+      }
+      cp_async_commit();  // possibly empty: keeps one group per row pair
+    } else if (r0 < g.h) {
+      for (int e = lane; e < buf_bytes / BPS; e += 32) {
+        int off = e * BPS;
+        const int img = off >= ps.img_bytes;
+        off -= img ? ps.img_bytes : 0;
+        bool ok;
+        const uint8_t *src = stage_src(g, ps, img ? fdis : fref, tx0, r0, off, BPS, ok);
+        if (ok) {
+          if (BPS == 1)
+            dst[e] = __ldg(src);
+          else
+            reinterpret_cast<uint16_t *>(dst)[e] = __ldg(reinterpret_cast<const uint16_t *>(src));
+        }
+      }
+    }
+  };
+  stage_rows(0);
+
+  // cbrt(bias_i) and the 8-bit normalisation tables, once per block
   if (threadIdx.x < 3) cb_s[threadIdx.x] = cbrt_cr(px.bias[threadIdx.x]);
   if (BPS == 1 && tabs.ynorm) {
     for (int i = threadIdx.x; i < 256; i += kPyrThreads) {
@@ -74,104 +182,187 @@ __global__ void __launch_bounds__(kPyrThreads)
 #pragma unroll
   for (int i = 0; i < 3; ++i) cb[i] = cb_s[i];
 
-  // ---- scale 0: unpack, matrix, EOTF, XYB ----
-  {
-    const uint8_t *frames[2] = {ref + (long long)frame * g.frame_bytes,
-                                dis + (long long)frame * g.frame_bytes};
-    const int k = 1 << (g.depth - 8);
-    const float dy = (float)(219 * k), dc = (float)(224 * k);
-    const int ysz = g.w * g.h, csz = g.cw * g.ch;
-    float *P0 = Xf + g.xoff[0];
-    const int plane0 = (int)g.plane[0], pitch0 = g.pitch[0];
-    for (int p = threadIdx.x; p < kTile * kTile; p += kPyrThreads) {
-      const int lx = p & (kTile - 1), ly = p / kTile;
-      const int x = tx0 + lx, y = ty0 + ly;
-      if (x >= g.w || y >= g.h) {
-#pragma unroll
-        for (int c = 0; c < 6; ++c) L[c][p] = 0.0f;
-        continue;
-      }
-      const int yi = y * g.w + x;
-      const int ci = (y >> g.sy) * g.cw + (x >> g.sx);
-      float *P = P0 + (y * pitch0 + x);
+  const int k = 1 << (g.depth - 8);
+  const float dy = (float)(219 * k), dc = (float)(224 * k);
+  const bool two_scales = g.nscales > 1;
+  float *P0 = Xf + g.xoff[0];
+  float *P1 = Xf + g.xoff[1];
+  const int plane0 = (int)g.plane[0], pitch0 = g.pitch[0];
+  const int plane1 = (int)g.plane[1], pitch1 = g.pitch[1];
+  const int lx0 = 2 * lane;                             // the quad's tile columns
+  const int lx1 = min(lx0 + 1, g.w - 1 - tx0);          // clamped at an odd right edge
+  const bool has_x1 = tx0 + lx0 + 1 < g.w;
+
+  // ---- scales 0 and 1 ----
+  for (int i = 0; i < kPyrIters; ++i) {
+    if (i + 1 < kPyrIters) stage_rows(i + 1);
+    if (ps.vec) {
+      if (i + 1 < kPyrIters)
+        cp_async_wait<1>();
+      else
+        cp_async_wait<0>();
+    }
+    __syncwarp();
+    const int rp = warp + kPyrWarps * i;
+    const int y0 = ty0 + 2 * rp;
+    if (y0 < g.h && tx0 + lx0 < g.w) {
+      const bool has_y1 = y0 + 1 < g.h;
+      const unsigned char *sb = wst + (i & 1) * buf_bytes;
+      float lin1[6];
 #pragma unroll
       for (int img = 0; img < 2; ++img) {
-        const uint8_t *f = frames[img];
-        const int Ys = read_sample<BPS>(f, yi);
-        const int Us = read_sample<BPS>(f, ysz + ci);
-        const int Vs = read_sample<BPS>(f, ysz + csz + ci);
-        float yn, cbv, crv;
-        if (BPS == 1 && tabs.ynorm) {
-          yn = ntab[Ys];
-          cbv = ntab[256 + Us];
-          crv = ntab[256 + Vs];
-        } else if (tabs.ynorm) {
-          yn = __ldg(tabs.ynorm + Ys);
-          cbv = __ldg(tabs.cnorm + Us);
-          crv = __ldg(tabs.cnorm + Vs);
-        } else {
-          yn = __fdiv_rn((float)(Ys - 16 * k), dy);
-          cbv = __fdiv_rn((float)(Us - 128 * k), dc);
-          crv = __fdiv_rn((float)(Vs - 128 * k), dc);
+        const unsigned char *sY = sb + img * ps.img_bytes;
+        const unsigned char *sU = sY + 2 * ps.ybytes;
+        const unsigned char *sV = sU + ps.crows * ps.cbytes;
+        float acc[3];
+#pragma unroll 1
+        for (int dyy = 0; dyy < 2; ++dyy) {
+          const int rr = dyy && has_y1 ? 1 : 0;  // clamped at an odd bottom edge
+          const int crr = ps.crows == 2 ? rr : 0;
+          float o[2][3];
+#pragma unroll
+          for (int dxx = 0; dxx < 2; ++dxx) {
+            const int lx = dxx ? lx1 : lx0;
+            const int Ys = stage_sample<BPS>(sY + rr * ps.ybytes + lx * BPS);
+            const int cofs = crr * ps.cbytes + (lx >> g.sx) * BPS;
+            const int Us = stage_sample<BPS>(sU + cofs);
+            const int Vs = stage_sample<BPS>(sV + cofs);
+            float yn, cbv, crv;
+            if (BPS == 1 && tabs.ynorm) {
+              yn = ntab[Ys];
+              cbv = ntab[256 + Us];
+              crv = ntab[256 + Vs];
+            } else if (tabs.ynorm) {
+              yn = __ldg(tabs.ynorm + Ys);
+              cbv = __ldg(tabs.cnorm + Us);
+              crv = __ldg(tabs.cnorm + Vs);
+            } else {
+              yn = __fdiv_rn((float)(Ys - 16 * k), dy);
+              cbv = __fdiv_rn((float)(Us - 128 * k), dc);
+              crv = __fdiv_rn((float)(Vs - 128 * k), dc);
+            }
+            const float r = __fmaf_rn(px.yuv[0], crv, yn);
+            const float gg = __fmaf_rn(-px.yuv[2], crv, __fmaf_rn(-px.yuv[1], cbv, yn));
+            const float b = __fmaf_rn(px.yuv[3], cbv, yn);
+            const float R = eotf_lookup(tabs.eotf, clamp01(r));
+            const float G = eotf_lookup(tabs.eotf, clamp01(gg));
+            const float B = eotf_lookup(tabs.eotf, clamp01(b));
+            // the 2x2 mean in the order ((p00 + p01) + p10) + p11
+            if (dyy == 0 && dxx == 0) {
+              acc[0] = R;
+              acc[1] = G;
+              acc[2] = B;
+            } else {
+              acc[0] = __fadd_rn(acc[0], R);
+              acc[1] = __fadd_rn(acc[1], G);
+              acc[2] = __fadd_rn(acc[2], B);
+            }
+            if (lin_dbg && ps.dbg_scale == 0 && (dyy == 0 || has_y1) && (dxx == 0 || has_x1)) {
+              const long long q = (long long)(y0 + dyy) * g.w + tx0 + lx;
+              const long long n0 = (long long)g.w * g.h;
+              lin_dbg[(3 * img + 0) * n0 + q] = R;
+              lin_dbg[(3 * img + 1) * n0 + q] = G;
+              lin_dbg[(3 * img + 2) * n0 + q] = B;
+            }
+            pixel_xyb(px, cb, R, G, B, o[dxx][0], o[dxx][1], o[dxx][2]);
+          }
+          if (dyy == 0 || has_y1) {
+            float *P = P0 + ((y0 + dyy) * pitch0 + tx0 + lx0);
+#pragma unroll
+            for (int c = 0; c < 3; ++c) {
+              float *q = P + (3 * img + c) * plane0;
+              if (has_x1)
+                *reinterpret_cast<float2 *>(q) = make_float2(o[0][c], o[1][c]);
+              else
+                *q = o[0][c];
+            }
+          }
         }
-        const float r = __fmaf_rn(px.yuv[0], crv, yn);
-        const float gg = __fmaf_rn(-px.yuv[2], crv, __fmaf_rn(-px.yuv[1], cbv, yn));
-        const float b = __fmaf_rn(px.yuv[3], cbv, yn);
-        const float R = eotf_lookup(tabs.eotf, clamp01(r));
-        const float G = eotf_lookup(tabs.eotf, clamp01(gg));
-        const float B = eotf_lookup(tabs.eotf, clamp01(b));
-        L[3 * img + 0][p] = R;
-        L[3 * img + 1][p] = G;
-        L[3 * img + 2][p] = B;
-        float xo, yo, bo;
-        pixel_xyb(px, cb, R, G, B, xo, yo, bo);
-        P[(3 * img + 0) * plane0] = xo;
-        P[(3 * img + 1) * plane0] = yo;
-        P[(3 * img + 2) * plane0] = bo;
+#pragma unroll
+        for (int c = 0; c < 3; ++c) lin1[3 * img + c] = __fmul_rn(acc[c], 0.25f);
+      }
+      if (two_scales) {
+        const int x = (tx0 >> 1) + lane, y = (ty0 >> 1) + rp;
+        float *P = P1 + (y * pitch1 + x);
+#pragma unroll
+        for (int img = 0; img < 2; ++img) {
+          float xo, yo, bo;
+          pixel_xyb(px, cb, lin1[3 * img], lin1[3 * img + 1], lin1[3 * img + 2], xo, yo, bo);
+          P[(3 * img + 0) * plane1] = xo;
+          P[(3 * img + 1) * plane1] = yo;
+          P[(3 * img + 2) * plane1] = bo;
+        }
+#pragma unroll
+        for (int c = 0; c < 6; ++c) L[c][rp * 32 + lane] = lin1[c];
+        if (lin_dbg && ps.dbg_scale == 1) {
+          const long long n1 = (long long)g.ws[1] * g.hs[1];
+          const long long q = (long long)y * g.ws[1] + x;
+#pragma unroll
+          for (int c = 0; c < 6; ++c) lin_dbg[c * n1 + q] = lin1[c];
+        }
       }
     }
+    __syncwarp();  // buffer i & 1 is refilled by stage_rows(i + 2)
   }
+  if (g.nscales <= 2) return;
   __syncthreads();
 
-  // ---- scales 1..: downsample linear RGB inside the tile, then XYB ----
-  for (int s = 1; s < g.nscales; ++s) {
-    const int lw = 5 - s;                               // log2 of the tile edge at scale s
+  // ---- scales 2..: halve the shared tile, then XYB ----
+  for (int s = 2; s < g.nscales; ++s) {
+    if (s == 3 && warp >= 2) return;  // 64 pixels: warps 0-1
+    if (s == 4 && warp >= 1) return;  // 16 and 4 pixels: warp 0
+    const int lw = 6 - s;             // log2 of the tile edge at scale s
     const int tw = 1 << lw;
-    const int ox = tx0 >> s, oy = ty0 >> s;            // tile origin at scale s
+    const int ox = tx0 >> s, oy = ty0 >> s;               // tile origin at scale s
     const int pox = tx0 >> (s - 1), poy = ty0 >> (s - 1);  // at scale s-1
     const int pw = 2 * tw;
     const int ww = g.ws[s - 1], hh = g.hs[s - 1];
     float *Ps = Xf + g.xoff[s];
     const int planes = (int)g.plane[s], pitchs = g.pitch[s];
-    for (int p = threadIdx.x; p < tw * tw; p += kPyrThreads) {
+    const int p = threadIdx.x;
+    if (p < tw * tw) {
       const int lx = p & (tw - 1), ly = p >> lw;
       const int x = ox + lx, y = oy + ly;
-      if (x >= g.ws[s] || y >= g.hs[s]) continue;
-      const int x0 = 2 * x, x1 = min(2 * x + 1, ww - 1);
-      const int y0 = 2 * y, y1 = min(2 * y + 1, hh - 1);
-      const int i00 = (y0 - poy) * pw + (x0 - pox), i01 = (y0 - poy) * pw + (x1 - pox);
-      const int i10 = (y1 - poy) * pw + (x0 - pox), i11 = (y1 - poy) * pw + (x1 - pox);
-      float v[6];
+      if (x < g.ws[s] && y < g.hs[s]) {
+        const int x0 = 2 * x, x1 = min(2 * x + 1, ww - 1);
+        const int y0 = 2 * y, y1 = min(2 * y + 1, hh - 1);
+        const int i00 = (y0 - poy) * pw + (x0 - pox), i01 = (y0 - poy) * pw + (x1 - pox);
+        const int i10 = (y1 - poy) * pw + (x0 - pox), i11 = (y1 - poy) * pw + (x1 - pox);
+        float v[6];
 #pragma unroll
-      for (int c = 0; c < 6; ++c) {
-        const float *Lp = &L[c][lvl_off(s - 1)];
-        float t = __fadd_rn(Lp[i00], Lp[i01]);
-        t = __fadd_rn(t, Lp[i10]);
-        t = __fadd_rn(t, Lp[i11]);
-        v[c] = __fmul_rn(t, 0.25f);
-        L[c][lvl_off(s) + p] = v[c];
-      }
-      float *P = Ps + (y * pitchs + x);
+        for (int c = 0; c < 6; ++c) {
+          const float *Lp = &L[c][lvl_off(s - 1)];
+          float t = __fadd_rn(Lp[i00], Lp[i01]);
+          t = __fadd_rn(t, Lp[i10]);
+          t = __fadd_rn(t, Lp[i11]);
+          v[c] = __fmul_rn(t, 0.25f);
+          L[c][lvl_off(s) + p] = v[c];
+        }
+        float *P = Ps + (y * pitchs + x);
 #pragma unroll
-      for (int img = 0; img < 2; ++img) {
-        float xo, yo, bo;
-        pixel_xyb(px, cb, v[3 * img], v[3 * img + 1], v[3 * img + 2], xo, yo, bo);
-        P[(3 * img + 0) * planes] = xo;
-        P[(3 * img + 1) * planes] = yo;
-        P[(3 * img + 2) * planes] = bo;
+        for (int img = 0; img < 2; ++img) {
+          float xo, yo, bo;
+          pixel_xyb(px, cb, v[3 * img], v[3 * img + 1], v[3 * img + 2], xo, yo, bo);
+          P[(3 * img + 0) * planes] = xo;
+          P[(3 * img + 1) * planes] = yo;
+          P[(3 * img + 2) * planes] = bo;
+        }
+        if (lin_dbg && ps.dbg_scale == s) {
+          const long long ns = (long long)g.ws[s] * g.hs[s];
+          const long long q = (long long)y * g.ws[s] + x;
+#pragma unroll
+          for (int c = 0; c < 6; ++c) lin_dbg[c * ns + q] = v[c];
+        }
       }
     }
-    __syncthreads();
+    if (s + 1 < g.nscales) {
+      if (s == 2)
+        __syncthreads();
+      else if (s == 3)
+        asm volatile("bar.sync 1, 64;" ::: "memory");  // warps 0 and 1
+      else
+        __syncwarp();
+    }
   }
 }
 
@@ -394,8 +585,13 @@ struct Acc6 {
   ff v[kNSum];
 };
 
+// Every sum and every term here is non-negative (d, d^4, |r|, r^4 and their
+// running sums), so the exact error of hi + hi comes from Dekker's
+// quick_two_sum on (max, min): the same two words as Knuth's two_sum, one
+// instruction fewer.
 __device__ __forceinline__ ff acc_add(ff s, ff t) {
-  const ff h = two_sum(s.hi, t.hi);
+  const float a = fmaxf(s.hi, t.hi), b = fminf(s.hi, t.hi);
+  const ff h = quick_two_sum(a, b);
   return {h.hi, __fadd_rn(s.lo, __fadd_rn(h.lo, t.lo))};
 }
 
@@ -418,8 +614,13 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
   // float-pair part: d = max(1 - num_m num_s / den_s, 0), formed as
   // (den_s - num_m num_s) / den_s with the product exact as a pair and the
   // numerator's leading difference exact (two_sum)
+  // den_s - p.hi exactly: quick_two_sum on (max, min) is exact whenever the
+  // larger operand has the larger magnitude, which holds for every outcome
+  // that survives the clamp below (den_s > 0: either -p.hi >= 0, or
+  // -p.hi < 0 with |p.hi| <= den_s, else the difference is negative and d
+  // is clamped to zero)
   const ff p = two_prod(num_m, num_s);
-  const ff nd = two_sum(den_s, -p.hi);
+  const ff nd = quick_two_sum(fmaxf(den_s, -p.hi), fminf(den_s, -p.hi));
   ff d = ff_div_f(quick_two_sum(nd.hi, __fsub_rn(nd.lo, p.lo)), den_s);
   if (!(d.hi > 0.0f)) d = {0.0f, 0.0f};
   const ff d2 = ff_sqr_lazy(d);
@@ -430,7 +631,8 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
   // a = |x - mu|; the numerator and denominator are exact pairs
   const float a2 = fabsf(__fsub_rn(x2, mu2));
   const float a1 = fabsf(__fsub_rn(x1, mu1));
-  const ff r = ff_div(two_sum(a2, -a1), two_sum(1.0f, a1));
+  // 1 + a1 with a1 >= 0: quick_two_sum on (max, min) is exact
+  const ff r = ff_div(two_sum(a2, -a1), quick_two_sum(fmaxf(1.0f, a1), fminf(1.0f, a1)));
   const ff r2 = ff_sqr_lazy(r);
   const ff r4 = ff_sqr_lazy(r2);
   // artifact (r > 0) and detail lost (r < 0) are exclusive: one addition each
@@ -607,14 +809,22 @@ __global__ void __launch_bounds__(kVWarps * 32)
 // warp partials of its (scale, channel, sum) in index order, then forms the
 // 1-norm (mean) or 4-norm (fourth root of the mean fourth power) in fp64.
 // Thread 0 pools: P = sum_i w_i |v_i| in index order, then the map.
+// With an error word given and set, the batch's values and scores are NaN.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(128)
     k_finalize(Geom g, const float2 *__restrict__ part, const double *__restrict__ params,
-               double *__restrict__ values, double *__restrict__ scores) {
+               double *__restrict__ values, double *__restrict__ scores,
+               const int *__restrict__ err) {
   __shared__ double v[kNValues];
   const int frame = blockIdx.x;
   const int j = threadIdx.x;
+  if (err && *err != 0) {
+    const double nan = __longlong_as_double(0x7ff8000000000000LL);
+    if (j < kNValues) values[(long long)frame * kNValues + j] = nan;
+    if (j == 0) scores[frame] = nan;
+    return;
+  }
   if (j < kNValues) {
     const int kind = j % 3, n = (j / 3) % 2, s = (j / 6) % 6, c = j / 36;
     double out = 0.0;
@@ -705,12 +915,41 @@ cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st) 
 }
 
 cudaError_t launch_pyramid(const Geom &g, const Pix &px, const PyrTabs &tabs, const uint8_t *ref,
-                           const uint8_t *dis, float *X, int nframes, cudaStream_t st) {
-  dim3 grid((g.w + kTile - 1) / kTile, (g.h + kTile - 1) / kTile, nframes);
+                           const uint8_t *dis, float *X, int nframes, cudaStream_t st,
+                           float *lin_dbg, int dbg_scale) {
+  PyrStage ps;
+  ps.ybytes = kPT * g.bps;
+  ps.cbytes = (kPT >> g.sx) * g.bps;
+  ps.crows = g.sy ? 1 : 2;
+  ps.img_bytes = 2 * ps.ybytes + 2 * ps.crows * ps.cbytes;
+  // every staged row starts on 16 bytes: frame bases, plane offsets and row
+  // pitches of both planes, and the tile origins (multiples of 64 samples)
+  ps.vec = (reinterpret_cast<uintptr_t>(ref) % 16 == 0) &&
+           (reinterpret_cast<uintptr_t>(dis) % 16 == 0) && g.frame_bytes % 16 == 0 &&
+           (g.w * g.bps) % 16 == 0 && (g.cw * g.bps) % 16 == 0;
+  ps.dbg_scale = lin_dbg ? dbg_scale : -1;
+  const int smem = (int)sizeof(float) * (6 * kLvlTotal + (g.bps == 1 ? 512 : 0) + 4) +
+                   kPyrWarps * 2 * 2 * ps.img_bytes;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::atomic<bool> configured[64];
+  if (dev < 64 && !configured[dev].load()) {
+    e = cudaFuncSetAttribute(k_pyramid<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(float) * (6 * kLvlTotal + 512 + 4) +
+                                 kPyrWarps * 2 * 2 * (2 * kPT + 2 * 2 * kPT));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_pyramid<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(float) * (6 * kLvlTotal + 4) +
+                                   kPyrWarps * 2 * 2 * 2 * (2 * kPT + 2 * 2 * kPT));
+    if (e != cudaSuccess) return e;
+    configured[dev].store(true);
+  }
+  dim3 grid((g.w + kPT - 1) / kPT, (g.h + kPT - 1) / kPT, nframes);
   if (g.bps == 1)
-    k_pyramid<1><<<grid, kPyrThreads, 0, st>>>(g, px, tabs, ref, dis, X);
+    k_pyramid<1><<<grid, kPyrThreads, smem, st>>>(g, px, tabs, ps, ref, dis, X, lin_dbg);
   else
-    k_pyramid<2><<<grid, kPyrThreads, 0, st>>>(g, px, tabs, ref, dis, X);
+    k_pyramid<2><<<grid, kPyrThreads, smem, st>>>(g, px, tabs, ps, ref, dis, X, lin_dbg);
   return cudaGetLastError();
 }
 
@@ -719,11 +958,11 @@ cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool configured[64] = {};
-  if (dev < 64 && !configured[dev]) {
+  static std::atomic<bool> configured[64];
+  if (dev < 64 && !configured[dev].load()) {
     e = cudaFuncSetAttribute(k_hblur, cudaFuncAttributeMaxDynamicSharedMemorySize, kHSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true);
   }
   const int units = g.hunit_off[g.nscales];
   const dim3 grid((units * nframes + kHWarps - 1) / kHWarps);
@@ -736,11 +975,11 @@ cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, co
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool configured[64] = {};
-  if (dev < 64 && !configured[dev]) {
+  static std::atomic<bool> configured[64];
+  if (dev < 64 && !configured[dev].load()) {
     e = cudaFuncSetAttribute(k_vblur, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true);
   }
   const int warps = g.vwarp_off[g.nscales];
   const dim3 grid((warps * nframes + kVWarps - 1) / kVWarps);
@@ -752,14 +991,15 @@ cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, co
 // then take the next free SM slots ahead of the other lane's pending blocks,
 // and the lane's stream moves on to its next batch sooner.
 cudaError_t launch_finalize(const Geom &g, const float2 *part, const double *params,
-                            double *values, double *scores, int nframes, cudaStream_t st) {
-  static int greatest = 1;   // numerically lowest priority value; 1 = not yet read
-  if (greatest == 1) {
+                            double *values, double *scores, int nframes, cudaStream_t st,
+                            const int *err) {
+  // numerically lowest priority value, read once (thread-safe initialisation)
+  static const std::pair<cudaError_t, int> greatest = [] {
     int least = 0, hi = 0;
     const cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &hi);
-    if (e != cudaSuccess) return e;
-    greatest = hi;
-  }
+    return std::make_pair(e, hi);
+  }();
+  if (greatest.first != cudaSuccess) return greatest.first;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nframes);
   cfg.blockDim = dim3(128);
@@ -767,10 +1007,10 @@ cudaError_t launch_finalize(const Geom &g, const float2 *part, const double *par
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributePriority;
-  attr[0].val.priority = greatest;
+  attr[0].val.priority = greatest.second;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_finalize, g, part, params, values, scores);
+  return cudaLaunchKernelEx(&cfg, k_finalize, g, part, params, values, scores, err);
 }
 
 }  // namespace ss2

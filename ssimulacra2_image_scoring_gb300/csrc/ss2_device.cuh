@@ -60,8 +60,8 @@ __device__ __forceinline__ ff ff_mul(ff a, ff b) {
 }
 
 // a^2 as a pair without the final renormalisation: hi = fl(a.hi^2) and lo
-// gathers that product's exact error and 2 a.hi a.lo in one rounding (a.lo^2,
-// below 2^-46 a^2, is dropped).  If |a.lo| <= e |a.hi| then |lo| <= (2^-24 +
+// gathers that product's exact error and 2 a.hi a.lo in one fused rounding
+// (a.lo^2, below 2^-46 a^2, is dropped).  If |a.lo| <= e |a.hi| then |lo| <= (2^-24 +
 // 2.01 e) |hi|: from a quotient pair (e = 2^-23) the low word stays below
 // 2^-20 |hi| after the two squarings of a fourth power, and each squaring
 // adds about 2^-45 relative error.  The pair can be squared again or added
@@ -69,8 +69,7 @@ __device__ __forceinline__ ff ff_mul(ff a, ff b) {
 // instructions of quick_two_sum.
 __device__ __forceinline__ ff ff_sqr_lazy(ff a) {
   const ff p = two_prod(a.hi, a.hi);
-  const float c = __fmul_rn(__fadd_rn(a.hi, a.hi), a.lo);
-  return {p.hi, __fadd_rn(p.lo, c)};
+  return {p.hi, __fmaf_rn(__fadd_rn(a.hi, a.hi), a.lo, p.lo)};
 }
 
 // Approximate reciprocal (relative error near 2^-23).  The .ftz form: every

@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
             L.ss2_values.restype = i
             L.ss2_debug_planes.argtypes = [vp, vp, vp, i, vp, vp, vp]
             L.ss2_debug_planes.restype = i
+            L.ss2_debug_linear.argtypes = [vp, vp, vp, i, vp, vp]
+            L.ss2_debug_linear.restype = i
             L.ss2_debug_cbrt.argtypes = [vp, vp, ctypes.c_longlong, vp]
             L.ss2_debug_cbrt.restype = i
             L.ss2_profile_begin.argtypes = [vp]
@@ -516,5 +518,16 @@ class Scorer(_Context):
         _check(lib().ss2_debug_planes(self.handle, ref.data_ptr(), dis.data_ptr(), scale,
                                       xyb.ctypes.data, hb.ctypes.data, _stream_handle(stream)))
         return xyb, hb
+
+    def debug_linear(self, ref, dis, scale: int, stream=None):
+        """Linear RGB planes (6, hs, ws) of one scale for the first frame pair,
+        as the pyramid kernel forms them (ref R, G, B then dis R, G, B)."""
+        ws, hs = self.width, self.height
+        for _ in range(scale):
+            ws, hs = (ws + 1) // 2, (hs + 1) // 2
+        lin = np.zeros((6, hs, ws), np.float32)
+        _check(lib().ss2_debug_linear(self.handle, ref.data_ptr(), dis.data_ptr(), scale,
+                                      lin.ctypes.data, _stream_handle(stream)))
+        return lin
 
 

@@ -7,7 +7,7 @@ Findings 2 and 4):
   - the 108 pooled values: relative 1e-9 (double-float sums in a fixed tree
     against the oracle's sequential fp64 sums; the page measured ~1e-12 on
     the score);
-  - scores: |d| <= 1e-6 per frame.
+  - scores: |d| <= 1e-6 per frame, on every frame of the five workloads.
 """
 from __future__ import annotations
 
@@ -62,13 +62,20 @@ def _check_values(got_v, want_v):
 
 
 GEOMS = [
-    # (w, h, depth, chroma): ragged tails, odd sizes, every chroma layout
+    # (w, h, depth, chroma): ragged tails, odd sizes, every chroma layout.
+    # Rows whose starts all fall on 16 bytes take the pyramid kernel's
+    # 16-byte staging copies (64x48, 224x100, 224x101, 96x70, 80x72); the
+    # others take its sample-by-sample staging.
     (64, 48, 8, 420),
     (853, 481, 8, 444),
     (17, 13, 10, 444),
     (130, 66, 9, 422),
     (200, 97, 11, 420),
     (8, 8, 8, 444),
+    (224, 100, 8, 420),
+    (224, 101, 10, 420),
+    (96, 70, 12, 422),
+    (80, 72, 8, 444),
 ]
 
 
@@ -86,6 +93,22 @@ def test_planes_bitwise(cuda, geom):
                 f"XYB differs at scale {s}"
             assert np.array_equal(hb.view(np.uint32), dump["hblur"].view(np.uint32)), \
                 f"horizontal blur differs at scale {s}"
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: "x".join(map(str, g)))
+def test_linear_pyramid_bitwise(cuda, geom):
+    """Linear RGB at scale 0 and the 2x2-downsampled linear RGB of scales 1-5
+    (which the pyramid kernel keeps on chip) bitwise against the oracle's."""
+    w, h, d, c = geom
+    wl = synth.custom(w, h, d, c, 1, seed=13)
+    ref, dis = _to_dev(wl.ref), _to_dev(wl.dis)
+    dims = oracle.scale_dims(w, h)
+    with _scorer(wl.spec) as sc:
+        for s in range(len(dims)):
+            lin = sc.debug_linear(ref, dis, s)
+            _, _, dump = oracle.score(wl.ref[0], wl.dis[0], w, h, d, c, dump_scale=s)
+            assert np.array_equal(lin.view(np.uint32), dump["lin"].view(np.uint32)), \
+                f"linear RGB differs at scale {s}"
 
 
 @pytest.mark.parametrize("geom", GEOMS, ids=lambda g: "x".join(map(str, g)))
@@ -160,9 +183,13 @@ def test_determinism_and_batch_invariance(cuda):
     assert np.array_equal(s1, s3) and np.array_equal(v1, v3)
 
 
-def test_host_input_path_matches_device_path(cuda):
+def test_host_input_path_matches_device_path_and_oracle(cuda):
+    """The host-input path (pinned and pageable frames, calls shorter than its
+    short first batch) against the device-input path bitwise, and against the
+    oracle within the score tolerance."""
     import torch
     wl = synth.custom(256, 144, 10, 422, 9, seed=2)
+    want, _ = _oracle_frames(wl)
     with _scorer(wl.spec, batch=4) as sc:
         s_dev = sc.score(_to_dev(wl.ref), _to_dev(wl.dis))
         pr = torch.from_numpy(wl.ref).pin_memory()
@@ -174,6 +201,8 @@ def test_host_input_path_matches_device_path(cuda):
         s_two = sc.score_host(pr[:2], pd[:2])
     assert np.array_equal(s_dev, s_host) and np.array_equal(s_dev, s_page)
     assert np.array_equal(s_dev[:1], s_one) and np.array_equal(s_dev[:2], s_two)
+    assert np.max(np.abs(s_host - want)) <= SCORE_TOL
+    assert np.max(np.abs(s_page - want)) <= SCORE_TOL
 
 
 def test_context_reuse_two_geometries(cuda):
@@ -232,29 +261,30 @@ def test_zero_frames_and_bad_calls(cuda):
 
 # ---------------------------------------------------------------------------
 # The five workloads, in the launch configuration the benchmark times
-# (default batch), on all frames; the oracle checks a sample of frames.
+# (default batch), every frame against the oracle; the 4K workloads also
+# through the host-input path.
 # ---------------------------------------------------------------------------
 
-CONFIG_SAMPLES = {
-    "c0_576x324_8b_420": None,            # all 4 frames
-    "c1_853x481_8b_444": [0, 1, 2, 3, 47],
-    "c2_1920x1080_10b_420": [0, 1, 2],
-    "c3_3840x2160_8b_420": [0, 49],
-    "c4_3840x2160_12b_444": [0, 1, 2, 3],
-}
+WORKLOADS = ["c0_576x324_8b_420", "c1_853x481_8b_444", "c2_1920x1080_10b_420",
+             "c3_3840x2160_8b_420", "c4_3840x2160_12b_444"]
 
 
-@pytest.mark.parametrize("name", list(CONFIG_SAMPLES))
+@pytest.mark.parametrize("name", WORKLOADS)
 def test_workload_parity(cuda, name):
+    import torch
     spec = synth.SPECS[name]
-    sample = CONFIG_SAMPLES[name]
     wl = synth.make(name)
     with _scorer(spec) as sc:
         got = sc.score(_to_dev(wl.ref), _to_dev(wl.dis))
-    idx = list(range(spec.frames)) if sample is None else sample
-    want, _ = _oracle_frames(wl, frames=idx)
-    err = np.abs(got[idx] - want)
-    assert err.max() <= SCORE_TOL, f"{name}: max |d| {err.max():.3e} at frame {idx[int(err.argmax())]}"
+        got_host = None
+        if spec.width >= 3840:
+            got_host = sc.score_host(torch.from_numpy(wl.ref).pin_memory(),
+                                     torch.from_numpy(wl.dis).pin_memory())
+    want, _ = _oracle_frames(wl)
+    err = np.abs(got - want)
+    assert err.max() <= SCORE_TOL, f"{name}: max |d| {err.max():.3e} at frame {int(err.argmax())}"
+    if got_host is not None:
+        assert np.array_equal(got_host, got)
     if name == "c1_853x481_8b_444":
         assert want[0] == 100.0 and got[0] == 100.0
     if name == "c4_3840x2160_12b_444":
