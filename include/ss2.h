@@ -232,12 +232,27 @@ int ss2_host_tables(float *eotf, float *iir);
  * set-up (looks up the array's address, copies the constant tables with
  * synchronous copies); make it before any stream capture.  All calls on a
  * device share the array and keep the last call's contents; calls that
- * overlap on the GPU race and corrupt each other's results.  Returns 0 or a
- * negative code as the other entry points.
+ * overlap on the GPU race and corrupt each other's results.  Each call
+ * first clears the array's error word on `stream` (a memset, which
+ * allocates nothing).  A kernel whose bounded wait for a copy runs out sets
+ * that word; the call cannot see it (it reads nothing back), so the scores
+ * of the batch then being scored, and of every later batch of the call, are
+ * written as NaN: check the scores for NaN where that matters.  The set-up
+ * is kept for the life of the process: do not use this entry point after a
+ * cudaDeviceReset of a device it ran on.  Returns 0 or a negative code as
+ * the other entry points.
  */
 int ss2_score_frames_noalloc(int width, int height, int bitdepth, int chroma,
                              const void *ref, const void *dis, int n_frames,
                              double *scores, void *stream);
+
+/* ss2_debug_noalloc_timeout — test hook of ss2_score_frames_noalloc (no
+ * counterpart on the source pages): with spins > 0, every later call first
+ * runs a one-warp bounded wait on a barrier phase that nothing completes
+ * (spins polls), which gives up and sets the call's error word, so that the
+ * NaN signal above can be checked without faulting anything; 0 turns it off.
+ * Returns 0.                                                               */
+int ss2_debug_noalloc_timeout(unsigned spins);
 
 /*
  * float_ssim with decimation on the device ("ADR-1405: float_ssim_hip

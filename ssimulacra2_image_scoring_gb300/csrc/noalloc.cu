@@ -22,15 +22,28 @@
 // stream capture on the device.  Later calls enqueue kernels only.
 //
 // Sharing: all calls on a device share the one array, which keeps the last
-// call's contents.  Nothing in it needs to start at zero: each call writes
-// every scratch word before reading it.  Calls whose work overlaps on the GPU
-// (different streams, or different host threads without ordering) race on
-// the array and corrupt each other's scores; order them on one stream.
+// call's contents.  Each call clears the array's error word on its stream
+// before its kernels run, and its kernels write every other scratch word
+// before reading it.  Calls whose work overlaps on the GPU (different
+// streams, or different host threads without ordering) race on the array and
+// corrupt each other's scores; order them on one stream.
+//
+// Failure signal: the blur kernels' bounded waits raise a bit in that error
+// word when a copy never arrives.  Nothing is read back, so the host cannot
+// see it; instead k_finalize writes NaN to every score of its batch when the
+// word is set, which marks the failed batch and every later batch of the
+// call.
+//
+// Device reset: the set-up is cached per device for the life of the
+// process.  After cudaDeviceReset the array's contents (the constant tables)
+// are gone, so this entry point must not be used in a process that has
+// reset a device it ran on.
 //
 // Parameters: the library defaults (see ss2_default_params).
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -58,6 +71,11 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_setup_mutex;
 unsigned char *g_dev_ptr[kMaxDevices] = {};   // device address of g_scratch per device
+
+// Test hook (ss2_debug_noalloc_timeout): when non-zero, each call runs a
+// bounded wait that nothing completes, with this poll limit, against the
+// call's error word, so that the failure signal can be checked.
+std::atomic<unsigned> g_timeout_probe_spins{0};
 
 }  // namespace
 
@@ -143,15 +161,28 @@ SS2_API int ss2_score_frames_noalloc(int width, int height, int bitdepth, int ch
   if (encode_maps(g, X, H, nb_max, maps)) return ss2_last_error();
   int *err = reinterpret_cast<int *>(base + kErrOff);
   cudaStream_t st = (cudaStream_t)stream;
+  // a word left set by an earlier call must not mark this call's scores
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(e, "error word reset");
+  const unsigned probe = g_timeout_probe_spins.load();
+  if (probe) {
+    e = launch_wait_probe(probe, err, st);
+    if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
+  }
   const uint8_t *r8 = static_cast<const uint8_t *>(ref), *d8 = static_cast<const uint8_t *>(dis);
   for (int f0 = 0; f0 < n_frames; f0 += nb_max) {
     const int nb = std::min(nb_max, n_frames - f0);
     const long long off = (long long)f0 * g.frame_bytes;
-    cudaError_t e = launch_pyramid(g, px, tabs, r8 + off, d8 + off, X, nb, st);
+    e = launch_pyramid(g, px, tabs, r8 + off, d8 + off, X, nb, st);
     if (e == cudaSuccess) e = launch_hblur(g, px, maps, err, nb, st);
     if (e == cudaSuccess) e = launch_vblur(g, px, maps, X, part, err, nb, st);
-    if (e == cudaSuccess) e = launch_finalize(g, part, params, values, scores + f0, nb, st);
+    if (e == cudaSuccess) e = launch_finalize(g, part, params, values, scores + f0, nb, st, err);
     if (e != cudaSuccess) return cuda_fail(e, "allocation-free scoring launch");
   }
+  return 0;
+}
+
+SS2_API int ss2_debug_noalloc_timeout(unsigned spins) {
+  g_timeout_probe_spins.store(spins);
   return 0;
 }

@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
             L.ss2_score_frames_noalloc.restype = i
             L.ss2_debug_wait_probe.argtypes = [ctypes.c_uint, vp]
             L.ss2_debug_wait_probe.restype = i
+            L.ss2_debug_noalloc_timeout.argtypes = [ctypes.c_uint]
+            L.ss2_debug_noalloc_timeout.restype = i
             L.ss2_fssim_create.argtypes = [i, i, i, i, i]
             L.ss2_fssim_create.restype = vp
             L.ss2_fssim_score.argtypes = [vp, vp, vp, i, vp, vp]
@@ -179,6 +181,8 @@ def score_noalloc(width: int, height: int, bitdepth: int, chroma: int, ref, dis,
     for t in (ref, dis):
         if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
             raise TypeError("frames must be contiguous CUDA tensors")
+    if ref.device != dis.device:
+        raise ValueError(f"ref is on {ref.device} and dis on {dis.device}")
     fe = (width * height + 2 * ((width + (chroma != 444)) >> (chroma != 444)) *
           ((height + (chroma == 420)) >> (chroma == 420)))
     fb = fe * (1 if bitdepth <= 8 else 2)
@@ -188,9 +192,15 @@ def score_noalloc(width: int, height: int, bitdepth: int, chroma: int, ref, dis,
     n = nbytes // fb
     if scores is None:
         scores = torch.empty(n, dtype=torch.float64, device=ref.device)
-    _check(lib().ss2_score_frames_noalloc(width, height, bitdepth, chroma, ref.data_ptr(),
-                                          dis.data_ptr(), n, scores.data_ptr(),
-                                          _stream_handle(stream)))
+    elif not (isinstance(scores, torch.Tensor) and scores.dtype == torch.float64 and
+              scores.device == ref.device and scores.is_contiguous() and scores.numel() >= n):
+        raise ValueError(f"scores must be a contiguous float64 tensor of at least {n} elements "
+                         f"on {ref.device}")
+    # the C side runs on the current device: make it the frames' device
+    with torch.cuda.device(ref.device):
+        _check(lib().ss2_score_frames_noalloc(width, height, bitdepth, chroma, ref.data_ptr(),
+                                              dis.data_ptr(), n, scores.data_ptr(),
+                                              _stream_handle(stream)))
     return scores
 
 
