@@ -69,7 +69,11 @@ KERNELS = ("k_pyramid", "k_hblur", "k_vblur", "k_finalize")
 
 
 # ---------------------------------------------------------------------------
-# byte models (stated in the design doc)
+# byte models: the algorithmic bytes each kernel must move per frame, and
+# the pipeline minimum B_min (the YUV pair read once; per scale the six XYB
+# planes written once and read twice and the fifteen horizontally blurred
+# planes written and read once; the linear RGB of scales 0-4 written and
+# read once by the downsample)
 # ---------------------------------------------------------------------------
 
 def scale_dims(w: int, h: int) -> list[tuple[int, int]]:
@@ -227,10 +231,57 @@ def oracle_throughput(wl, n_frames: int, threads: int) -> tuple[float, float]:
 
 
 def host_cores() -> int:
+    """Cores this process may run on (its affinity set)."""
     try:
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model string from /proc/cpuinfo (x86: 'model name';
+    Arm: 'Model name' if present, else the implementer and part codes)."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        return "unknown"
+    for key in ("model name", "cpu model", "hardware"):
+        if fields.get(key):
+            return fields[key]
+    if "cpu implementer" in fields:
+        return (f"implementer {fields['cpu implementer']} part {fields.get('cpu part', '?')} "
+                f"variant {fields.get('cpu variant', '?')}")
+    return "unknown"
+
+
+def host_info() -> dict:
+    return {"affinity_cores": host_cores(), "host_cores_total": os.cpu_count() or 1,
+            "cpu_model": cpu_model()}
+
+
+# single-threaded oracle samples per workload: the full frame sets of the
+# small workloads, 8 frames at 1080p, 2 frames at 4K
+ORACLE_SINGLE_FRAMES = {"c0_576x324_8b_420": 4, "c1_853x481_8b_444": 48,
+                        "c2_1920x1080_10b_420": 8, "c3_3840x2160_8b_420": 2,
+                        "c4_3840x2160_12b_444": 2}
+
+
+def oracle_single_thread(wl, n_frames: int) -> float:
+    """Seconds per frame of the oracle on one thread, over the first
+    n_frames frames scored one after another."""
+    import oracle
+    oracle.build()
+    sp = wl.spec
+    n = min(n_frames, wl.ref.shape[0])
+    t0 = time.perf_counter()
+    for j in range(n):
+        oracle.score(wl.ref[j], wl.dis[j], sp.width, sp.height, sp.depth, sp.chroma)
+    return (time.perf_counter() - t0) / n
 
 
 # ---------------------------------------------------------------------------
@@ -270,7 +321,7 @@ def run_reference(args, ws, rank):
         return 0
     spec = synth.SPECS[args.workload]
     cores = host_cores()
-    per_step = max(1, min(cores, 16))
+    per_step = cores
     wl = synth.make(args.workload, per_step, workers=min(per_step, cores))
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; the first step pays nothing extra
@@ -295,7 +346,7 @@ def run_reference(args, ws, rank):
     dt = time.perf_counter() - t0
     fps = scale * per_step * args.steps / dt
     sample = (f"{per_step} frames of {spec.name} per step, one oracle thread per frame "
-              f"on {per_step} host cores" + ("; CAMBI: a full-width sixteenth of each frame, "
+              f"on the {per_step} cores of this process's affinity set" + ("; CAMBI: a full-width sixteenth of each frame, "
                                              "scaled to frames" if scale != 1.0 else ""))
     line = {
         "impl": "reference", "metric": metric, "value": fps,
@@ -305,7 +356,7 @@ def run_reference(args, ws, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+f64", "data": "synthetic",
         "config": {"workload": spec.name, "frames_per_step": per_step},
         "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": per_step,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, **host_info()},
         "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -313,68 +364,133 @@ def run_reference(args, ws, rank):
     return 0
 
 
-def run_ours(args, ws, rank, local):
-    spec = synth.SPECS[args.workload]
-    # generate before any CUDA work (the pool is spawned)
-    wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
+def load_peaks() -> tuple[float, str]:
+    """The measured HBM copy bandwidth (GB/s) and where it came from."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = json.load(f).get("hbm_gbs")
+    except (OSError, ValueError):
+        peak = None
+    if peak:
+        return float(peak), "measured"
+    return 6800.0, "fallback"
+
+
+L2_BYTES = 129e6
+
+
+def time_pipeline(spec, wl, args, ws, dev, steps: int, clocks=None) -> dict:
+    """Scores the workload `steps` times (after the warm-up) with the frames
+    resident in HBM; CUDA events on the scoring stream, per-kernel events
+    inside the library.  Returns the measured figures and the scorer."""
     import torch
-    import torch.distributed as dist
 
     from ssimulacra2_image_scoring_gb300 import Scorer
-    if ws > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", init_method="env://")
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
     ref = torch.from_numpy(wl.ref).to(dev)
     dis = torch.from_numpy(wl.dis).to(dev)
     n = wl.ref.shape[0]
     batch = args.batch or (min(n, 1024) if args.frames else None)
     sc = Scorer(spec.width, spec.height, spec.depth, spec.chroma, batch=batch)
     stream = torch.cuda.current_stream()
-
     for _ in range(args.warmup):
         sc.score(ref, dis, stream)
-
-    clocks = ClockSampler(torch.cuda.current_device())
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
     sc.profile_begin()
     start.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         scores = sc.score(ref, dis, stream)
     end.record(stream)
     torch.cuda.synchronize()
     prof = sc.profile_end()
     barrier(ws)
-    clk = clocks.stop()
-    ms_total = start.elapsed_time(end)
-    ms_total = max_over_ranks(ms_total, ws)
-    ms_step = ms_total / args.steps
-    value = n * ws * args.steps / (ms_total / 1000.0)
-
-    # roofline of the dominant kernel
+    clk = clocks.stop() if clocks else None
+    ms_total = max_over_ranks(start.elapsed_time(end), ws)
+    value = n * ws * steps / (ms_total / 1000.0)
+    peak, peak_src = load_peaks()
     bm = byte_model(spec)
     dom = max(KERNELS, key=lambda k: prof[k][0])
     dom_ms, dom_launches = prof[dom]
-    frames_per_launch = n * args.steps / max(1, dom_launches)
+    frames_per_launch = n * steps / max(1, dom_launches)
     algo_bytes_launch = bm[dom] * frames_per_launch
     achieved_gbs = algo_bytes_launch / (dom_ms / dom_launches / 1000.0) / 1e9
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        peaks = {}
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured"
-    if not peak:
-        peak, peak_src = 6800.0, "fallback"
-    traffic = profile_traffic(dom, spec.name, frames_per_launch)
+    per_kernel = {k: {"ms_total": prof[k][0], "launches": prof[k][1],
+                      "share": prof[k][0] / max(1e-9, sum(prof[j][0] for j in KERNELS))}
+                  for k in KERNELS}
+    pipe_gbs = bm["b_min"] * value / ws / 1e9
+    # L2 residency: a batch's workspace (XYB and blurred planes) against the L2
+    batch_ws = min(sc.batch, n) * 84 * bm["sum_n"]
+    resident = batch_ws + (wl.ref.nbytes + wl.dis.nbytes) <= L2_BYTES
+    return {
+        "sc": sc, "ref": ref, "dis": dis, "scores": scores, "n": n, "value": value,
+        "ms_step": ms_total / steps, "clocks": clk, "prof": prof,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved_gbs, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved_gbs / peak,
+                     "traffic": profile_traffic(dom, spec.name, frames_per_launch),
+                     "algo_bytes_per_launch": algo_bytes_launch,
+                     "avg_launch_ms": dom_ms / dom_launches},
+        "pipeline": {"b_min_bytes_per_frame": bm["b_min"], "achieved_gbs": pipe_gbs,
+                     "frac": pipe_gbs / peak, "frac_vs_nominal_8tbs": pipe_gbs / 8000.0,
+                     "per_kernel": per_kernel},
+        "l2": ("L2-resident: inputs and a batch's workspace fit the 129 MB L2, so the HBM "
+               "roofline does not bound it" if resident else
+               f"inputs larger than L2 (YUV {(wl.ref.nbytes + wl.dis.nbytes) / 1e9:.2f} GB "
+               f"per step, workspace {sc.workspace_bytes / 1e9:.1f} GB)"),
+    }
+
+
+def oracle_baseline(wl, workloads=None) -> dict:
+    """The oracle on the host cores: frame-parallel throughput over every core
+    this process may use (one single-threaded oracle per frame, one frame per
+    core), and the single-threaded seconds per frame of each workload given
+    (name -> Workload), all timed in the same run."""
+    import concurrent.futures as cf
+    info = host_info()
+    single = {}
+    if workloads:
+        # the single-threaded samples of the workloads run side by side, one
+        # core each
+        with cf.ThreadPoolExecutor(max_workers=len(workloads)) as ex:
+            futs = {name: ex.submit(oracle_single_thread, w, ORACLE_SINGLE_FRAMES.get(name, 2))
+                    for name, w in workloads.items()}
+            for name, f in futs.items():
+                single[name] = {"s_per_frame": f.result(),
+                                "frames": min(ORACLE_SINGLE_FRAMES.get(name, 2),
+                                              workloads[name].ref.shape[0])}
+    k = info["affinity_cores"]
+    fps_cpu, dt_cpu = oracle_throughput(wl, k, k)
+    return {"value": fps_cpu, "unit": "frames/s", "cores": k, "kind": "oracle",
+            "sample": f"{k} frames of {wl.spec.name} (frames 0..{min(k, wl.ref.shape[0]) - 1}"
+                      f"{', repeated' if k > wl.ref.shape[0] else ''}), one single-threaded "
+                      f"oracle per frame on all {k} cores of this process's affinity set, "
+                      f"{dt_cpu:.1f} s",
+            **info, "single_thread": single}
+
+
+def run_ours(args, ws, rank, local):
+    spec = synth.SPECS[args.workload]
+    others = [] if (args.frames or args.workloads == "one") else \
+        [name for name in synth.SPECS if name != spec.name]
+    # generate before any CUDA work (the pool is spawned)
+    wl = synth.make(args.workload, args.frames or None, workers=min(16, host_cores()))
+    import torch
+    import torch.distributed as dist
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    m = time_pipeline(spec, wl, args, ws, dev, args.steps, clocks)
+    sc, n = m["sc"], m["n"]
+    batch = sc.batch
+    stream = torch.cuda.current_stream()
 
     # e2e through the host-input entry point from pinned memory
     pr = torch.from_numpy(wl.ref).pin_memory()
@@ -393,48 +509,59 @@ def run_ours(args, ws, rank, local):
         windows.append(max_over_ranks(time.perf_counter() - t0, ws))
     e2e_s = statistics.median(windows)
     e2e_fps = n * ws * max(1, args.steps) / e2e_s
+    gpu_launches = sum(m["prof"][k][1] for k in KERNELS)
+    scores = m["scores"]
+    sc.close()
+    del pr, pd, m["ref"], m["dis"]
+
+    # the other workloads at the same settings, frames resident in HBM
+    per_workload = {spec.name: {
+        "frames_per_s": m["value"], "ms_per_step": m["ms_step"], "frames_per_step": n,
+        "pipeline_frac": m["pipeline"]["frac"], "pipeline_gbs": m["pipeline"]["achieved_gbs"],
+        "b_min_bytes_per_frame": m["pipeline"]["b_min_bytes_per_frame"],
+        "roofline_kernel": m["roofline"]["kernel"], "roofline_frac": m["roofline"]["frac"],
+        "l2": m["l2"]}}
+    host_wls = {spec.name: wl}
+    for name in others:
+        sp = synth.SPECS[name]
+        w2 = synth.make(name, None, workers=min(16, host_cores()))
+        m2 = time_pipeline(sp, w2, args, ws, dev, args.steps)
+        per_workload[name] = {
+            "frames_per_s": m2["value"], "ms_per_step": m2["ms_step"],
+            "frames_per_step": m2["n"], "pipeline_frac": m2["pipeline"]["frac"],
+            "pipeline_gbs": m2["pipeline"]["achieved_gbs"],
+            "b_min_bytes_per_frame": m2["pipeline"]["b_min_bytes_per_frame"],
+            "roofline_kernel": m2["roofline"]["kernel"],
+            "roofline_frac": m2["roofline"]["frac"], "l2": m2["l2"]}
+        m2["sc"].close()
+        del m2
+        host_wls[name] = w2
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cores = host_cores()
-        k = max(1, min(cores, 16))
-        fps_cpu, dt_cpu = oracle_throughput(wl, k, k)
-        cpu = {"value": fps_cpu, "unit": "frames/s", "cores": k, "kind": "oracle",
-               "sample": f"{k} frames of {spec.name} (frames 0..{k - 1}), one oracle thread "
-                         f"per frame on {k} host cores, {dt_cpu:.1f} s"}
+        cpu = oracle_baseline(wl, host_wls)
 
-    gpu_launches = sum(prof[k][1] for k in KERNELS)
-    per_kernel = {k: {"ms_total": prof[k][0], "launches": prof[k][1],
-                      "share": prof[k][0] / max(1e-9, sum(prof[j][0] for j in KERNELS))}
-                  for k in KERNELS}
-    pipe_gbs = bm["b_min"] * value / ws / 1e9
     line = {
-        "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "metric": METRIC, "value": m["value"], "unit": "frames/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": spec.name, "frames_per_step": n, "batch": sc.batch,
-                   "l2": "inputs larger than L2 (YUV 1.24 GB per step, workspace "
-                         f"{sc.workspace_bytes / 1e9:.1f} GB)"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved_gbs, "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved_gbs / peak,
-                     "traffic": traffic,
-                     "algo_bytes_per_launch": algo_bytes_launch,
-                     "avg_launch_ms": dom_ms / dom_launches},
-        "pipeline": {"b_min_bytes_per_frame": bm["b_min"], "achieved_gbs": pipe_gbs,
-                     "frac": pipe_gbs / peak, "frac_vs_nominal_8tbs": pipe_gbs / 8000.0,
-                     "per_kernel": per_kernel},
-        "clocks": clk,
+        "config": {"workload": spec.name, "frames_per_step": n, "batch": batch,
+                   "l2": m["l2"]},
+        "roofline": m["roofline"],
+        "pipeline": m["pipeline"],
+        "clocks": m["clocks"],
         "e2e": {"value": e2e_fps, "unit": "frames/s",
                 "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
                 "d2h_bytes_per_step": 8 * n, "windows_s": windows},
         "gpu_launches": gpu_launches,
         "cpu_baseline": cpu,
+        "workloads": per_workload,
         "scores_head": [float(x) for x in scores[:3]],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    sc.close()
     if ws > 1:
         dist.destroy_process_group()
     return 0
@@ -734,12 +861,13 @@ def run_cambi(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cores = max(1, min(host_cores(), 16))
+        cores = host_cores()
         fps_cpu, dt_cpu = oracle_cambi_throughput(lv_host[:, :h // 16, :], cores, cores,
                                                   (h // 16) * w // 4)
         cpu = {"value": fps_cpu / 16.0, "unit": "frames/s", "cores": cores, "kind": "oracle",
                "sample": f"{cores} bands of {w}x{h // 16} (a sixteenth of a frame each, "
-                         f"scaled to frames), one oracle thread per band, {dt_cpu:.1f} s"}
+                         f"scaled to frames), one oracle thread per band, {dt_cpu:.1f} s",
+               **host_info()}
     line = {
         "metric": CAMBI_METRIC, "value": value, "unit": "frames/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
@@ -840,11 +968,12 @@ def run_fssim(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        k = max(1, min(host_cores(), 16))
+        k = host_cores()
         fps_cpu, dt_cpu = oracle_fssim_throughput(wl, 4 * k, k)
         cpu = {"value": fps_cpu, "unit": "frames/s", "cores": k, "kind": "oracle",
-               "sample": f"{4 * k} frames of {spec.name}, one oracle thread per frame on {k} "
-                         f"host cores, {dt_cpu:.1f} s"}
+               "sample": f"{4 * k} frames of {spec.name}, one oracle thread per frame on the "
+                         f"{k} cores of this process's affinity set, {dt_cpu:.1f} s",
+               **host_info()}
     per_kernel = {k: {"ms_total": prof[k][0], "launches": prof[k][1]} for k in fs.KERNELS}
     pipe_gbs = bm["b_min"] * value / ws / 1e9
     line = {
@@ -886,6 +1015,10 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", choices=["all", "one"], default="all",
+                    help="all (default): after the headline workload, time the other four "
+                         "workloads too and report each under 'workloads'; one: only "
+                         "--workload")
     ap.add_argument("--batch", type=int, default=0,
                     help="frames per pass (default: the library's choice for the geometry)")
     ap.add_argument("--frames", type=int, default=0,
