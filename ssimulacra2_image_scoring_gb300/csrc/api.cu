@@ -68,6 +68,9 @@ SS2_API const char *ss2_last_error_string(void) { return t_msg; }
 // sRGB decoding (IEC 61966-2-1) in fp64.
 static double srgb_to_linear(double v);
 
+// (T[i], T[i+1] - T[i]) for i < N, then (T[N], 0): the interpolation at
+// t = N with index N gives T[N] + 0 * 0 = T[N], which is what index N - 1
+// with weight 1 gives (T[N] - T[N-1] is exact, both lying in [1/2, 1]).
 void ss2::build_eotf_pairs(float *P) {
   float T[kEotfN + 1];
   build_eotf(T);
@@ -75,9 +78,13 @@ void ss2::build_eotf_pairs(float *P) {
     P[2 * i] = T[i];
     P[2 * i + 1] = T[i + 1] - T[i];
   }
+  P[2 * kEotfN] = T[kEotfN];
+  P[2 * kEotfN + 1] = 0.0f;
 }
 
-int ss2::norm_entries(int depth) { return depth == 8 ? 256 : 65536; }
+// 8-bit samples read their normalisations from tables (256 entries each);
+// deeper ones divide without a table on the device.
+int ss2::norm_entries(int depth) { return depth == 8 ? 256 : 0; }
 
 // (v - 16k) / 219k and (v - 128k) / 224k, k = 2^(depth-8), as float
 // quotients of exactly representable operands (correctly rounded).
@@ -486,19 +493,21 @@ static ss2_ctx *create(int w, int h, int depth, int chroma, int batch) {
   }
   if (dev_alloc((void **)&c->d_params, kNParams * sizeof(double), &tot) ||
       dev_alloc((void **)&c->d_tabs,
-                (2 * kEotfN + 2 * norm_entries(depth)) * sizeof(float), &tot) ||
+                (2 * kEotfPairs + 2 * norm_entries(depth)) * sizeof(float), &tot) ||
       dev_alloc((void **)&c->d_err, sizeof(int), &tot)) {
     free_ctx(c);
     return nullptr;
   }
   c->ws_bytes = tot;
   const int nn = norm_entries(depth);
-  std::vector<float> tab((size_t)2 * kEotfN + 2 * (size_t)nn);
+  std::vector<float> tab((size_t)2 * kEotfPairs + 2 * (size_t)nn);
   build_eotf_pairs(tab.data());
-  build_norm(depth, tab.data() + 2 * kEotfN, tab.data() + 2 * kEotfN + nn);
+  build_norm(depth, tab.data() + 2 * kEotfPairs, tab.data() + 2 * kEotfPairs + nn);
   c->tabs.eotf = reinterpret_cast<const float2 *>(c->d_tabs);
-  c->tabs.ynorm = c->d_tabs + 2 * kEotfN;
-  c->tabs.cnorm = c->d_tabs + 2 * kEotfN + nn;
+  c->tabs.ynorm = nn ? c->d_tabs + 2 * kEotfPairs : nullptr;
+  c->tabs.cnorm = nn ? c->d_tabs + 2 * kEotfPairs + nn : nullptr;
+  c->tabs.rdy = 1.0f / (float)(219 << (depth - 8));
+  c->tabs.rdc = 1.0f / (float)(224 << (depth - 8));
   cudaError_t e = cudaMemcpy(c->d_tabs, tab.data(), tab.size() * sizeof(float),
                              cudaMemcpyHostToDevice);
   if (e == cudaSuccess)

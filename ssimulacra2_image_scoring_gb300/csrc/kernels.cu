@@ -56,17 +56,30 @@ constexpr int kPT = 64;  // scale-0 tile edge; 64 = 2^6 keeps 5 halvings inside 
 constexpr int kPyrThreads = 256;
 constexpr int kPyrWarps = kPyrThreads / 32;
 constexpr int kPyrIters = kPT / 2 / kPyrWarps;  // row pairs per warp
-// shared-memory offset of the level-s tile (s >= 1) inside each plane's
-// region: sum_{k=1}^{s-1} (64 >> k)^2 = (4096 - (4096 >> 2(s-1))) / 3
-__host__ __device__ constexpr int lvl_off(int s) { return (4096 - (4096 >> (2 * (s - 1)))) / 3; }
-constexpr int kLvlTotal = lvl_off(kMaxScales);  // 1364 floats per plane
+// Shared tiles of linear RGB: scale 1 (32 x 32 per plane) in a region of
+// its own, scales 2-5 (16^2 + 8^2 + 4^2 + 2^2 = 340 floats per plane) in a
+// region that the row staging of scales 0-1 uses first.  Offset of the
+// scale-s tile (s >= 2) in a plane's part of that region:
+// sum_{k=2}^{s-1} (64 >> k)^2 = (1024 - (4096 >> 2(s-1))) / 3
+constexpr int kLvl1 = 1024;
+__host__ __device__ constexpr int lvl_off(int s) { return (1024 - (4096 >> (2 * (s - 1)))) / 3; }
+constexpr int kLvlRest = lvl_off(kMaxScales);  // 340 floats per plane
 
-// Staging geometry of one launch.
+// Staging geometry, fixed per instantiation (sample width and chroma
+// layout), and the per-launch choices.
+template <int BPS, int SX, int SY>
+struct StageGeo {
+  static constexpr int ybytes = kPT * BPS;            // one staged luma row
+  static constexpr int cbytes = (kPT >> SX) * BPS;    // one staged chroma row
+  static constexpr int crows = SY ? 1 : 2;            // chroma rows per luma row pair
+  static constexpr int img_bytes = 2 * ybytes + 2 * crows * cbytes;  // a multiple of 16
+  static constexpr int buf_bytes = 2 * img_bytes;     // both frames
+  // the staging (two buffers per warp) shares its region with scales 2-5
+  static constexpr int stage_bytes = kPyrWarps * 2 * buf_bytes;
+  static constexpr int union_bytes =
+      stage_bytes > 6 * kLvlRest * 4 ? stage_bytes : 6 * kLvlRest * 4;
+};
 struct PyrStage {
-  int ybytes;     // one staged luma row: 64 samples
-  int cbytes;     // one staged chroma row: 64 >> sx samples
-  int crows;      // chroma rows per luma row pair: 1 (4:2:0) or 2
-  int img_bytes;  // one frame's rows: 2 ybytes + 2 crows cbytes (a multiple of 16)
   int vec;        // 1: 16-byte copies (every staged row starts on 16 bytes)
   int dbg_scale;  // scale whose linear RGB is written to lin_dbg, or -1
 };
@@ -86,24 +99,25 @@ __device__ __forceinline__ void cp_async_wait() {
 // Source of byte `off` of one frame's staged rows for the row pair starting
 // at luma row r0 (layout: luma row r0, luma row r0 + 1, the U rows, the V
 // rows), and whether that byte lies inside the frame.
-__device__ __forceinline__ const uint8_t *stage_src(const Geom &g, const PyrStage &ps,
-                                                    const uint8_t *f, int tx0, int r0, int off,
-                                                    int bps, bool &ok) {
-  if (off < 2 * ps.ybytes) {
-    const int r = off >= ps.ybytes;
-    const int col = off - (r ? ps.ybytes : 0);
+template <int BPS, int SX, int SY>
+__device__ __forceinline__ const uint8_t *stage_src(const Geom &g, const uint8_t *f, int tx0,
+                                                    int r0, int off, bool &ok) {
+  using SG = StageGeo<BPS, SX, SY>;
+  if (off < 2 * SG::ybytes) {
+    const int r = off >= SG::ybytes;
+    const int col = off - (r ? SG::ybytes : 0);
     const int y = r0 + r;
-    ok = y < g.h && tx0 * bps + col < g.w * bps;
-    return f + (y * g.w + tx0) * bps + col;
+    ok = y < g.h && tx0 * BPS + col < g.w * BPS;
+    return f + (y * g.w + tx0) * BPS + col;
   }
-  off -= 2 * ps.ybytes;
-  const int plane = off >= ps.crows * ps.cbytes;
-  off -= plane ? ps.crows * ps.cbytes : 0;
-  const int r = off >= ps.cbytes;  // 0 when there is one chroma row
-  const int col = off - (r ? ps.cbytes : 0);
-  const int cy = (r0 >> g.sy) + r, cx0 = tx0 >> g.sx;
-  ok = cy < g.ch && cx0 * bps + col < g.cw * bps;
-  return f + (g.w * g.h + plane * g.cw * g.ch + cy * g.cw + cx0) * bps + col;
+  off -= 2 * SG::ybytes;
+  const int plane = off >= SG::crows * SG::cbytes;
+  off -= plane ? SG::crows * SG::cbytes : 0;
+  const int r = SG::crows == 2 && off >= SG::cbytes;
+  const int col = off - (r ? SG::cbytes : 0);
+  const int cy = (r0 >> SY) + r, cx0 = tx0 >> SX;
+  ok = cy < g.ch && cx0 * BPS + col < g.cw * BPS;
+  return f + (g.w * g.h + plane * g.cw * g.ch + cy * g.cw + cx0) * BPS + col;
 }
 
 template <int BPS>
@@ -116,23 +130,25 @@ __device__ __forceinline__ int stage_sample(const unsigned char *p) {
 // 16384 x 16384 samples and the byte offset of a V sample stays below
 // 2 x 1.5 x 2^28; each scale's XYB block is reached from a 64-bit base and
 // its six planes lie within 6 x 2^28 floats of it.
-template <int BPS>
+template <int BPS, int SX, int SY, bool DBG>
 __global__ void __launch_bounds__(kPyrThreads, 4)
     k_pyramid(Geom g, Pix px, PyrTabs tabs, PyrStage ps, const uint8_t *__restrict__ ref,
               const uint8_t *__restrict__ dis, float *__restrict__ X,
               float *__restrict__ lin_dbg) {
+  using SG = StageGeo<BPS, SX, SY>;
   extern __shared__ __align__(16) unsigned char psm[];
-  float(*L)[kLvlTotal] = reinterpret_cast<float(*)[kLvlTotal]>(psm);
-  float *ntab = reinterpret_cast<float *>(psm + sizeof(float) * 6 * kLvlTotal);
+  float(*L1)[kLvl1] = reinterpret_cast<float(*)[kLvl1]>(psm);
+  unsigned char *stage = psm + sizeof(float) * 6 * kLvl1;           // scales 0-1 ...
+  float(*Lr)[kLvlRest] = reinterpret_cast<float(*)[kLvlRest]>(stage);  // ... then 2-5
+  float *ntab = reinterpret_cast<float *>(stage + SG::union_bytes);
   float *cb_s = ntab + (BPS == 1 ? 512 : 0);
-  unsigned char *stage = reinterpret_cast<unsigned char *>(cb_s + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int frame = blockIdx.z;
   const int tx0 = blockIdx.x * kPT, ty0 = blockIdx.y * kPT;
   float *Xf = X + (long long)frame * g.x_fs;
   const uint8_t *fref = ref + (long long)frame * g.frame_bytes;
   const uint8_t *fdis = dis + (long long)frame * g.frame_bytes;
-  const int buf_bytes = 2 * ps.img_bytes;
+  constexpr int buf_bytes = SG::buf_bytes;
   unsigned char *wst = stage + warp * 2 * buf_bytes;  // this warp's two buffers
 
   // row pair i of this warp -> buffer i & 1 (vec: one copy group per row pair)
@@ -143,10 +159,10 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
       if (r0 < g.h) {
         for (int c = lane; c < (buf_bytes >> 4); c += 32) {
           int off = c << 4;
-          const int img = off >= ps.img_bytes;
-          off -= img ? ps.img_bytes : 0;
+          const int img = off >= SG::img_bytes;
+          off -= img ? SG::img_bytes : 0;
           bool ok;
-          const uint8_t *src = stage_src(g, ps, img ? fdis : fref, tx0, r0, off, BPS, ok);
+          const uint8_t *src = stage_src<BPS, SX, SY>(g, img ? fdis : fref, tx0, r0, off, ok);
           if (ok) cp_async16(dst + (c << 4), src);
         }
       }
@@ -154,10 +170,10 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
     } else if (r0 < g.h) {
       for (int e = lane; e < buf_bytes / BPS; e += 32) {
         int off = e * BPS;
-        const int img = off >= ps.img_bytes;
-        off -= img ? ps.img_bytes : 0;
+        const int img = off >= SG::img_bytes;
+        off -= img ? SG::img_bytes : 0;
         bool ok;
-        const uint8_t *src = stage_src(g, ps, img ? fdis : fref, tx0, r0, off, BPS, ok);
+        const uint8_t *src = stage_src<BPS, SX, SY>(g, img ? fdis : fref, tx0, r0, off, ok);
         if (ok) {
           if (BPS == 1)
             dst[e] = __ldg(src);
@@ -192,6 +208,7 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
   const int lx0 = 2 * lane;                             // the quad's tile columns
   const int lx1 = min(lx0 + 1, g.w - 1 - tx0);          // clamped at an odd right edge
   const bool has_x1 = tx0 + lx0 + 1 < g.w;
+  const bool dbg0 = DBG && ps.dbg_scale == 0, dbg1 = DBG && ps.dbg_scale == 1;
 
   // ---- scales 0 and 1 ----
   for (int i = 0; i < kPyrIters; ++i) {
@@ -208,23 +225,25 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
     if (y0 < g.h && tx0 + lx0 < g.w) {
       const bool has_y1 = y0 + 1 < g.h;
       const unsigned char *sb = wst + (i & 1) * buf_bytes;
-      float lin1[6];
-#pragma unroll
+      const int x1 = (tx0 >> 1) + lane, y1 = (ty0 >> 1) + rp;  // the scale-1 pixel
+      // one image at a time (not unrolled: the body holds three cube roots
+      // per pixel, and one copy of it keeps the code in the instruction cache)
+#pragma unroll 1
       for (int img = 0; img < 2; ++img) {
-        const unsigned char *sY = sb + img * ps.img_bytes;
-        const unsigned char *sU = sY + 2 * ps.ybytes;
-        const unsigned char *sV = sU + ps.crows * ps.cbytes;
+        const unsigned char *sY = sb + img * SG::img_bytes;
+        const unsigned char *sU = sY + 2 * SG::ybytes;
+        const unsigned char *sV = sU + SG::crows * SG::cbytes;
         float acc[3];
 #pragma unroll 1
         for (int dyy = 0; dyy < 2; ++dyy) {
           const int rr = dyy && has_y1 ? 1 : 0;  // clamped at an odd bottom edge
-          const int crr = ps.crows == 2 ? rr : 0;
+          const int crr = SG::crows == 2 ? rr : 0;
           float o[2][3];
 #pragma unroll
           for (int dxx = 0; dxx < 2; ++dxx) {
             const int lx = dxx ? lx1 : lx0;
-            const int Ys = stage_sample<BPS>(sY + rr * ps.ybytes + lx * BPS);
-            const int cofs = crr * ps.cbytes + (lx >> g.sx) * BPS;
+            const int Ys = stage_sample<BPS>(sY + rr * SG::ybytes + lx * BPS);
+            const int cofs = crr * SG::cbytes + (lx >> SX) * BPS;
             const int Us = stage_sample<BPS>(sU + cofs);
             const int Vs = stage_sample<BPS>(sV + cofs);
             float yn, cbv, crv;
@@ -232,14 +251,10 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
               yn = ntab[Ys];
               cbv = ntab[256 + Us];
               crv = ntab[256 + Vs];
-            } else if (tabs.ynorm) {
-              yn = __ldg(tabs.ynorm + Ys);
-              cbv = __ldg(tabs.cnorm + Us);
-              crv = __ldg(tabs.cnorm + Vs);
             } else {
-              yn = __fdiv_rn((float)(Ys - 16 * k), dy);
-              cbv = __fdiv_rn((float)(Us - 128 * k), dc);
-              crv = __fdiv_rn((float)(Vs - 128 * k), dc);
+              yn = norm_div(Ys - 16 * k, dy, tabs.rdy);
+              cbv = norm_div(Us - 128 * k, dc, tabs.rdc);
+              crv = norm_div(Vs - 128 * k, dc, tabs.rdc);
             }
             const float r = __fmaf_rn(px.yuv[0], crv, yn);
             const float gg = __fmaf_rn(-px.yuv[2], crv, __fmaf_rn(-px.yuv[1], cbv, yn));
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
               acc[1] = __fadd_rn(acc[1], G);
               acc[2] = __fadd_rn(acc[2], B);
             }
-            if (lin_dbg && ps.dbg_scale == 0 && (dyy == 0 || has_y1) && (dxx == 0 || has_x1)) {
+            if (dbg0 && (dyy == 0 || has_y1) && (dxx == 0 || has_x1)) {
               const long long q = (long long)(y0 + dyy) * g.w + tx0 + lx;
               const long long n0 = (long long)g.w * g.h;
               lin_dbg[(3 * img + 0) * n0 + q] = R;
@@ -278,33 +293,33 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
             }
           }
         }
+        if (two_scales) {
+          float lin1[3];
 #pragma unroll
-        for (int c = 0; c < 3; ++c) lin1[3 * img + c] = __fmul_rn(acc[c], 0.25f);
-      }
-      if (two_scales) {
-        const int x = (tx0 >> 1) + lane, y = (ty0 >> 1) + rp;
-        float *P = P1 + (y * pitch1 + x);
-#pragma unroll
-        for (int img = 0; img < 2; ++img) {
+          for (int c = 0; c < 3; ++c) {
+            lin1[c] = __fmul_rn(acc[c], 0.25f);
+            L1[3 * img + c][rp * 32 + lane] = lin1[c];
+          }
+          float *P = P1 + (y1 * pitch1 + x1);
           float xo, yo, bo;
-          pixel_xyb(px, cb, lin1[3 * img], lin1[3 * img + 1], lin1[3 * img + 2], xo, yo, bo);
+          pixel_xyb(px, cb, lin1[0], lin1[1], lin1[2], xo, yo, bo);
           P[(3 * img + 0) * plane1] = xo;
           P[(3 * img + 1) * plane1] = yo;
           P[(3 * img + 2) * plane1] = bo;
-        }
+          if (dbg1) {
+            const long long n1 = (long long)g.ws[1] * g.hs[1];
+            const long long q = (long long)y1 * g.ws[1] + x1;
 #pragma unroll
-        for (int c = 0; c < 6; ++c) L[c][rp * 32 + lane] = lin1[c];
-        if (lin_dbg && ps.dbg_scale == 1) {
-          const long long n1 = (long long)g.ws[1] * g.hs[1];
-          const long long q = (long long)y * g.ws[1] + x;
-#pragma unroll
-          for (int c = 0; c < 6; ++c) lin_dbg[c * n1 + q] = lin1[c];
+            for (int c = 0; c < 3; ++c) lin_dbg[(3 * img + c) * n1 + q] = lin1[c];
+          }
         }
       }
     }
     __syncwarp();  // buffer i & 1 is refilled by stage_rows(i + 2)
   }
   if (g.nscales <= 2) return;
+  // every warp's staging reads and copies are done: the region holds
+  // scales 2-5 from here on
   __syncthreads();
 
   // ---- scales 2..: halve the shared tile, then XYB ----
@@ -328,30 +343,30 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
         const int y0 = 2 * y, y1 = min(2 * y + 1, hh - 1);
         const int i00 = (y0 - poy) * pw + (x0 - pox), i01 = (y0 - poy) * pw + (x1 - pox);
         const int i10 = (y1 - poy) * pw + (x0 - pox), i11 = (y1 - poy) * pw + (x1 - pox);
-        float v[6];
-#pragma unroll
-        for (int c = 0; c < 6; ++c) {
-          const float *Lp = &L[c][lvl_off(s - 1)];
-          float t = __fadd_rn(Lp[i00], Lp[i01]);
-          t = __fadd_rn(t, Lp[i10]);
-          t = __fadd_rn(t, Lp[i11]);
-          v[c] = __fmul_rn(t, 0.25f);
-          L[c][lvl_off(s) + p] = v[c];
-        }
         float *P = Ps + (y * pitchs + x);
-#pragma unroll
+#pragma unroll 1
         for (int img = 0; img < 2; ++img) {
+          float v[3];
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            const float *Lp = s == 2 ? L1[3 * img + c] : &Lr[3 * img + c][lvl_off(s - 1)];
+            float t = __fadd_rn(Lp[i00], Lp[i01]);
+            t = __fadd_rn(t, Lp[i10]);
+            t = __fadd_rn(t, Lp[i11]);
+            v[c] = __fmul_rn(t, 0.25f);
+            Lr[3 * img + c][lvl_off(s) + p] = v[c];
+          }
           float xo, yo, bo;
-          pixel_xyb(px, cb, v[3 * img], v[3 * img + 1], v[3 * img + 2], xo, yo, bo);
+          pixel_xyb(px, cb, v[0], v[1], v[2], xo, yo, bo);
           P[(3 * img + 0) * planes] = xo;
           P[(3 * img + 1) * planes] = yo;
           P[(3 * img + 2) * planes] = bo;
-        }
-        if (lin_dbg && ps.dbg_scale == s) {
-          const long long ns = (long long)g.ws[s] * g.hs[s];
-          const long long q = (long long)y * g.ws[s] + x;
+          if (DBG && ps.dbg_scale == s) {
+            const long long ns = (long long)g.ws[s] * g.hs[s];
+            const long long q = (long long)y * g.ws[s] + x;
 #pragma unroll
-          for (int c = 0; c < 6; ++c) lin_dbg[c * ns + q] = v[c];
+            for (int c = 0; c < 3; ++c) lin_dbg[(3 * img + c) * ns + q] = v[c];
+          }
         }
       }
     }
@@ -914,43 +929,66 @@ cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st) 
   return cudaGetLastError();
 }
 
+// Dynamic shared memory of one instantiation: the scale-1 tiles, the region
+// shared by the staging buffers and the scale 2-5 tiles, the 8-bit
+// normalisation tables and cbrt(bias).
+template <int BPS, int SX, int SY>
+constexpr int pyr_smem() {
+  return (int)sizeof(float) * (6 * kLvl1 + (BPS == 1 ? 512 : 0) + 4) +
+         StageGeo<BPS, SX, SY>::union_bytes;
+}
+
+template <int BPS, int SX, int SY, bool DBG>
+static cudaError_t launch_pyr_dbg(const Geom &g, const Pix &px, const PyrTabs &tabs,
+                                  PyrStage ps, const uint8_t *ref, const uint8_t *dis, float *X,
+                                  float *lin_dbg, int nframes, cudaStream_t st) {
+  constexpr int smem = pyr_smem<BPS, SX, SY>();
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::atomic<bool> configured[64];
+  if (dev < 64 && !configured[dev].load()) {
+    e = cudaFuncSetAttribute(k_pyramid<BPS, SX, SY, DBG>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev].store(true);
+  }
+  dim3 grid((g.w + kPT - 1) / kPT, (g.h + kPT - 1) / kPT, nframes);
+  k_pyramid<BPS, SX, SY, DBG>
+      <<<grid, kPyrThreads, smem, st>>>(g, px, tabs, ps, ref, dis, X, lin_dbg);
+  return cudaGetLastError();
+}
+
+// The linear-RGB dump of the parity tests is a separate instantiation: the
+// scoring kernels carry no trace of it.
+template <int BPS, int SX, int SY>
+static cudaError_t launch_pyr(const Geom &g, const Pix &px, const PyrTabs &tabs, PyrStage ps,
+                              const uint8_t *ref, const uint8_t *dis, float *X, float *lin_dbg,
+                              int nframes, cudaStream_t st) {
+  if (lin_dbg)
+    return launch_pyr_dbg<BPS, SX, SY, true>(g, px, tabs, ps, ref, dis, X, lin_dbg, nframes, st);
+  return launch_pyr_dbg<BPS, SX, SY, false>(g, px, tabs, ps, ref, dis, X, nullptr, nframes, st);
+}
+
 cudaError_t launch_pyramid(const Geom &g, const Pix &px, const PyrTabs &tabs, const uint8_t *ref,
                            const uint8_t *dis, float *X, int nframes, cudaStream_t st,
                            float *lin_dbg, int dbg_scale) {
   PyrStage ps;
-  ps.ybytes = kPT * g.bps;
-  ps.cbytes = (kPT >> g.sx) * g.bps;
-  ps.crows = g.sy ? 1 : 2;
-  ps.img_bytes = 2 * ps.ybytes + 2 * ps.crows * ps.cbytes;
   // every staged row starts on 16 bytes: frame bases, plane offsets and row
   // pitches of both planes, and the tile origins (multiples of 64 samples)
   ps.vec = (reinterpret_cast<uintptr_t>(ref) % 16 == 0) &&
            (reinterpret_cast<uintptr_t>(dis) % 16 == 0) && g.frame_bytes % 16 == 0 &&
            (g.w * g.bps) % 16 == 0 && (g.cw * g.bps) % 16 == 0;
   ps.dbg_scale = lin_dbg ? dbg_scale : -1;
-  const int smem = (int)sizeof(float) * (6 * kLvlTotal + (g.bps == 1 ? 512 : 0) + 4) +
-                   kPyrWarps * 2 * 2 * ps.img_bytes;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  static std::atomic<bool> configured[64];
-  if (dev < 64 && !configured[dev].load()) {
-    e = cudaFuncSetAttribute(k_pyramid<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(float) * (6 * kLvlTotal + 512 + 4) +
-                                 kPyrWarps * 2 * 2 * (2 * kPT + 2 * 2 * kPT));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_pyramid<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sizeof(float) * (6 * kLvlTotal + 4) +
-                                   kPyrWarps * 2 * 2 * 2 * (2 * kPT + 2 * 2 * kPT));
-    if (e != cudaSuccess) return e;
-    configured[dev].store(true);
+  const int layout = g.sx * 2 + g.sy;  // 3: 4:2:0, 2: 4:2:2, 0: 4:4:4
+  if (g.bps == 1) {
+    if (layout == 3) return launch_pyr<1, 1, 1>(g, px, tabs, ps, ref, dis, X, lin_dbg, nframes, st);
+    if (layout == 2) return launch_pyr<1, 1, 0>(g, px, tabs, ps, ref, dis, X, lin_dbg, nframes, st);
+    return launch_pyr<1, 0, 0>(g, px, tabs, ps, ref, dis, X, lin_dbg, nframes, st);
   }
-  dim3 grid((g.w + kPT - 1) / kPT, (g.h + kPT - 1) / kPT, nframes);
-  if (g.bps == 1)
-    k_pyramid<1><<<grid, kPyrThreads, smem, st>>>(g, px, tabs, ps, ref, dis, X, lin_dbg);
-  else
-    k_pyramid<2><<<grid, kPyrThreads, smem, st>>>(g, px, tabs, ps, ref, dis, X, lin_dbg);
-  return cudaGetLastError();
+  if (layout == 3) return launch_pyr<2, 1, 1>(g, px, tabs, ps, ref, dis, X, lin_dbg, nframes, st);
+  if (layout == 2) return launch_pyr<2, 1, 0>(g, px, tabs, ps, ref, dis, X, lin_dbg, nframes, st);
+  return launch_pyr<2, 0, 0>(g, px, tabs, ps, ref, dis, X, lin_dbg, nframes, st);
 }
 
 cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, int *err,

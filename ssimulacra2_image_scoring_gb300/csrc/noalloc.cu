@@ -63,7 +63,7 @@ constexpr size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign;
 
 // head of the array: constant tables written once at set-up
 constexpr size_t kEotfOff = 0;
-constexpr size_t kParamsOff = align_up(kEotfOff + sizeof(float) * 2 * ss2::kEotfN);
+constexpr size_t kParamsOff = align_up(kEotfOff + sizeof(float) * 2 * ss2::kEotfPairs);
 constexpr size_t kErrOff = align_up(kParamsOff + sizeof(double) * ss2::kNParams);
 constexpr size_t kHeadBytes = align_up(kErrOff + sizeof(int));
 
@@ -92,7 +92,7 @@ static int scratch_for_device(int dev, unsigned char **out) {
     void *p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-    float table[2 * kEotfN];
+    float table[2 * kEotfPairs];
     double params[kNParams];
     build_eotf_pairs(table);
     default_params(params);
@@ -145,8 +145,10 @@ SS2_API int ss2_score_frames_noalloc(int width, int height, int bitdepth, int ch
   double *values = reinterpret_cast<double *>(work + nb_max * (x_bytes + h_bytes + p_bytes));
   PyrTabs tabs;
   tabs.eotf = reinterpret_cast<const float2 *>(base + kEotfOff);
-  tabs.ynorm = nullptr;   // normalisation by division on the device
+  tabs.ynorm = nullptr;   // normalisation without tables on the device
   tabs.cnorm = nullptr;
+  tabs.rdy = 1.0f / (float)(219 << (bitdepth - 8));
+  tabs.rdc = 1.0f / (float)(224 << (bitdepth - 8));
   const double *params = reinterpret_cast<const double *>(base + kParamsOff);
   // the kernels index frames by g.x_fs / g.h_fs / g.p_fs; use the padded strides
   g.x_fs = (long long)(x_bytes / sizeof(float));

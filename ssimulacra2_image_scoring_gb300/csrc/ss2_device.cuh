@@ -176,6 +176,13 @@ __device__ __noinline__ float cbrt_round_exact(float x, float y) {
   return y;
 }
 
+// Inputs below 2^-100 (zeros included): the first guess from CUDA's cbrtf,
+// settled by the exact decision.  Out of line: it is rare, and inlining the
+// library cube root at every call site would bloat the kernels' code.
+__device__ __noinline__ float cbrt_tiny(float x) {
+  return x == 0.0f ? x : cbrt_round_exact(x, cbrtf(x));
+}
+
 // log2 and 2^x approximations in the .ftz form: the cube root's fast path
 // calls them only for x >= 2^-100, where neither operand nor result is
 // subnormal.
@@ -200,15 +207,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
 //   3. One Newton step y0 + R / (3 y0^2), whose error is about 2^-41 y0,
 //      with the rounding error of the final addition kept exactly
 //      (quick_two_sum: the correction is below 2^-19 y0): the root lies at
-//      that error (plus 2^-41 y0) from the float y, so y is the nearest
-//      float unless the error is within 2^-14 ulp of half an ulp.
-//   4. Those near-ties, powers of two (where the spacing below halves) and
-//      x < 2^-100 (where the products' error terms underflow) take the exact
-//      128-bit integer decision; +-0 return themselves.
+//      y.hi + y.lo, give or take 2^-41 y0.
+//   4. y.hi is the nearest float when y.lo is below half the float spacing
+//      on its side of y.hi, with a margin that covers that 2^-41: one fma
+//      decides it, y.hi + y.lo (1 + 2^-13) rounding back to y.hi (rounding
+//      uses the spacing on the side y.lo points to, so the halved spacing
+//      below a power of two is taken care of).  Only near-ties (about one
+//      input in 2^13) and x < 2^-100 (where the products' error terms
+//      underflow) take the exact 128-bit integer decision; +-0 return
+//      themselves.
 __device__ __forceinline__ float cbrt_cr(float x) {
   // magnitude below 2^-100, zeros included (the sign bit shifted out)
   if ((__float_as_uint(x) << 1) < (0x0d800000u << 1))
-    return x == 0.0f ? x : cbrt_round_exact(x, cbrtf(x));
+    return cbrt_tiny(x);
   const float y0 = ex2_approx(__fmul_rn(lg2_approx(x), 0.333333343f));
   const ff p = two_prod(y0, y0);
   const ff q = two_prod(y0, p.hi);
@@ -217,9 +228,7 @@ __device__ __forceinline__ float cbrt_cr(float x) {
   r = __fmaf_rn(-y0, p.lo, r);
   const float d = __fmul_rn(r, rcp_approx(__fmul_rn(3.0f, p.hi)));
   const ff y = quick_two_sum(y0, d);
-  const uint32_t yb = __float_as_uint(y.hi);
-  const float half_u = __uint_as_float((yb & 0x7f800000u) - (24u << 23));
-  if ((yb & 0x7fffffu) != 0u && fabsf(y.lo) < __fmul_rn(half_u, 0.99993896484375f)) return y.hi;
+  if (__fmaf_rn(y.lo, 1.0001220703125f, y.hi) == y.hi) return y.hi;
   return cbrt_round_exact(x, y.hi);
 }
 
@@ -233,12 +242,24 @@ __device__ __forceinline__ float clamp01(float v) {
   return v;
 }
 
+// (float)n / d correctly rounded without a division, for d = 219 k or
+// 224 k (k a power of two) and |n| <= 65536, from rd = RN(1 / d): the
+// product, its exact fma residual and one correction.  Checked against the
+// IEEE quotient for every such n and both divisors (the power-of-two k
+// scales every step exactly); the limited-range normalisation of samples of
+// any depth stays within that range.
+__device__ __forceinline__ float norm_div(int n, float d, float rd) {
+  const float nf = (float)n;
+  const float q0 = __fmul_rn(nf, rd);
+  return __fmaf_rn(__fmaf_rn(-q0, d, nf), rd, q0);
+}
+
 // Linear interpolation in the sRGB EOTF table (uniform grid, 4096 intervals),
-// stored as (T[i], T[i+1] - T[i]) pairs.
+// stored as (T[i], T[i+1] - T[i]) pairs plus a last pair (T[4096], 0): for
+// v in [0, 1] the index is at most 4096 and needs no clamp.
 __device__ __forceinline__ float eotf_lookup(const float2 *__restrict__ P, float v) {
   float t = __fmul_rn(v, (float)kEotfN);
   int i = (int)t;
-  i = i > kEotfN - 1 ? kEotfN - 1 : i;
   float f = __fsub_rn(t, (float)i);
   const float2 e = __ldg(P + i);
   return __fmaf_rn(f, e.y, e.x);

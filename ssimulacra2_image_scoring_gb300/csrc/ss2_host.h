@@ -29,8 +29,8 @@ int encode_maps(const Geom &g, float *X, float *H, int batch, PlaneMaps &maps);
 void default_params(double *params);                      // kNParams doubles
 void build_pix(const double *params, Pix &p);
 void build_eotf(float *table);                            // kEotfN + 1 floats
-void build_eotf_pairs(float *pairs);                      // 2 * kEotfN floats
-int norm_entries(int depth);                              // 256 or 65536
+void build_eotf_pairs(float *pairs);                      // 2 * kEotfPairs floats
+int norm_entries(int depth);                              // 256 (8-bit) or 0
 void build_norm(int depth, float *ynorm, float *cnorm);   // norm_entries(depth) each
 
 // Per-kernel CUDA-event timing of one context (the ss2*_profile_begin /

@@ -14,6 +14,7 @@ constexpr int kMaxScales = 6;
 constexpr int kNValues = 108;
 constexpr int kNParams = 133;
 constexpr int kEotfN = 4096;   // table intervals; the table has kEotfN + 1 entries
+constexpr int kEotfPairs = kEotfN + 1;  // device (value, slope) pairs, the last (T[N], 0)
 constexpr int kIirR = 4;       // recursive Gaussian support |m| <= R
 constexpr int kReach = kIirR + 1;  // taps at n +- (R + 1)
 constexpr int kNq = 5;         // blurred quantities per channel: mu1 mu2 s11 s22 s12
@@ -57,15 +58,19 @@ struct PlaneMaps {
 constexpr int kBoxCols = 8, kBoxRows = 32;      // horizontal pass box
 constexpr int kVCols = 32, kVRows = 8;          // vertical pass box
 
-// Tables the pyramid kernel reads.  eotf: 4096 (value, slope) pairs of the
-// sRGB EOTF table, slope = T[i+1] - T[i] rounded to float.  ynorm / cnorm:
-// the limited-range normalisations (v - 16k) / 219k and (v - 128k) / 224k of
-// every sample value v (256 entries at 8 bits, 65536 above), each a
-// correctly rounded float quotient; null means divide on the device.
+// Tables the pyramid kernel reads.  eotf: 4097 (value, slope) pairs of the
+// sRGB EOTF table, slope = T[i+1] - T[i] rounded to float, and a last pair
+// (T[4096], 0) so that an input of exactly 1 needs no index clamp.
+// ynorm / cnorm (8-bit samples only, else null): the limited-range
+// normalisations (v - 16) / 219 and (v - 128) / 224 of every sample value v,
+// each a correctly rounded float quotient.  rdy / rdc: RN(1 / (219 k)) and
+// RN(1 / (224 k)), k = 2^(depth - 8), for the division-free normalisation
+// of deeper samples (and of 8-bit ones when the tables are null).
 struct PyrTabs {
   const float2 *eotf;
   const float *ynorm;
   const float *cnorm;
+  float rdy, rdc;
 };
 
 // Per-pixel constants (fp32 pipeline), rounded from the parameter vector.
