@@ -131,7 +131,7 @@ __device__ __forceinline__ int stage_sample(const unsigned char *p) {
 // 2 x 1.5 x 2^28; each scale's XYB block is reached from a 64-bit base and
 // its six planes lie within 6 x 2^28 floats of it.
 template <int BPS, int SX, int SY, bool DBG>
-__global__ void __launch_bounds__(kPyrThreads, 4)
+__global__ void __launch_bounds__(kPyrThreads, 5)
     k_pyramid(Geom g, Pix px, PyrTabs tabs, PyrStage ps, const uint8_t *__restrict__ ref,
               const uint8_t *__restrict__ dis, float *__restrict__ X,
               float *__restrict__ lin_dbg) {
