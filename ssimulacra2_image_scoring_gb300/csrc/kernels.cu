@@ -233,35 +233,64 @@ __global__ void __launch_bounds__(kPyrThreads, 5)
         const unsigned char *sY = sb + img * SG::img_bytes;
         const unsigned char *sU = sY + 2 * SG::ybytes;
         const unsigned char *sV = sU + SG::crows * SG::cbytes;
+        // normalised chroma of (staged row crr, chroma column cl)
+        auto chroma = [&](int crr, int cl, float &cbv, float &crv) {
+          const int cofs = crr * SG::cbytes + cl * BPS;
+          const int Us = stage_sample<BPS>(sU + cofs);
+          const int Vs = stage_sample<BPS>(sV + cofs);
+          if (BPS == 1 && tabs.ynorm) {
+            cbv = ntab[256 + Us];
+            crv = ntab[256 + Vs];
+          } else {
+            cbv = norm_div(Us - 128 * k, dc, tabs.rdc);
+            crv = norm_div(Vs - 128 * k, dc, tabs.rdc);
+          }
+        };
+        // horizontally subsampled chroma: both pixels of a quad row share
+        // one chroma sample (column lane, also when the right one is
+        // clamped); vertically subsampled: both rows share one chroma row
+        float cbq[2][2], crq[2][2];   // [dyy][dxx]
+        if (SY) {
+          chroma(0, lx0 >> SX, cbq[0][0], crq[0][0]);
+          if (SX) {
+            cbq[0][1] = cbq[0][0];
+            crq[0][1] = crq[0][0];
+          } else {
+            chroma(0, lx1, cbq[0][1], crq[0][1]);
+          }
+        }
         float acc[3];
 #pragma unroll 1
         for (int dyy = 0; dyy < 2; ++dyy) {
           const int rr = dyy && has_y1 ? 1 : 0;  // clamped at an odd bottom edge
-          const int crr = SG::crows == 2 ? rr : 0;
+          float cbr[2], crr_[2];
+          if (SY) {
+#pragma unroll
+            for (int d = 0; d < 2; ++d) {
+              cbr[d] = cbq[0][d];
+              crr_[d] = crq[0][d];
+            }
+          } else {
+            chroma(rr, lx0 >> SX, cbr[0], crr_[0]);
+            if (SX) {
+              cbr[1] = cbr[0];
+              crr_[1] = crr_[0];
+            } else {
+              chroma(rr, lx1, cbr[1], crr_[1]);
+            }
+          }
           float o[2][3];
 #pragma unroll
           for (int dxx = 0; dxx < 2; ++dxx) {
             const int lx = dxx ? lx1 : lx0;
             const int Ys = stage_sample<BPS>(sY + rr * SG::ybytes + lx * BPS);
-            const int cofs = crr * SG::cbytes + (lx >> SX) * BPS;
-            const int Us = stage_sample<BPS>(sU + cofs);
-            const int Vs = stage_sample<BPS>(sV + cofs);
-            float yn, cbv, crv;
-            if (BPS == 1 && tabs.ynorm) {
-              yn = ntab[Ys];
-              cbv = ntab[256 + Us];
-              crv = ntab[256 + Vs];
-            } else {
-              yn = norm_div(Ys - 16 * k, dy, tabs.rdy);
-              cbv = norm_div(Us - 128 * k, dc, tabs.rdc);
-              crv = norm_div(Vs - 128 * k, dc, tabs.rdc);
-            }
-            const float r = __fmaf_rn(px.yuv[0], crv, yn);
-            const float gg = __fmaf_rn(-px.yuv[2], crv, __fmaf_rn(-px.yuv[1], cbv, yn));
-            const float b = __fmaf_rn(px.yuv[3], cbv, yn);
-            const float R = eotf_lookup(tabs.eotf, clamp01(r));
-            const float G = eotf_lookup(tabs.eotf, clamp01(gg));
-            const float B = eotf_lookup(tabs.eotf, clamp01(b));
+            const float yn = BPS == 1 && tabs.ynorm ? ntab[Ys] : norm_div(Ys - 16 * k, dy, tabs.rdy);
+            const float cbv = cbr[dxx], crv = crr_[dxx];
+            // R'G'B' clamped to [0, 1] as part of the matrix's last fma
+            const float R = eotf_lookup(tabs.eotf, fma_sat(px.yuv[0], crv, yn));
+            const float G = eotf_lookup(
+                tabs.eotf, fma_sat(-px.yuv[2], crv, __fmaf_rn(-px.yuv[1], cbv, yn)));
+            const float B = eotf_lookup(tabs.eotf, fma_sat(px.yuv[3], cbv, yn));
             // the 2x2 mean in the order ((p00 + p01) + p10) + p11
             if (dyy == 0 && dxx == 0) {
               acc[0] = R;

@@ -198,7 +198,9 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return r;
 }
 
-// Correctly rounded cbrt for x >= 0 finite.
+// Correctly rounded cbrt for x >= 0 finite, in two parts so that a caller
+// with several cube roots can take one branch for all of their rare slow
+// paths.  cbrt_fast:
 //   1. y0 = 2^(log2(x) / 3) from the hardware approximations (within about
 //      2^-20 relative).
 //   2. The residual R = x - y0^3 to about 2^-46 x: y0^2 = p + e and
@@ -212,14 +214,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
 //      on its side of y.hi, with a margin that covers that 2^-41: one fma
 //      decides it, y.hi + y.lo (1 + 2^-13) rounding back to y.hi (rounding
 //      uses the spacing on the side y.lo points to, so the halved spacing
-//      below a power of two is taken care of).  Only near-ties (about one
-//      input in 2^13) and x < 2^-100 (where the products' error terms
-//      underflow) take the exact 128-bit integer decision; +-0 return
-//      themselves.
-__device__ __forceinline__ float cbrt_cr(float x) {
-  // magnitude below 2^-100, zeros included (the sign bit shifted out)
-  if ((__float_as_uint(x) << 1) < (0x0d800000u << 1))
-    return cbrt_tiny(x);
+//      below a power of two is taken care of).
+// It returns y.hi and whether that is settled; it is not for near-ties
+// (about one input in 2^13) and x < 2^-100 (where the products' error terms
+// underflow; zeros included), which cbrt_slow decides exactly (128-bit
+// integer test, CUDA's cbrtf as the first guess for the tiny inputs).
+__device__ __forceinline__ float cbrt_fast(float x, bool &settled) {
   const float y0 = ex2_approx(__fmul_rn(lg2_approx(x), 0.333333343f));
   const ff p = two_prod(y0, y0);
   const ff q = two_prod(y0, p.hi);
@@ -228,8 +228,20 @@ __device__ __forceinline__ float cbrt_cr(float x) {
   r = __fmaf_rn(-y0, p.lo, r);
   const float d = __fmul_rn(r, rcp_approx(__fmul_rn(3.0f, p.hi)));
   const ff y = quick_two_sum(y0, d);
-  if (__fmaf_rn(y.lo, 1.0001220703125f, y.hi) == y.hi) return y.hi;
-  return cbrt_round_exact(x, y.hi);
+  // x >= 2^-100 (x is not negative here; zeros fail the test)
+  settled = x >= 7.8886090522101181e-31f && __fmaf_rn(y.lo, 1.0001220703125f, y.hi) == y.hi;
+  return y.hi;
+}
+
+__device__ __noinline__ float cbrt_slow(float x, float y) {
+  if ((__float_as_uint(x) << 1) < (0x0d800000u << 1)) return cbrt_tiny(x);
+  return cbrt_round_exact(x, y);
+}
+
+__device__ __forceinline__ float cbrt_cr(float x) {
+  bool settled;
+  const float y = cbrt_fast(x, settled);
+  return settled ? y : cbrt_slow(x, y);
 }
 
 // ---------------------------------------------------------------------------
@@ -240,6 +252,16 @@ __device__ __forceinline__ float clamp01(float v) {
   if (v < 0.0f) return 0.0f;
   if (v > 1.0f) return 1.0f;
   return v;
+}
+
+// clamp01(fma(a, b, c)) in one instruction (the .sat form clamps the
+// rounded result to [0, 1]; a NaN, which the finite operands here never
+// give, would become 0, and -0 is equivalent downstream: the EOTF maps both
+// zeros to +0).
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float r;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // (float)n / d correctly rounded without a division, for d = 219 k or
@@ -265,11 +287,13 @@ __device__ __forceinline__ float eotf_lookup(const float2 *__restrict__ P, float
   return __fmaf_rn(f, e.y, e.x);
 }
 
-// Linear RGB -> XYB with the make-positive affine.
+// Linear RGB -> XYB with the make-positive affine.  The three cube roots
+// share one branch to their rare slow paths.
 __device__ __forceinline__ void pixel_xyb(const Pix &p, const float cb[3], float r,
                                           float g, float b, float &X, float &Y,
                                           float &B) {
-  float c[3];
+  float m[3], root[3];
+  bool ok[3];
 #pragma unroll
   for (int i = 0; i < 3; ++i) {
     float t0 = __fmul_rn(p.opsin[3 * i + 0], r);
@@ -277,9 +301,17 @@ __device__ __forceinline__ void pixel_xyb(const Pix &p, const float cb[3], float
     float t2 = __fmul_rn(p.opsin[3 * i + 2], b);
     float s = __fadd_rn(__fadd_rn(t0, t1), t2);
     s = __fadd_rn(s, p.bias[i]);
-    s = s < 0.0f ? 0.0f : s;
-    c[i] = __fsub_rn(cbrt_cr(s), cb[i]);
+    m[i] = s < 0.0f ? 0.0f : s;
+    root[i] = cbrt_fast(m[i], ok[i]);
   }
+  if (!(ok[0] && ok[1] && ok[2])) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+      if (!ok[i]) root[i] = cbrt_slow(m[i], root[i]);
+  }
+  float c[3];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) c[i] = __fsub_rn(root[i], cb[i]);
   float x = __fmul_rn(0.5f, __fsub_rn(c[0], c[1]));
   float y = __fmul_rn(0.5f, __fadd_rn(c[0], c[1]));
   X = __fadd_rn(__fmul_rn(x, p.sx), p.ox);
