@@ -13,6 +13,7 @@
 #include <cerrno>
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -349,10 +350,64 @@ static int default_batch(const Geom &g) {
   return (int)b;
 }
 
+// A positive finite float as X 2^e, X an integer below 2^24.
+static void split_float(float v, uint64_t &X, int &e) {
+  uint32_t b;
+  std::memcpy(&b, &v, sizeof(b));
+  const uint32_t be = (b >> 23) & 0xffu, m = b & 0x7fffffu;
+  X = be ? (m | 0x800000u) : m;
+  e = be ? (int)be - 150 : -149;
+}
+
+// Sign of (M 2^f)^3 - X 2^g, exact in 128-bit integers (M < 2^26, X < 2^24).
+static int cube_vs(uint64_t M, int f, uint64_t X, int g) {
+  const unsigned __int128 c = (unsigned __int128)(M * M) * M;  // below 2^78
+  const int d = 3 * f - g;
+  if (d >= 0) {
+    if (d >= 24) return 1;  // c >= 1 and X < 2^24
+    const unsigned __int128 l = c << d;
+    return l > X ? 1 : (l < X ? -1 : 0);
+  }
+  if (-d >= 104) return -1;  // X >= 1: X 2^-d >= 2^104 > c
+  const unsigned __int128 r = (unsigned __int128)X << (-d);
+  return c > r ? 1 : (c < r ? -1 : 0);
+}
+
+// Correctly rounded cube root of a finite float on the host (for the three
+// cbrt(bias_i) the XYB conversion subtracts): the double cube root rounded
+// to float is an ulp or so off at most, and the exact comparisons of x with
+// the cubes of the midpoints to the neighbouring floats move it to the
+// nearest one (below a power of two the lower neighbour is half as far).
+static float cbrt_rn_host(float x) {
+  if (x == 0.0f || !std::isfinite(x)) return x;
+  if (x < 0.0f) return -cbrt_rn_host(-x);
+  uint64_t X;
+  int g;
+  split_float(x, X, g);
+  float y = (float)std::cbrt((double)x);
+  for (int it = 0; it < 8; ++it) {
+    uint64_t Y;
+    int e;
+    split_float(y, Y, e);
+    if (cube_vs(2 * Y + 1, e - 1, X, g) < 0) {  // x beyond the upper midpoint's cube
+      y = std::nextafter(y, HUGE_VALF);
+      continue;
+    }
+    const bool at_floor = Y == 0x800000u && e > -149;
+    if (cube_vs(at_floor ? 4 * Y - 1 : 2 * Y - 1, at_floor ? e - 2 : e - 1, X, g) > 0) {
+      y = std::nextafter(y, 0.0f);  // x below the lower midpoint's cube
+      continue;
+    }
+    break;
+  }
+  return y;
+}
+
 void ss2::build_pix(const double *params, Pix &p) {
   build_yuv(p.yuv);
   for (int i = 0; i < 9; ++i) p.opsin[i] = (float)params[kPOpsin + i];
   for (int i = 0; i < 3; ++i) p.bias[i] = (float)params[kPBias + i];
+  for (int i = 0; i < 3; ++i) p.cbias[i] = cbrt_rn_host(p.bias[i]);
   p.sx = (float)params[kPAffine + 0];
   p.ox = (float)params[kPAffine + 1];
   p.oy = (float)params[kPAffine + 2];

@@ -130,8 +130,13 @@ __device__ __forceinline__ int stage_sample(const unsigned char *p) {
 // 16384 x 16384 samples and the byte offset of a V sample stays below
 // 2 x 1.5 x 2^28; each scale's XYB block is reached from a 64-bit base and
 // its six planes lie within 6 x 2^28 floats of it.
+//
+// Four blocks per SM (up to 64 registers): at five (48 registers) the loop
+// spilled a register pair to local memory (0.78 M spill stores and 1.04 M
+// spill loads, in warp instructions, per launch over four 4K frames), which
+// cost more than the fifth block gained.
 template <int BPS, int SX, int SY, bool DBG>
-__global__ void __launch_bounds__(kPyrThreads, 5)
+__global__ void __launch_bounds__(kPyrThreads, 4)
     k_pyramid(Geom g, Pix px, PyrTabs tabs, PyrStage ps, const uint8_t *__restrict__ ref,
               const uint8_t *__restrict__ dis, float *__restrict__ X,
               float *__restrict__ lin_dbg) {
@@ -141,7 +146,6 @@ __global__ void __launch_bounds__(kPyrThreads, 5)
   unsigned char *stage = psm + sizeof(float) * 6 * kLvl1;           // scales 0-1 ...
   float(*Lr)[kLvlRest] = reinterpret_cast<float(*)[kLvlRest]>(stage);  // ... then 2-5
   float *ntab = reinterpret_cast<float *>(stage + SG::union_bytes);
-  float *cb_s = ntab + (BPS == 1 ? 512 : 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int frame = blockIdx.z;
   const int tx0 = blockIdx.x * kPT, ty0 = blockIdx.y * kPT;
@@ -185,8 +189,7 @@ __global__ void __launch_bounds__(kPyrThreads, 5)
   };
   stage_rows(0);
 
-  // cbrt(bias_i) and the 8-bit normalisation tables, once per block
-  if (threadIdx.x < 3) cb_s[threadIdx.x] = cbrt_cr(px.bias[threadIdx.x]);
+  // the 8-bit normalisation tables, once per block
   if (BPS == 1 && tabs.ynorm) {
     for (int i = threadIdx.x; i < 256; i += kPyrThreads) {
       ntab[i] = __ldg(tabs.ynorm + i);
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(kPyrThreads, 5)
   __syncthreads();
   float cb[3];
 #pragma unroll
-  for (int i = 0; i < 3; ++i) cb[i] = cb_s[i];
+  for (int i = 0; i < 3; ++i) cb[i] = px.cbias[i];
 
   const int k = 1 << (g.depth - 8);
   const float dy = (float)(219 * k), dc = (float)(224 * k);
@@ -959,11 +962,11 @@ cudaError_t launch_cbrt(const float *x, float *y, long long n, cudaStream_t st) 
 }
 
 // Dynamic shared memory of one instantiation: the scale-1 tiles, the region
-// shared by the staging buffers and the scale 2-5 tiles, the 8-bit
-// normalisation tables and cbrt(bias).
+// shared by the staging buffers and the scale 2-5 tiles, and the 8-bit
+// normalisation tables.
 template <int BPS, int SX, int SY>
 constexpr int pyr_smem() {
-  return (int)sizeof(float) * (6 * kLvl1 + (BPS == 1 ? 512 : 0) + 4) +
+  return (int)sizeof(float) * (6 * kLvl1 + (BPS == 1 ? 512 : 0)) +
          StageGeo<BPS, SX, SY>::union_bytes;
 }
 

@@ -78,6 +78,7 @@ struct Pix {
   float yuv[4];        // cr->R', cb->G' (magnitude), cr->G' (magnitude), cb->B'
   float opsin[9];
   float bias[3];
+  float cbias[3];      // cbrt(bias[i]), correctly rounded (set on the host)
   float sx, ox, oy, sb, ob;
   float c2;
   float iir_c2[3];     // 2 cos(w_k)
