@@ -727,10 +727,11 @@ def run_msssim(args, ws, rank, local):
         "clocks": clk,
         "e2e": {"value": e2e_fps, "unit": "frames/s",
                 "h2d_bytes_per_step": int(wl.ref.nbytes + wl.dis.nbytes),
-                "d2h_bytes_per_step": 8 * n},
+                "d2h_bytes_per_step": 8 * n * ms.planes},
         "gpu_launches": sum(prof[k][1] for k in ms.KERNELS),
         "cpu_baseline": cpu,
-        "scores_head": [float(x) for x in scores[:3]],
+        # per frame: Y, Cb, Cr
+        "scores_head": [[float(v) for v in np.atleast_1d(x)] for x in scores[:3]],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
