@@ -157,6 +157,17 @@ int ss2_debug_linear(ss2_ctx *ctx, const void *ref, const void *dis, int scale,
 int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream);
 
 /*
+ * ss2_debug_cbrt_host — the host's correctly rounded cube root, the one that
+ * sets the three cbrt(bias_i) constants of the XYB conversion (Research-1363,
+ * Finding 2) whenever parameters are set.  x, y: HOST arrays of n floats
+ * (may alias); every finite input, of either sign, gets cbrt rounded to
+ * nearest (odd: cbrt(-x) = -cbrt(x), zeros keep their sign); infinities and
+ * NaN are copied.  Needs no GPU.  Returns -EINVAL for a NULL array with
+ * n > 0 or a negative n.
+ */
+int ss2_debug_cbrt_host(const float *x, float *y, long long n);
+
+/*
  * ss2_profile_begin / ss2_profile_end — per-kernel device timing.  Between
  * the two calls every kernel launch of the context is bracketed by a pair of
  * CUDA events on its launching stream.  ss2_profile_end waits for those

@@ -914,6 +914,12 @@ SS2_API int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream) 
   return 0;
 }
 
+SS2_API int ss2_debug_cbrt_host(const float *x, float *y, long long n) {
+  if (n < 0 || (n > 0 && (!x || !y))) return fail(SS2_EINVAL, "bad cbrt arguments");
+  for (long long i = 0; i < n; ++i) y[i] = cbrt_rn_host(x[i]);
+  return 0;
+}
+
 SS2_API int ss2_debug_wait_probe(unsigned spins, void *stream) {
   int dev = 0;
   if (check_device(&dev)) return t_err;

@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
             L.ss2_debug_linear.restype = i
             L.ss2_debug_cbrt.argtypes = [vp, vp, ctypes.c_longlong, vp]
             L.ss2_debug_cbrt.restype = i
+            L.ss2_debug_cbrt_host.argtypes = [vp, vp, ctypes.c_longlong]
+            L.ss2_debug_cbrt_host.restype = i
             L.ss2_profile_begin.argtypes = [vp]
             L.ss2_profile_begin.restype = i
             L.ss2_profile_end.argtypes = [vp, vp, vp]
@@ -170,6 +172,15 @@ def debug_cbrt(x, out=None, stream=None):
     out = torch.empty_like(x) if out is None else out
     _check(lib().ss2_debug_cbrt(x.data_ptr(), out.data_ptr(), x.numel(), _stream_handle(stream)))
     return out
+
+
+def debug_cbrt_host(x: np.ndarray) -> np.ndarray:
+    """The host's cube root (the one behind the cbrt(bias) constants)
+    applied to a float32 array; needs no GPU."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    _check(lib().ss2_debug_cbrt_host(x.ctypes.data, y.ctypes.data, x.size))
+    return y
 
 
 def score_noalloc(width: int, height: int, bitdepth: int, chroma: int, ref, dis,

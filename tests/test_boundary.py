@@ -109,3 +109,31 @@ def test_binding_has_no_fallback(monkeypatch, built):
     with pytest.raises(RuntimeError):
         ss2.lib()
     _ = ctypes
+
+
+def test_host_cube_root_matches_oracle(L):
+    """The host cube root behind the cbrt(bias) constants: bitwise equal to
+    the oracle's correctly rounded cbrtf on a sweep of bit patterns of both
+    signs (subnormals, binade edges, powers of two and their neighbours,
+    random finite floats, the default biases), with zeros keeping their sign
+    and non-finite inputs copied."""
+    from ssimulacra2_image_scoring_gb300 import ss2
+    rng = np.random.default_rng(7)
+    bits = [rng.integers(0, 0x7f800000, 200_000, dtype=np.uint32)]            # random finite
+    bits.append(np.arange(0, 1 << 16, dtype=np.uint32))                       # subnormals
+    e = np.arange(1, 255, dtype=np.uint32) << 23
+    bits += [e, e + 1, e - 1, e | 0x7fffff]                                   # binade edges
+    bits.append(np.arange(0x3f800000 - 50_000, 0x3f800000 + 50_000, dtype=np.uint32))
+    b = np.concatenate(bits)
+    x = np.concatenate([b, b | np.uint32(0x80000000)]).view(np.float32)
+    x = np.concatenate([x, np.array([0.0, -0.0, np.inf, -np.inf, np.nan], np.float32)])
+    bias = oracle.default_params()[oracle.P_BIAS:oracle.P_BIAS + 3].astype(np.float32)
+    x = np.concatenate([x, bias, -bias])
+    got = ss2.debug_cbrt_host(x)
+    fin = np.isfinite(x)
+    want = oracle.cbrtf_cr_array(x[fin])
+    assert np.array_equal(got[fin].view(np.uint32), want.view(np.uint32))
+    assert np.array_equal(got[~fin].view(np.uint32), x[~fin].view(np.uint32))
+    zeros = x == 0
+    assert np.array_equal(np.signbit(got[zeros]), np.signbit(x[zeros]))
+    assert L.ss2_debug_cbrt_host(None, None, 1) == -22
