@@ -295,37 +295,66 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// One 4-D map over a stack of fp32 planes: (column, row, plane, frame), boxes
-// of bc x br x bp x 1, zero fill outside the tensor.
-static int encode_stack(CUtensorMap *m, float *base, int ws, int hs, int nplanes, int batch,
-                        long long pitch, long long plane, long long frame_stride, int bc, int br,
-                        int bp) {
+// One tiled map over fp32 data of the given rank: dims[0] is the innermost
+// extent, strides[i] the byte stride of dims[i + 1]; zero fill outside the
+// tensor.
+static int encode_tiled(CUtensorMap *m, float *base, int rank, const cuuint64_t *dims,
+                        const cuuint64_t *strides, const cuuint32_t *box,
+                        CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return fail(SS2_EIO, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[4] = {(cuuint64_t)ws, (cuuint64_t)hs, (cuuint64_t)nplanes,
-                              (cuuint64_t)batch};
-  const cuuint64_t strides[3] = {(cuuint64_t)pitch * 4, (cuuint64_t)plane * 4,
-                                 (cuuint64_t)frame_stride * 4};
-  const cuuint32_t box[4] = {(cuuint32_t)bc, (cuuint32_t)br, (cuuint32_t)bp, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, base, dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SS2_EIO, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return 0;
 }
 
+// (column, row, plane, frame) over a stack of planes, boxes of bc x br x bp.
+static int encode_stack(CUtensorMap *m, float *base, int ws, int hs, int nplanes, int batch,
+                        long long pitch, long long plane, long long frame_stride, int bc, int br,
+                        int bp) {
+  const cuuint64_t dims[4] = {(cuuint64_t)ws, (cuuint64_t)hs, (cuuint64_t)nplanes,
+                              (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)pitch * 4, (cuuint64_t)plane * 4,
+                                 (cuuint64_t)frame_stride * 4};
+  const cuuint32_t box[4] = {(cuuint32_t)bc, (cuuint32_t)br, (cuuint32_t)bp, 1};
+  return encode_tiled(m, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// (float of the quad row, row, channel, frame) over the interleaved quads of
+// mu1, mu2, s11, s22 (a quad row is 4 x pitch floats, a channel 4 x plane):
+// boxes of bf floats x br rows.
+static int encode_quads(CUtensorMap *m, float *base, int ws, int hs, int batch, long long pitch,
+                        long long plane, long long frame_stride, int bf, int br,
+                        CUtensorMapSwizzle swizzle) {
+  const cuuint64_t dims[4] = {4 * (cuuint64_t)ws, (cuuint64_t)hs, 3, (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)pitch * 16, (cuuint64_t)plane * 16,
+                                 (cuuint64_t)frame_stride * 4};
+  const cuuint32_t box[4] = {(cuuint32_t)bf, (cuuint32_t)br, 1, 1};
+  return encode_tiled(m, base, 4, dims, strides, box, swizzle);
+}
+
 int ss2::encode_maps(const Geom &g, float *X, float *H, int batch, PlaneMaps &m) {
   std::memset(&m, 0, sizeof(m));
   for (int s = 0; s < g.nscales; ++s) {
-    float *xb = X + g.xoff[s], *hb = H + g.hoff[s];
+    float *xb = X + g.xoff[s], *hb = H + g.hoff[s], *sb = hb + 12 * g.plane[s];
     const int ws = g.ws[s], hs = g.hs[s];
-    if (encode_stack(&m.x[s], xb, ws, hs, 6, batch, g.pitch[s], g.plane[s], g.x_fs, kBoxCols,
-                     kBoxRows, 1) ||
-        encode_stack(&m.h[s], hb, ws, hs, 3 * kNq, batch, g.pitch[s], g.plane[s], g.h_fs,
-                     kBoxCols, kBoxRows, 1) ||
-        encode_stack(&m.hv[s], hb, ws, hs, 3 * kNq, batch, g.pitch[s], g.plane[s], g.h_fs,
-                     kVCols, kVRows, kNq))
+    const long long pitch = g.pitch[s], plane = g.plane[s];
+    // the horizontal pass stores a box row of 8 quads (128 bytes) per image
+    // row, swizzled so that its lanes (one row each) write without bank
+    // conflicts; the vertical pass loads rows of 32 quads, unswizzled (its
+    // lanes read consecutive 16-byte units)
+    if (encode_stack(&m.h.x[s], xb, ws, hs, 6, batch, pitch, plane, g.x_fs, kBoxCols, kBoxRows,
+                     1) ||
+        encode_quads(&m.h.q4[s], hb, ws, hs, batch, pitch, plane, g.h_fs, 4 * kBoxCols,
+                     kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        encode_stack(&m.h.s1[s], sb, ws, hs, 3, batch, pitch, plane, g.h_fs, kBoxCols, kBoxRows,
+                     1) ||
+        encode_quads(&m.v.vq4[s], hb, ws, hs, batch, pitch, plane, g.h_fs, 4 * kVCols, kVRows,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        encode_stack(&m.v.vs1[s], sb, ws, hs, 3, batch, pitch, plane, g.h_fs, kVCols, kVRows, 1))
       return t_err;
   }
   return 0;
@@ -871,14 +900,32 @@ SS2_API int ss2_debug_planes(ss2_ctx *ctx, const void *ref, const void *dis, int
                            L.X + g.xoff[scale] + p * g.plane[scale], pitch_b,
                            ws * sizeof(float), hs, cudaMemcpyDeviceToHost, st),
          "plane read-back");
-  if (hblur)
-    for (int p = 0; p < 3 * kNq; ++p)
-      CU(cudaMemcpy2DAsync(hblur + p * ws * hs, ws * sizeof(float),
-                           L.H + g.hoff[scale] + p * g.plane[scale], pitch_b,
+  // blurred planes, per channel c: mu1, mu2, s11, s22 interleaved as quads
+  // (de-interleaved on the host below), then s12
+  std::vector<float> quads;
+  if (hblur) {
+    const size_t plane = (size_t)g.plane[scale];
+    quads.resize(3 * 4 * plane);
+    CU(cudaMemcpyAsync(quads.data(), L.H + g.hoff[scale], quads.size() * sizeof(float),
+                       cudaMemcpyDeviceToHost, st),
+       "quad read-back");
+    for (int c = 0; c < 3; ++c)
+      CU(cudaMemcpy2DAsync(hblur + (c * kNq + 4) * ws * hs, ws * sizeof(float),
+                           L.H + g.hoff[scale] + (12 + c) * plane, pitch_b,
                            ws * sizeof(float), hs, cudaMemcpyDeviceToHost, st),
          "plane read-back");
+  }
   if (enqueue_err_readback(ctx, st)) return t_err;
   CU(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  if (hblur) {
+    const size_t pitch = (size_t)g.pitch[scale], plane = (size_t)g.plane[scale];
+    for (int c = 0; c < 3; ++c)
+      for (int q = 0; q < 4; ++q)
+        for (size_t y = 0; y < hs; ++y)
+          for (size_t x = 0; x < ws; ++x)
+            hblur[(c * kNq + q) * ws * hs + y * ws + x] =
+                quads[c * 4 * plane + (y * pitch + x) * 4 + q];
+  }
   return check_err_word(ctx, st);
 }
 

@@ -449,7 +449,8 @@ __device__ __forceinline__ void res_zero(Res3 &r) {
 // samples 5 ahead and 5 behind the step (the window of radius R = 4 has
 // taps at +-(R+1)), kept in rolling registers.  The five quantities
 // (x1, x2, x1^2, x2^2, x1 x2) are formed in registers.  The chunk's 5 x 8
-// outputs per lane go to a ring of kHOutBufs shared tiles and leave with TMA
+// outputs per lane go to a ring of kHOutBufs shared tiles (mu1, mu2, s11,
+// s22 as one float4 per pixel, s12 on its own) and leave with two TMA
 // stores (clipped to the image), so global traffic is whole boxes both ways;
 // a tile is rewritten once the store issued from it kHOutBufs chunks earlier
 // has read it.  Every mbarrier wait is bounded; a timeout raises
@@ -466,20 +467,24 @@ constexpr int kHSlots = 4;
 constexpr int kHOutBufs = 3;
 constexpr int kHBox = kBoxRows * kBoxCols;  // floats in one plane box (1 KB)
 
+// Output tiles: per buffer, the quads (mu1, mu2, s11, s22) of the 32 x 8
+// pixels in the 128-byte-swizzled order their TMA map expects (16-byte unit
+// swz128(row * 8 + col)), then the s12 tile.
 struct HWarpSmem {
-  float in[kHSlots][2][kHBox];   // [slot][x1 | x2][row * 8 + col]
-  float out[kHOutBufs][kNq][kHBox];  // [buffer][quantity][row * 8 + col]
+  float quad[kHOutBufs][4 * kHBox];  // [buffer][swizzled (row, col), quantity 0..3]
+  float s12[kHOutBufs][kHBox];       // [buffer][row * 8 + col]
+  float in[kHSlots][2][kHBox];       // [slot][x1 | x2][row * 8 + col]
 };
-static_assert(sizeof(HWarpSmem) % 128 == 0, "every TMA box starts on 128 bytes");
-// warp tiles, then the mbarriers; +128 to align the base for TMA
-constexpr int kHSmemBytes = kHWarps * (int)sizeof(HWarpSmem) + kHWarps * kHSlots * 8 + 128;
+static_assert(sizeof(HWarpSmem) % 1024 == 0, "every quad tile starts on 1024 bytes");
+// warp tiles, then the mbarriers; +1024 to align the base for the swizzle
+constexpr int kHSmemBytes = kHWarps * (int)sizeof(HWarpSmem) + kHWarps * kHSlots * 8 + 1024;
 
 __global__ void __launch_bounds__(kHWarps * 32)
-    k_hblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, int nframes,
+    k_hblur(Geom g, Pix px, const __grid_constant__ HMaps maps, int nframes,
             int *__restrict__ err) {
   extern __shared__ __align__(16) unsigned char hsm_raw[];
   unsigned char *hsm = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(hsm_raw) + 127) & ~uintptr_t(127));
+      (reinterpret_cast<uintptr_t>(hsm_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // units in scale-major order over the batch (every frame's scale-0 rows
   // first): the longest walks start first and the shortest fill the tail
@@ -496,7 +501,8 @@ __global__ void __launch_bounds__(kHWarps * 32)
   HWarpSmem &sm = reinterpret_cast<HWarpSmem *>(hsm)[warp];
   uint64_t *bar = reinterpret_cast<uint64_t *>(hsm + kHWarps * sizeof(HWarpSmem)) + warp * kHSlots;
   const CUtensorMap *mx = &maps.x[s];
-  const CUtensorMap *mh = &maps.h[s];
+  const CUtensorMap *mq = &maps.q4[s];
+  const CUtensorMap *ms = &maps.s1[s];
 
   if (lane == 0) {
     for (int i = 0; i < kHSlots; ++i) mbar_init(&bar[i], 1);
@@ -600,18 +606,20 @@ __global__ void __launch_bounds__(kHWarps * 32)
     if (lane == 0) bulk_wait_read<kHOutBufs - 1>();
     __syncwarp();
     const int ob = k % kHOutBufs;
+    // lane = row: column j's quad is 16-byte unit row * 8 + j of the tile
+    // (eight lanes of a phase hit eight different units of their lines)
+    float4 *dq = reinterpret_cast<float4 *>(sm.quad[ob]);
 #pragma unroll
-    for (int q = 0; q < kNq; ++q) {
-      float4 *d = reinterpret_cast<float4 *>(&sm.out[ob][q][lane * kBoxCols]);
-      d[0] = make_float4(o[q][0], o[q][1], o[q][2], o[q][3]);
-      d[1] = make_float4(o[q][4], o[q][5], o[q][6], o[q][7]);
-    }
+    for (int j = 0; j < kBoxCols; ++j)
+      dq[swz128(lane * kBoxCols + j)] = make_float4(o[0][j], o[1][j], o[2][j], o[3][j]);
+    float4 *ds = reinterpret_cast<float4 *>(&sm.s12[ob][lane * kBoxCols]);
+    ds[0] = make_float4(o[4][0], o[4][1], o[4][2], o[4][3]);
+    ds[1] = make_float4(o[4][4], o[4][5], o[4][6], o[4][7]);
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-#pragma unroll
-      for (int q = 0; q < kNq; ++q)
-        tma_store_4d(mh, sm.out[ob][q], k * kBoxCols, row0, c * kNq + q, frame);
+      tma_store_4d(mq, sm.quad[ob], 4 * k * kBoxCols, row0, c, frame);
+      tma_store_4d(ms, sm.s12[ob], k * kBoxCols, row0, c, frame);
       bulk_commit();
     }
   }
@@ -700,8 +708,9 @@ __device__ __forceinline__ void ssim_edge_terms(const Pix &px, float mu1, float 
 }
 
 // Column walkers.  One warp per 32 columns of one (frame, scale, channel);
-// lane = column.  TMA brings 8-row chunks of the channel's five blurred
-// planes (one 32 x 8 x 5 box) into a 3-slot ring; the slot of chunk k - 1 is
+// lane = column.  TMA brings 8-row chunks of the channel's blurred planes
+// (a 32 x 8 box of quads and one of s12) into a 3-slot ring, so a tap is
+// one 16-byte and one 4-byte shared load; the slot of chunk k - 1 is
 // refilled with chunk k + 2 as soon as its last row has been read (after
 // step 5 of chunk k), six steps before that chunk is first needed.  The two
 // XYB rows each step needs are loaded from global memory one chunk ahead
@@ -713,14 +722,17 @@ constexpr int kVWarps = 4;
 constexpr int kVSlots = 3;
 constexpr int kVBox = kVRows * kVCols;          // floats per plane box (1 KB)
 
+// Per slot: the quads (mu1, mu2, s11, s22) of the 8 x 32 pixels, then the
+// s12 box.
 struct VWarpSmem {
-  float h[kVSlots][kNq][kVBox];   // [slot][quantity][row * 32 + col]
+  float quad[kVSlots][4 * kVBox];  // [slot][(row * 32 + col) * 4 + quantity]
+  float s12[kVSlots][kVBox];       // [slot][row * 32 + col]
 };
-static_assert(sizeof(VWarpSmem) == 15360, "per-warp tile");
+static_assert(sizeof(VWarpSmem) == 15360, "per-warp tiles");
 constexpr int kVSmemBytes = kVWarps * (int)sizeof(VWarpSmem) + kVWarps * 4 * 8 + 1024;
 
 __global__ void __launch_bounds__(kVWarps * 32)
-    k_vblur(Geom g, Pix px, const __grid_constant__ PlaneMaps maps, const float *__restrict__ X,
+    k_vblur(Geom g, Pix px, const __grid_constant__ VMaps maps, const float *__restrict__ X,
             int nframes, float2 *__restrict__ part, int *__restrict__ err) {
   extern __shared__ __align__(16) unsigned char vsm_raw[];
   unsigned char *vsm = reinterpret_cast<unsigned char *>(
@@ -742,7 +754,12 @@ __global__ void __launch_bounds__(kVWarps * 32)
   const int nchunk = (h + kVRows - 1) / kVRows;
   VWarpSmem &sm = reinterpret_cast<VWarpSmem *>(vsm)[warp];
   uint64_t *hbar = reinterpret_cast<uint64_t *>(vsm + kVWarps * sizeof(VWarpSmem)) + warp * 4;
-  const CUtensorMap *mh = &maps.hv[s];
+  const CUtensorMap *mq = &maps.vq4[s];
+  const CUtensorMap *ms = &maps.vs1[s];
+  // this lane's quad of row r of a slot (rows of 32 quads, unswizzled)
+  auto quad_at = [&](int slot, int r) -> float4 {
+    return reinterpret_cast<const float4 *>(sm.quad[slot])[r * kVCols + lane];
+  };
   // XYB rows of this lane's column (pitch padding keeps every lane in bounds)
   const long long pitch = g.pitch[s];
   const float *x1p = X + (long long)frame * g.x_fs + g.xoff[s] + c * g.plane[s] + col0 + lane;
@@ -758,7 +775,8 @@ __global__ void __launch_bounds__(kVWarps * 32)
   auto issue_h = [&](int m) {
     const int slot = slot_of(m);
     mbar_arrive_expect_tx(&hbar[slot], kNq * kVBox * (int)sizeof(float));
-    tma_load_4d(sm.h[slot][0], mh, &hbar[slot], col0, m * kVRows, c * kNq, frame);
+    tma_load_4d(sm.quad[slot], mq, &hbar[slot], 4 * col0, m * kVRows, c, frame);
+    tma_load_4d(sm.s12[slot], ms, &hbar[slot], col0, m * kVRows, c, frame);
   };
   if (lane == 0)
     for (int m = -1; m <= 1 && m <= nchunk; ++m) issue_h(m);
@@ -791,9 +809,10 @@ __global__ void __launch_bounds__(kVWarps * 32)
   // warm-up steps producing Y[-4] .. Y[-1]: rows 0..3 ahead, zeros behind
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    const float4 a = quad_at(slot_of(0), j);
+    const float in[kNq] = {a.x, a.y, a.z, a.w, sm.s12[slot_of(0)][j * kVCols + lane]};
 #pragma unroll
-    for (int q = 0; q < kNq; ++q)
-      res_step(r[q], px, __fadd_rn(sm.h[slot_of(0)][q][j * kVCols + lane], 0.0f));
+    for (int q = 0; q < kNq; ++q) res_step(r[q], px, __fadd_rn(in[q], 0.0f));
   }
 
   for (int k = 0; k < nchunk; ++k) {
@@ -807,14 +826,14 @@ __global__ void __launch_bounds__(kVWarps * 32)
 #pragma unroll
     for (int j = 0; j < kVRows; ++j) {
       // ahead row 8k + j + 4, behind row 8k + j - 6
-      const float *ha = j < 4 ? &sm.h[sk][0][(j + 4) * kVCols + lane]
-                              : &sm.h[sn][0][(j - 4) * kVCols + lane];
-      const float *hb = j < 6 ? &sm.h[sp][0][(j + 2) * kVCols + lane]
-                              : &sm.h[sk][0][(j - 6) * kVCols + lane];
+      const int sa = j < 4 ? sk : sn, ra = j < 4 ? j + 4 : j - 4;
+      const int sb = j < 6 ? sp : sk, rb = j < 6 ? j + 2 : j - 6;
+      const float4 qa = quad_at(sa, ra), qb = quad_at(sb, rb);
+      const float ina[kNq] = {qa.x, qa.y, qa.z, qa.w, sm.s12[sa][ra * kVCols + lane]};
+      const float inb[kNq] = {qb.x, qb.y, qb.z, qb.w, sm.s12[sb][rb * kVCols + lane]};
       float o[kNq];
 #pragma unroll
-      for (int q = 0; q < kNq; ++q)
-        o[q] = res_step(r[q], px, __fadd_rn(ha[q * kVBox], hb[q * kVBox]));
+      for (int q = 0; q < kNq; ++q) o[q] = res_step(r[q], px, __fadd_rn(ina[q], inb[q]));
       if (j == 5) {
         // chunk k - 1 is read for the last time: refill its slot with k + 2
         // (the reads are ordered before the async-proxy refill by a proxy
@@ -1036,7 +1055,7 @@ cudaError_t launch_hblur(const Geom &g, const Pix &px, const PlaneMaps &maps, in
   }
   const int units = g.hunit_off[g.nscales];
   const dim3 grid((units * nframes + kHWarps - 1) / kHWarps);
-  k_hblur<<<grid, kHWarps * 32, kHSmemBytes, st>>>(g, px, maps, nframes, err);
+  k_hblur<<<grid, kHWarps * 32, kHSmemBytes, st>>>(g, px, maps.h, nframes, err);
   return cudaGetLastError();
 }
 
@@ -1053,7 +1072,7 @@ cudaError_t launch_vblur(const Geom &g, const Pix &px, const PlaneMaps &maps, co
   }
   const int warps = g.vwarp_off[g.nscales];
   const dim3 grid((warps * nframes + kVWarps - 1) / kVWarps);
-  k_vblur<<<grid, kVWarps * 32, kVSmemBytes, st>>>(g, px, maps, X, nframes, part, err);
+  k_vblur<<<grid, kVWarps * 32, kVSmemBytes, st>>>(g, px, maps.v, X, nframes, part, err);
   return cudaGetLastError();
 }
 

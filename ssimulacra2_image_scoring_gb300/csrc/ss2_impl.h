@@ -45,15 +45,33 @@ struct Geom {
   int vwarp_off[kMaxScales + 1];   // prefix of 3 * nw[s]            (vertical warps)
 };
 
-// TMA descriptors of the plane stacks, one per scale.  x[s] views the XYB
-// block as a 4-D tensor (column, row, plane 0..5, frame), h[s] / hv[s] the
-// horizontally blurred block (column, row, plane 0..14, frame).
-//   x, h:  8-column x 32-row boxes (row walkers of the horizontal pass)
-//   hv:    32-column x 8-row x 5-plane boxes (column walkers, one channel)
-struct PlaneMaps {
+// TMA descriptors, one per scale.  x[s] views the XYB block as a 4-D tensor
+// (column, row, plane 0..5, frame).  The horizontally blurred block of a
+// scale holds, per channel c, the quantities mu1, mu2, s11, s22 interleaved
+// (four floats per pixel: the "quad" rows, 4 x pitch floats each, channel c
+// at c * 4 * plane) and then, per channel, the s12 plane (at 12 * plane +
+// c * plane).  q4 / vq4 view the quads as a 4-D tensor (float of the quad
+// row, row, channel, frame), s1 / vs1 the s12 planes as (column, row,
+// channel, frame).
+//   x, s1:  8-column x 32-row boxes (row walkers of the horizontal pass)
+//   q4:     32-float (8-pixel) x 32-row boxes, 128-byte swizzled in shared
+//           memory (one box row is one 128-byte line)
+//   vq4:    128-float (32-pixel) x 8-row boxes, vs1: 32-column x 8-row
+//           boxes (column walkers, one channel)
+// Each pass gets only its own maps, which keeps the kernels' parameters
+// under 4 KB.
+struct HMaps {
   CUtensorMap x[kMaxScales];
-  CUtensorMap h[kMaxScales];
-  CUtensorMap hv[kMaxScales];
+  CUtensorMap q4[kMaxScales];
+  CUtensorMap s1[kMaxScales];
+};
+struct VMaps {
+  CUtensorMap vq4[kMaxScales];
+  CUtensorMap vs1[kMaxScales];
+};
+struct PlaneMaps {
+  HMaps h;
+  VMaps v;
 };
 constexpr int kBoxCols = 8, kBoxRows = 32;      // horizontal pass box
 constexpr int kVCols = 32, kVRows = 8;          // vertical pass box

@@ -92,6 +92,12 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void 
       : "memory");
 }
 
+// Offset, in 16-byte units, of 16-byte unit u of a tile whose box rows are
+// 128 bytes and which a TMA map with 128-byte swizzling moves (the tile
+// starting on 1024 bytes): within each row of eight units, the unit index is
+// XORed with the row's index modulo 8 (address bits 4-6 XOR bits 7-9).
+__device__ __forceinline__ int swz128(int u) { return u ^ ((u >> 3) & 7); }
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
