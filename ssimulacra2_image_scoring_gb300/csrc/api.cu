@@ -314,13 +314,13 @@ static int encode_tiled(CUtensorMap *m, float *base, int rank, const cuuint64_t 
 // (column, row, plane, frame) over a stack of planes, boxes of bc x br x bp.
 static int encode_stack(CUtensorMap *m, float *base, int ws, int hs, int nplanes, int batch,
                         long long pitch, long long plane, long long frame_stride, int bc, int br,
-                        int bp) {
+                        int bp, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   const cuuint64_t dims[4] = {(cuuint64_t)ws, (cuuint64_t)hs, (cuuint64_t)nplanes,
                               (cuuint64_t)batch};
   const cuuint64_t strides[3] = {(cuuint64_t)pitch * 4, (cuuint64_t)plane * 4,
                                  (cuuint64_t)frame_stride * 4};
   const cuuint32_t box[4] = {(cuuint32_t)bc, (cuuint32_t)br, (cuuint32_t)bp, 1};
-  return encode_tiled(m, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  return encode_tiled(m, base, 4, dims, strides, box, swizzle);
 }
 
 // (float of the quad row, row, channel, frame) over the interleaved quads of
@@ -342,16 +342,17 @@ int ss2::encode_maps(const Geom &g, float *X, float *H, int batch, PlaneMaps &m)
     float *xb = X + g.xoff[s], *hb = H + g.hoff[s], *sb = hb + 12 * g.plane[s];
     const int ws = g.ws[s], hs = g.hs[s];
     const long long pitch = g.pitch[s], plane = g.plane[s];
-    // the horizontal pass stores a box row of 8 quads (128 bytes) per image
-    // row, swizzled so that its lanes (one row each) write without bank
-    // conflicts; the vertical pass loads rows of 32 quads, unswizzled (its
-    // lanes read consecutive 16-byte units)
+    // the horizontal pass's lanes own one row each: its boxes are swizzled
+    // by their row width (8 floats = 32 bytes for XYB and s12, 8 quads =
+    // 128 bytes for the quads) so that those lanes read and write 16-byte
+    // units without bank conflicts; the vertical pass loads rows of 32
+    // quads, unswizzled (its lanes read consecutive 16-byte units)
     if (encode_stack(&m.h.x[s], xb, ws, hs, 6, batch, pitch, plane, g.x_fs, kBoxCols, kBoxRows,
-                     1) ||
+                     1, CU_TENSOR_MAP_SWIZZLE_32B) ||
         encode_quads(&m.h.q4[s], hb, ws, hs, batch, pitch, plane, g.h_fs, 4 * kBoxCols,
                      kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         encode_stack(&m.h.s1[s], sb, ws, hs, 3, batch, pitch, plane, g.h_fs, kBoxCols, kBoxRows,
-                     1) ||
+                     1, CU_TENSOR_MAP_SWIZZLE_32B) ||
         encode_quads(&m.v.vq4[s], hb, ws, hs, batch, pitch, plane, g.h_fs, 4 * kVCols, kVRows,
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
         encode_stack(&m.v.vs1[s], sb, ws, hs, 3, batch, pitch, plane, g.h_fs, kVCols, kVRows, 1))

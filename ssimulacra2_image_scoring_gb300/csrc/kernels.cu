@@ -472,8 +472,8 @@ constexpr int kHBox = kBoxRows * kBoxCols;  // floats in one plane box (1 KB)
 // swz128(row * 8 + col)), then the s12 tile.
 struct HWarpSmem {
   float quad[kHOutBufs][4 * kHBox];  // [buffer][swizzled (row, col), quantity 0..3]
-  float s12[kHOutBufs][kHBox];       // [buffer][row * 8 + col]
-  float in[kHSlots][2][kHBox];       // [slot][x1 | x2][row * 8 + col]
+  float s12[kHOutBufs][kHBox];       // [buffer][32-byte-swizzled (row, col)]
+  float in[kHSlots][2][kHBox];       // [slot][x1 | x2][32-byte-swizzled (row, col)]
 };
 static_assert(sizeof(HWarpSmem) % 1024 == 0, "every quad tile starts on 1024 bytes");
 // warp tiles, then the mbarriers; +1024 to align the base for the swizzle
@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kHWarps * 32)
   for (int p = 0; p < 2; ++p) {
     gm0[p] = make_float4(0.f, 0.f, 0.f, 0.f);
     gm1[p] = gm0[p];
-    g0[p] = *reinterpret_cast<const float4 *>(&sm.in[0][p][lane * kBoxCols]);
+    g0[p] = reinterpret_cast<const float4 *>(sm.in[0][p])[swz32(2 * lane)];
   }
   // warm-up steps producing Y[-4] .. Y[-1]: inputs x[0..3] ahead, zeros behind
   {
@@ -566,8 +566,8 @@ __global__ void __launch_bounds__(kHWarps * 32)
     float4 g1[2], gn[2];  // cols 8k+4..8k+7 and 8k+8..8k+11
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-      g1[p] = *reinterpret_cast<const float4 *>(&sm.in[sk][p][lane * kBoxCols + 4]);
-      gn[p] = *reinterpret_cast<const float4 *>(&sm.in[sk1][p][lane * kBoxCols]);
+      g1[p] = reinterpret_cast<const float4 *>(sm.in[sk][p])[swz32(2 * lane + 1)];
+      gn[p] = reinterpret_cast<const float4 *>(sm.in[sk1][p])[swz32(2 * lane)];
     }
     // slot k is free once every lane's reads of it are ordered before the
     // copy that refills it: the reads are generic-proxy accesses and the
@@ -612,9 +612,9 @@ __global__ void __launch_bounds__(kHWarps * 32)
 #pragma unroll
     for (int j = 0; j < kBoxCols; ++j)
       dq[swz128(lane * kBoxCols + j)] = make_float4(o[0][j], o[1][j], o[2][j], o[3][j]);
-    float4 *ds = reinterpret_cast<float4 *>(&sm.s12[ob][lane * kBoxCols]);
-    ds[0] = make_float4(o[4][0], o[4][1], o[4][2], o[4][3]);
-    ds[1] = make_float4(o[4][4], o[4][5], o[4][6], o[4][7]);
+    float4 *ds = reinterpret_cast<float4 *>(sm.s12[ob]);
+    ds[swz32(2 * lane)] = make_float4(o[4][0], o[4][1], o[4][2], o[4][3]);
+    ds[swz32(2 * lane + 1)] = make_float4(o[4][4], o[4][5], o[4][6], o[4][7]);
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {

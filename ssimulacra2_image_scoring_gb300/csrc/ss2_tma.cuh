@@ -98,6 +98,10 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void 
 // XORed with the row's index modulo 8 (address bits 4-6 XOR bits 7-9).
 __device__ __forceinline__ int swz128(int u) { return u ^ ((u >> 3) & 7); }
 
+// The same for box rows of 32 bytes under 32-byte swizzling: the two units
+// of a row swap when bit 2 of the row index is set (address bit 4 XOR bit 7).
+__device__ __forceinline__ int swz32(int u) { return u ^ ((u >> 3) & 1); }
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
