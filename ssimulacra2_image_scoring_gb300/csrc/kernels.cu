@@ -761,9 +761,11 @@ __global__ void __launch_bounds__(kVWarps * 32)
     return reinterpret_cast<const float4 *>(sm.quad[slot])[r * kVCols + lane];
   };
   // XYB rows of this lane's column (pitch padding keeps every lane in bounds)
-  const long long pitch = g.pitch[s];
-  const float *x1p = X + (long long)frame * g.x_fs + g.xoff[s] + c * g.plane[s] + col0 + lane;
-  const float *x2p = x1p + 3 * g.plane[s];
+  // (32-bit indices inside this (frame, scale) block: its six planes hold at
+  // most 6 x 2^28 floats)
+  const int pitch = g.pitch[s];
+  const float *xs = X + (long long)frame * g.x_fs + g.xoff[s];
+  const int xi1 = c * (int)g.plane[s] + col0 + lane, xi2 = xi1 + 3 * (int)g.plane[s];
 
   if (lane == 0) {
     for (int i = 0; i < kVSlots; ++i) mbar_init(&hbar[i], 1);
@@ -788,8 +790,8 @@ __global__ void __launch_bounds__(kVWarps * 32)
 #pragma unroll
     for (int j = 0; j < kVRows; ++j) {
       const int row = m * kVRows + j;
-      xa[j] = row < h ? __ldg(x1p + row * pitch) : 0.0f;
-      xb[j] = row < h ? __ldg(x2p + row * pitch) : 0.0f;
+      xa[j] = row < h ? __ldg(xs + (xi1 + row * pitch)) : 0.0f;
+      xb[j] = row < h ? __ldg(xs + (xi2 + row * pitch)) : 0.0f;
     }
   };
 
