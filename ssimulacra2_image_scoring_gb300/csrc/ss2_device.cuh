@@ -203,9 +203,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // paths.  cbrt_fast:
 //   1. y0 = 2^(log2(x) / 3) from the hardware approximations (within about
 //      2^-20 relative).
-//   2. The residual R = x - y0^3 to about 2^-46 x: y0^2 = p + e and
-//      y0 p = q + f exactly (fma), x - q exact by Sterbenz, then f and y0 e
-//      taken off (the latter in one fma).
+//   2. The residual R = x - y0^3 to about 2^-43 x: y0^2 = p + e exactly
+//      (fma), then x - y0 p and the y0 e term each in one fma (the product
+//      exact inside it); R is below about 2^-19 x, so each of the two
+//      roundings is below about 2^-44 x.
 //   3. One Newton step y0 + R / (3 y0^2), whose error is about 2^-41 y0,
 //      with the rounding error of the final addition kept exactly
 //      (quick_two_sum: the correction is below 2^-19 y0): the root lies at
@@ -222,9 +223,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ float cbrt_fast(float x, bool &settled) {
   const float y0 = ex2_approx(__fmul_rn(lg2_approx(x), 0.333333343f));
   const ff p = two_prod(y0, y0);
-  const ff q = two_prod(y0, p.hi);
-  float r = __fsub_rn(x, q.hi);
-  r = __fsub_rn(r, q.lo);
+  float r = __fmaf_rn(-y0, p.hi, x);
   r = __fmaf_rn(-y0, p.lo, r);
   const float d = __fmul_rn(r, rcp_approx(__fmul_rn(3.0f, p.hi)));
   const ff y = quick_two_sum(y0, d);
