@@ -207,10 +207,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 //      (fma), then x - y0 p and the y0 e term each in one fma (the product
 //      exact inside it); R is below about 2^-19 x, so each of the two
 //      roundings is below about 2^-44 x.
-//   3. One Newton step y0 + R / (3 y0^2), whose error is about 2^-41 y0,
-//      with the rounding error of the final addition kept exactly
-//      (quick_two_sum: the correction is below 2^-19 y0): the root lies at
-//      y.hi + y.lo, give or take 2^-41 y0.
+//   3. One Newton step y0 + R k, k = 1 / (3 y0^2), whose error is about
+//      2^-41 y0: y.hi = fma(R, k, y0) rounds the step once, and y.lo =
+//      fma(R, k, y0 - y.hi) is its rounding error to within 2^-24 of itself
+//      (y0 - y.hi is exact by Sterbenz, the correction being below 2^-19 y0):
+//      the root lies at y.hi + y.lo, give or take 2^-41 y0.
 //   4. y.hi is the nearest float when y.lo is below half the float spacing
 //      on its side of y.hi, with a margin that covers that 2^-41: one fma
 //      decides it, y.hi + y.lo (1 + 2^-13) rounding back to y.hi (rounding
@@ -225,8 +226,9 @@ __device__ __forceinline__ float cbrt_fast(float x, bool &settled) {
   const ff p = two_prod(y0, y0);
   float r = __fmaf_rn(-y0, p.hi, x);
   r = __fmaf_rn(-y0, p.lo, r);
-  const float d = __fmul_rn(r, rcp_approx(__fmul_rn(3.0f, p.hi)));
-  const ff y = quick_two_sum(y0, d);
+  const float k = rcp_approx(__fmul_rn(3.0f, p.hi));
+  const float hi = __fmaf_rn(r, k, y0);
+  const ff y = {hi, __fmaf_rn(r, k, __fsub_rn(y0, hi))};
   // x >= 2^-100 (x is not negative here; zeros fail the test)
   settled = x >= 7.8886090522101181e-31f && __fmaf_rn(y.lo, 1.0001220703125f, y.hi) == y.hi;
   return y.hi;
