@@ -23,6 +23,7 @@
 #include <utility>
 
 #include "ss2_device.cuh"
+#include "ss2_f32x2.cuh"
 #include "ss2_tma.cuh"
 #include "ss2_impl.h"
 #include "ss2_kernels.h"
@@ -438,6 +439,46 @@ __device__ __forceinline__ void res_zero(Res3 &r) {
   for (int k = 0; k < 3; ++k) r.prev[k] = r.cur[k] = 0.0f;
 }
 
+// The same recursion on two quantities at once, in packed fp32 pairs
+// (fma.rn.f32x2, add.rn.f32x2).  The pair instructions have no negation, so
+// the state is kept as Z_t = s_t Y_t with the sign pattern s = (+, +, -, -)
+// repeating over the step index t: s_t s_{t-2} = -1 for every t, so the
+// -Y_{t-2} term becomes +Z_{t-2}, and the other two coefficients take a sign
+// fixed by t mod 4 (c2 times s_t s_{t-1}: - for even t, + for odd; g times
+// s_t).  Round-to-nearest is symmetric, so s_t Z_t and the returned sum
+// times s_t equal the scalar recursion's values bit for bit.  m = t mod 4
+// must fold to a constant at every call (the callers' loops are unrolled).
+struct Res3x2 {
+  f2 prev[3], cur[3];
+};
+struct ResConsts2 {
+  f2 cp[3], cn[3], gp[3], gn[3];  // +c2, -c2, +g, -g in both halves
+};
+
+__device__ __forceinline__ void res2_init(Res3x2 &r, ResConsts2 &k, const Pix &px) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    r.prev[i] = r.cur[i] = f2_pack(0.0f, 0.0f);
+    k.cp[i] = f2_pack(px.iir_c2[i], px.iir_c2[i]);
+    k.cn[i] = f2_pack(-px.iir_c2[i], -px.iir_c2[i]);
+    k.gp[i] = f2_pack(px.iir_g[i], px.iir_g[i]);
+    k.gn[i] = f2_pack(-px.iir_g[i], -px.iir_g[i]);
+  }
+}
+
+// One step at t = m mod 4; returns s_t times the output sum (Y0 + Y1) + Y2.
+__device__ __forceinline__ f2 res2_step(Res3x2 &r, const ResConsts2 &k, int m, f2 in) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const f2 cc = (m & 1) ? k.cp[i] : k.cn[i];
+    const f2 gg = (m & 2) ? k.gn[i] : k.gp[i];
+    const f2 n = f2_fma(cc, r.cur[i], f2_fma(gg, in, r.prev[i]));
+    r.prev[i] = r.cur[i];
+    r.cur[i] = n;
+  }
+  return f2_add(f2_add(r.cur[0], r.cur[1]), r.cur[2]);
+}
+
 // ---------------------------------------------------------------------------
 // k_hblur: one warp per 32 rows of one (frame, scale, channel); lane = row.
 //
@@ -756,10 +797,6 @@ __global__ void __launch_bounds__(kVWarps * 32)
   uint64_t *hbar = reinterpret_cast<uint64_t *>(vsm + kVWarps * sizeof(VWarpSmem)) + warp * 4;
   const CUtensorMap *mq = &maps.vq4[s];
   const CUtensorMap *ms = &maps.vs1[s];
-  // this lane's quad of row r of a slot (rows of 32 quads, unswizzled)
-  auto quad_at = [&](int slot, int r) -> float4 {
-    return reinterpret_cast<const float4 *>(sm.quad[slot])[r * kVCols + lane];
-  };
   // XYB rows of this lane's column (pitch padding keeps every lane in bounds)
   // (32-bit indices inside this (frame, scale) block: its six planes hold at
   // most 6 x 2^28 floats)
@@ -798,9 +835,18 @@ __global__ void __launch_bounds__(kVWarps * 32)
   Acc6 acc;
 #pragma unroll
   for (int k = 0; k < kNSum; ++k) acc.v[k] = {0.0f, 0.0f};
-  Res3 r[kNq];
-#pragma unroll
-  for (int q = 0; q < kNq; ++q) res_zero(r[q]);
+  // (mu1, mu2) and (s11, s22) recurse as packed pairs, s12 alone
+  Res3x2 rm, rs;
+  ResConsts2 rk;
+  res2_init(rm, rk, px);
+  res2_init(rs, rk, px);
+  Res3 r12;
+  res_zero(r12);
+  const f2 zero2 = f2_pack(0.0f, 0.0f);
+  // this lane's quad of row r of a slot as two pairs
+  auto pairs_at = [&](int slot, int r) -> ulonglong2 {
+    return reinterpret_cast<const ulonglong2 *>(sm.quad[slot])[r * kVCols + lane];
+  };
   float xc1[kVRows], xc2[kVRows];
   load_x(0, xc1, xc2);
 
@@ -810,11 +856,11 @@ __global__ void __launch_bounds__(kVWarps * 32)
   }
   // warm-up steps producing Y[-4] .. Y[-1]: rows 0..3 ahead, zeros behind
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float4 a = quad_at(slot_of(0), j);
-    const float in[kNq] = {a.x, a.y, a.z, a.w, sm.s12[slot_of(0)][j * kVCols + lane]};
-#pragma unroll
-    for (int q = 0; q < kNq; ++q) res_step(r[q], px, __fadd_rn(in[q], 0.0f));
+  for (int j = 0; j < 4; ++j) {  // steps t = 0..3
+    const ulonglong2 a = pairs_at(slot_of(0), j);
+    res2_step(rm, rk, j, f2_add(a.x, zero2));
+    res2_step(rs, rk, j, f2_add(a.y, zero2));
+    res_step(r12, px, __fadd_rn(sm.s12[slot_of(0)][j * kVCols + lane], 0.0f));
   }
 
   for (int k = 0; k < nchunk; ++k) {
@@ -830,12 +876,18 @@ __global__ void __launch_bounds__(kVWarps * 32)
       // ahead row 8k + j + 4, behind row 8k + j - 6
       const int sa = j < 4 ? sk : sn, ra = j < 4 ? j + 4 : j - 4;
       const int sb = j < 6 ? sp : sk, rb = j < 6 ? j + 2 : j - 6;
-      const float4 qa = quad_at(sa, ra), qb = quad_at(sb, rb);
-      const float ina[kNq] = {qa.x, qa.y, qa.z, qa.w, sm.s12[sa][ra * kVCols + lane]};
-      const float inb[kNq] = {qb.x, qb.y, qb.z, qb.w, sm.s12[sb][rb * kVCols + lane]};
+      const ulonglong2 qa = pairs_at(sa, ra), qb = pairs_at(sb, rb);
+      // step t = 4 + 8k + j, so t mod 4 = j mod 4; the pairs carry s_t
+      const f2 om = res2_step(rm, rk, j, f2_add(qa.x, qb.x));
+      const f2 os = res2_step(rs, rk, j, f2_add(qa.y, qb.y));
       float o[kNq];
+      f2_unpack(om, o[0], o[1]);
+      f2_unpack(os, o[2], o[3]);
+      if (j & 2) {
 #pragma unroll
-      for (int q = 0; q < kNq; ++q) o[q] = res_step(r[q], px, __fadd_rn(ina[q], inb[q]));
+        for (int q = 0; q < 4; ++q) o[q] = -o[q];
+      }
+      o[4] = res_step(r12, px, __fadd_rn(sm.s12[sa][ra * kVCols + lane], sm.s12[sb][rb * kVCols + lane]));
       if (j == 5) {
         // chunk k - 1 is read for the last time: refill its slot with k + 2
         // (the reads are ordered before the async-proxy refill by a proxy

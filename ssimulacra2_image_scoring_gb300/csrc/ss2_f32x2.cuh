@@ -19,6 +19,13 @@ __device__ __forceinline__ void f2_unpack(f2 v, float &lo, float &hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
 
+// a + b per half, one rounding each (add.rn.f32x2)
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // a * b + c per half, one rounding each (fma.rn.f32x2)
 __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
   f2 d;
