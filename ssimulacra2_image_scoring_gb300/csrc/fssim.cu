@@ -479,7 +479,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // a * b per half, one rounding each (mul.rn.f32x2): the same bits as two
-// scalar __fmul_rn
+// scalar __fmul_rn.  Its results here only feed fma multiplicands, which
+// cannot absorb it (a pair product feeding a pair add is contracted into
+// one fused operation despite .rn).
 __device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
   f2 d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));

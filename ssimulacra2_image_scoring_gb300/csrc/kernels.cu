@@ -570,9 +570,14 @@ __global__ void __launch_bounds__(kHWarps * 32)
     }
   };
 
-  Res3 r[kNq];
-#pragma unroll
-  for (int q = 0; q < kNq; ++q) res_zero(r[q]);
+  // (mu1, mu2) and (s11, s22) recurse as packed pairs, s12 alone
+  Res3x2 rm, rs;
+  ResConsts2 rk;
+  res2_init(rm, rk, px);
+  res2_init(rs, rk, px);
+  Res3 r12;
+  res_zero(r12);
+  const f2 zero2 = f2_pack(0.0f, 0.0f);
 
   // rolling 4-column groups of both planes: gm0 = cols 8k-8..8k-5,
   // gm1 = 8k-4..8k-1, g0 = 8k..8k+3 (all zero before column 0)
@@ -589,15 +594,10 @@ __global__ void __launch_bounds__(kHWarps * 32)
     const float a1[4] = {g0[0].x, g0[0].y, g0[0].z, g0[0].w};
     const float a2[4] = {g0[1].x, g0[1].y, g0[1].z, g0[1].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float in[kNq];
-      in[0] = __fadd_rn(a1[j], 0.0f);
-      in[1] = __fadd_rn(a2[j], 0.0f);
-      in[2] = __fadd_rn(__fmul_rn(a1[j], a1[j]), 0.0f);
-      in[3] = __fadd_rn(__fmul_rn(a2[j], a2[j]), 0.0f);
-      in[4] = __fadd_rn(__fmul_rn(a1[j], a2[j]), 0.0f);
-#pragma unroll
-      for (int q = 0; q < kNq; ++q) res_step(r[q], px, in[q]);
+    for (int j = 0; j < 4; ++j) {  // steps t = 0..3
+      res2_step(rm, rk, j, f2_add(f2_pack(a1[j], a2[j]), zero2));
+      res2_step(rs, rk, j, f2_add(f2_pack(__fmul_rn(a1[j], a1[j]), __fmul_rn(a2[j], a2[j])), zero2));
+      res_step(r12, px, __fadd_rn(__fmul_rn(a1[j], a2[j]), 0.0f));
     }
   }
 
@@ -618,7 +618,8 @@ __global__ void __launch_bounds__(kHWarps * 32)
     fence_async_smem();
     __syncwarp();
     if (lane == 0 && k + kHSlots <= nchunk) issue(k + kHSlots);
-    float o[kNq][kBoxCols];
+    f2 om[kBoxCols], os[kBoxCols];  // (mu1, mu2), (s11, s22)
+    float o12[kBoxCols];
     {
       // step producing Y[8k + j] takes x[8k + j + 4] + x[8k + j - 6]
       const float ah1[8] = {g1[0].x, g1[0].y, g1[0].z, g1[0].w, gn[0].x, gn[0].y, gn[0].z, gn[0].w};
@@ -627,14 +628,21 @@ __global__ void __launch_bounds__(kHWarps * 32)
       const float bh2[8] = {gm0[1].z, gm0[1].w, gm1[1].x, gm1[1].y, gm1[1].z, gm1[1].w, g0[1].x, g0[1].y};
 #pragma unroll
       for (int j = 0; j < kBoxCols; ++j) {
-        float in[kNq];
-        in[0] = __fadd_rn(ah1[j], bh1[j]);
-        in[1] = __fadd_rn(ah2[j], bh2[j]);
-        in[2] = __fadd_rn(__fmul_rn(ah1[j], ah1[j]), __fmul_rn(bh1[j], bh1[j]));
-        in[3] = __fadd_rn(__fmul_rn(ah2[j], ah2[j]), __fmul_rn(bh2[j], bh2[j]));
-        in[4] = __fadd_rn(__fmul_rn(ah1[j], ah2[j]), __fmul_rn(bh1[j], bh2[j]));
-#pragma unroll
-        for (int q = 0; q < kNq; ++q) o[q][j] = res_step(r[q], px, in[q]);
+        // step t = 4 + 8k + j, so t mod 4 = j mod 4; the pairs carry s_t,
+        // taken off by 0 - v where s_t = -1 (a zero stays +0, as in the
+        // scalar recursion)
+        // (the squares are scalar products: a pair product feeding a pair
+        // sum is contracted into one fused operation, which would skip the
+        // squares' own rounding)
+        const f2 sa = f2_pack(__fmul_rn(ah1[j], ah1[j]), __fmul_rn(ah2[j], ah2[j]));
+        const f2 sb = f2_pack(__fmul_rn(bh1[j], bh1[j]), __fmul_rn(bh2[j], bh2[j]));
+        om[j] = res2_step(rm, rk, j, f2_add(f2_pack(ah1[j], ah2[j]), f2_pack(bh1[j], bh2[j])));
+        os[j] = res2_step(rs, rk, j, f2_add(sa, sb));
+        if (j & 2) {
+          om[j] = f2_sub(zero2, om[j]);
+          os[j] = f2_sub(zero2, os[j]);
+        }
+        o12[j] = res_step(r12, px, __fadd_rn(__fmul_rn(ah1[j], ah2[j]), __fmul_rn(bh1[j], bh2[j])));
       }
     }
 #pragma unroll
@@ -651,11 +659,15 @@ __global__ void __launch_bounds__(kHWarps * 32)
     // (eight lanes of a phase hit eight different units of their lines)
     float4 *dq = reinterpret_cast<float4 *>(sm.quad[ob]);
 #pragma unroll
-    for (int j = 0; j < kBoxCols; ++j)
-      dq[swz128(lane * kBoxCols + j)] = make_float4(o[0][j], o[1][j], o[2][j], o[3][j]);
+    for (int j = 0; j < kBoxCols; ++j) {
+      float4 v;
+      f2_unpack(om[j], v.x, v.y);
+      f2_unpack(os[j], v.z, v.w);
+      dq[swz128(lane * kBoxCols + j)] = v;
+    }
     float4 *ds = reinterpret_cast<float4 *>(sm.s12[ob]);
-    ds[swz32(2 * lane)] = make_float4(o[4][0], o[4][1], o[4][2], o[4][3]);
-    ds[swz32(2 * lane + 1)] = make_float4(o[4][4], o[4][5], o[4][6], o[4][7]);
+    ds[swz32(2 * lane)] = make_float4(o12[0], o12[1], o12[2], o12[3]);
+    ds[swz32(2 * lane + 1)] = make_float4(o12[4], o12[5], o12[6], o12[7]);
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {

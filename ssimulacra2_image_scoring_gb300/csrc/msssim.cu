@@ -128,7 +128,9 @@ __device__ __forceinline__ float div_by(float a, float b, float rb) {
 __device__ __forceinline__ float div_fast(float a, float b) { return div_by(a, b, rcp_approx(b)); }
 
 // a * b per half, one rounding each (mul.rn.f32x2): the same bits as two
-// scalar __fmul_rn
+// scalar __fmul_rn.  Its results here only feed fma multiplicands, which
+// cannot absorb it (a pair product feeding a pair add is contracted into
+// one fused operation despite .rn).
 __device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
   f2 d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
