@@ -108,7 +108,7 @@ def byte_model(spec) -> dict:
 # DRAM traffic from the committed ncu summary of a kernel
 # ---------------------------------------------------------------------------
 
-KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h"]
+KERNEL_SOURCES = ["kernels.cu", "ss2_device.cuh", "ss2_tma.cuh", "ss2_impl.h", "ss2_f32x2.cuh"]
 FSSIM_SOURCES = ["fssim.cu", "ss2_tma.cuh", "ss2_f32x2.cuh"]
 MSSSIM_SOURCES = ["msssim.cu", "ss2_f32x2.cuh"]
 CAMBI_SOURCES = ["cambi.cu"]
