@@ -75,6 +75,7 @@ struct StageGeo {
   static constexpr int crows = SY ? 1 : 2;            // chroma rows per luma row pair
   static constexpr int img_bytes = 2 * ybytes + 2 * crows * cbytes;  // a multiple of 16
   static constexpr int buf_bytes = 2 * img_bytes;     // both frames
+  static_assert(buf_bytes % 128 == 0, "a whole number of 4-byte words per lane");
   // the staging (two buffers per warp) shares its region with scales 2-5
   static constexpr int stage_bytes = kPyrWarps * 2 * buf_bytes;
   static constexpr int union_bytes =
@@ -173,18 +174,44 @@ __global__ void __launch_bounds__(kPyrThreads, 4)
       }
       cp_async_commit();  // possibly empty: keeps one group per row pair
     } else if (r0 < g.h) {
-      for (int e = lane; e < buf_bytes / BPS; e += 32) {
-        int off = e * BPS;
+      // rows that do not all start on 16 bytes: 4-byte words, each the
+      // funnel shift of the two aligned words that cover it.  A word whose
+      // first byte lies outside its row is skipped (nothing reads it); one
+      // whose first byte is inside may run past the row's end into bytes
+      // that nothing reads, so the aligned loads are only taken when both
+      // lie inside the frame, and a word at the frame's first or last bytes
+      // is read sample by sample up to the frame's end.  The segments (luma
+      // and chroma rows) are multiples of 4 bytes, so no word spans two.
+#pragma unroll
+      for (int it = 0; it < buf_bytes / 128; ++it) {
+        const int e = lane + 32 * it;
+        int off = e * 4;
         const int img = off >= SG::img_bytes;
         off -= img ? SG::img_bytes : 0;
+        const uint8_t *f = img ? fdis : fref;
         bool ok;
-        const uint8_t *src = stage_src<BPS, SX, SY>(g, img ? fdis : fref, tx0, r0, off, ok);
-        if (ok) {
-          if (BPS == 1)
-            dst[e] = __ldg(src);
-          else
-            reinterpret_cast<uint16_t *>(dst)[e] = __ldg(reinterpret_cast<const uint16_t *>(src));
+        const uint8_t *src = stage_src<BPS, SX, SY>(g, f, tx0, r0, off, ok);
+        if (!ok) continue;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+        const uintptr_t a = sa & ~uintptr_t(3);
+        const uint32_t sh = (uint32_t)(sa & 3u) * 8u;
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(f);
+        const uintptr_t hi = lo + (uintptr_t)g.frame_bytes;
+        uint32_t w = 0;
+        if (a >= lo && a + (sh ? 8u : 4u) <= hi) {
+          const uint32_t *wp = reinterpret_cast<const uint32_t *>(a);
+          const uint32_t w0 = __ldg(wp);
+          const uint32_t w1 = sh ? __ldg(wp + 1) : 0u;
+          w = __funnelshift_r(w0, w1, sh);
+        } else {
+          for (int b = 0; b < 4; b += BPS)
+            if (sa + (uintptr_t)b < hi) {
+              const uint32_t v = BPS == 1 ? (uint32_t)__ldg(src + b)
+                                          : (uint32_t)__ldg(reinterpret_cast<const uint16_t *>(src + b));
+              w |= v << (8 * b);
+            }
         }
+        reinterpret_cast<uint32_t *>(dst)[e] = w;
       }
     }
   };

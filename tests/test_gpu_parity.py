@@ -65,7 +65,8 @@ GEOMS = [
     # (w, h, depth, chroma): ragged tails, odd sizes, every chroma layout.
     # Rows whose starts all fall on 16 bytes take the pyramid kernel's
     # 16-byte staging copies (64x48, 224x100, 224x101, 96x70, 80x72); the
-    # others take its sample-by-sample staging.
+    # others take its 4-byte word staging (aligned loads inside the frame,
+    # single samples at a frame's ends).
     (64, 48, 8, 420),
     (853, 481, 8, 444),
     (17, 13, 10, 444),
