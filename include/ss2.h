@@ -168,6 +168,29 @@ int ss2_debug_cbrt(const float *x, float *y, long long n, void *stream);
 int ss2_debug_cbrt_host(const float *x, float *y, long long n);
 
 /*
+ * ss2_set_graphs — how ss2_score_frames and ss2_values launch their work
+ * (CUDA graphs, a launch mechanism, not a step of the method).
+ * enable = 0 (the default): every kernel is launched one by one.
+ * enable != 0: a context's first device-input call launches its kernels
+ * one by one; a later call captures the call's whole launch
+ * sequence (both lanes' kernels, the score and value read-backs and the
+ * error-word read) as a CUDA graph on a stream of the context's own, then
+ * replays it with one graph launch on the caller's stream, and so do the
+ * calls after it while the frame pointers, the frame count, the outputs
+ * asked for and the profiling state stay the same; any change captures
+ * again, and ss2_set_params drops the graph.  A capture that the runtime
+ * refuses returns the context to one-by-one launches.  The kernels and
+ * their inputs are the same in both modes, so are the results, bit for bit.
+ * With ss2_profile_begin on, the captured launches carry timing events and
+ * ss2_profile_end counts them like the others.  ss2_score_frames_host
+ * always launches one by one.  Replays measured no faster on GB300 at the
+ * sizes tried, 576x324 to 3840x2160 (a call's time is its kernels' serial
+ * walks, not their launches), hence the default.  Returns 0, or -EINVAL for
+ * a NULL context.
+ */
+int ss2_set_graphs(ss2_ctx *ctx, int enable);
+
+/*
  * ss2_profile_begin / ss2_profile_end — per-kernel device timing.  Between
  * the two calls every kernel launch of the context is bracketed by a pair of
  * CUDA events on its launching stream.  ss2_profile_end waits for those

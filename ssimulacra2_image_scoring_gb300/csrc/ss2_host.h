@@ -49,6 +49,15 @@ class KernelTimer {
   void begin() {
     on_ = true;
     used_.clear();
+    added_.clear();
+  }
+
+  bool on() const { return on_; }
+
+  // Adds one launch of class cls timed outside the event pool (the timing
+  // events of a replayed CUDA graph, read after its stream synchronised).
+  void add(int cls, float ms) {
+    if (on_) added_.push_back({cls, ms});
   }
 
   // Records the start (start = true) or end event of one launch of class cls.
@@ -87,8 +96,14 @@ class KernelTimer {
         n[(size_t)u.first] += 1;
       }
     }
+    for (const auto &a : added_)
+      if (a.first >= 0 && a.first < ncls) {
+        t[(size_t)a.first] += a.second;
+        n[(size_t)a.first] += 1;
+      }
     on_ = false;
     used_.clear();
+    added_.clear();
     if (e != cudaSuccess) return e;
     for (int i = 0; i < ncls; ++i) {
       if (ms) ms[i] = t[(size_t)i];
@@ -101,6 +116,7 @@ class KernelTimer {
   bool on_ = false;
   std::vector<cudaEvent_t> pool_;
   std::vector<std::pair<int, size_t>> used_;  // (kernel class, index of the start event)
+  std::vector<std::pair<int, float>> added_;  // (kernel class, milliseconds)
 };
 
 }  // namespace ss2

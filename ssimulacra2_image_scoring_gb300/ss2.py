@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
             L.ss2_profile_begin.restype = i
             L.ss2_profile_end.argtypes = [vp, vp, vp]
             L.ss2_profile_end.restype = i
+            L.ss2_set_graphs.argtypes = [vp, i]
+            L.ss2_set_graphs.restype = i
             L.ss2_score_frames_noalloc.argtypes = [i, i, i, i, vp, vp, i, vp, vp]
             L.ss2_score_frames_noalloc.restype = i
             L.ss2_debug_wait_probe.argtypes = [ctypes.c_uint, vp]
@@ -472,6 +474,11 @@ class Scorer(_Context):
     def set_params(self, params: np.ndarray) -> None:
         p = np.ascontiguousarray(params, np.float64)
         _check(lib().ss2_set_params(self.handle, p.ctypes.data, p.size))
+
+    def set_graphs(self, enable: bool) -> None:
+        """Replays repeated device-input calls from a captured CUDA graph, or
+        launches every kernel one by one (the default)."""
+        _check(lib().ss2_set_graphs(self.handle, 1 if enable else 0))
 
     # -- scoring -----------------------------------------------------------
     def _frames(self, t) -> int:

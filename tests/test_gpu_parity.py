@@ -184,6 +184,42 @@ def test_determinism_and_batch_invariance(cuda):
     assert np.array_equal(s1, s3) and np.array_equal(v1, v3)
 
 
+def test_graph_replay_matches_eager_launches(cuda):
+    """Device-input calls replayed from a captured CUDA graph give the bits of
+    one-by-one launches: repeated calls, another frame count, with and without
+    the values, under per-kernel timing (the same launches counted) and after
+    new parameters (which drop the graph)."""
+    wl = synth.custom(200, 97, 11, 420, 5, seed=23)
+    ref, dis = _to_dev(wl.ref), _to_dev(wl.dis)
+    with _scorer(wl.spec, batch=2) as sc:      # three batches over both lanes
+        sc.set_graphs(False)
+        v0, s0 = sc.values(ref, dis)
+        sc.profile_begin()
+        sc.score(ref, dis)
+        sc.score(ref, dis)
+        prof_eager = sc.profile_end()
+        sc.set_graphs(True)
+        for _ in range(3):                     # capture, then replays
+            v, s = sc.values(ref, dis)
+            assert np.array_equal(v, v0) and np.array_equal(s, s0)
+            assert np.array_equal(sc.score(ref, dis), s0)
+        assert np.array_equal(sc.score(ref[:3], dis[:3]), s0[:3])
+        sc.profile_begin()
+        sc.score(ref, dis)
+        sc.score(ref, dis)
+        prof_graph = sc.profile_end()
+        assert {k: n for k, (_, n) in prof_graph.items()} == \
+               {k: n for k, (_, n) in prof_eager.items()}
+        assert all(ms > 0.0 for ms, _ in prof_graph.values())
+        p = oracle.default_params()
+        p[132] = 0.002                         # C2
+        sc.set_params(p)
+        s_new = sc.score(ref, dis)
+        sc.set_graphs(False)
+        assert np.array_equal(sc.score(ref, dis), s_new)
+    assert not np.array_equal(s_new, s0)
+
+
 def test_host_input_path_matches_device_path_and_oracle(cuda):
     """The host-input path (pinned and pageable frames, calls shorter than its
     short first batch) against the device-input path bitwise, and against the
