@@ -965,9 +965,11 @@ __global__ void __launch_bounds__(kVWarps * 32)
 
 // ---------------------------------------------------------------------------
 // k_finalize: one block per frame.  Thread j < 108 owns value j: it adds the
-// warp partials of its (scale, channel, sum) in index order, then forms the
-// 1-norm (mean) or 4-norm (fourth root of the mean fourth power) in fp64.
-// Thread 0 pools: P = sum_i w_i |v_i| in index order, then the map.
+// warp partials of its (scale, channel, sum) in index order, forms the
+// 1-norm (mean) or 4-norm (fourth root of the mean fourth power) in fp64 and
+// its pooling term w_j |v_j|.  Thread 0 pools: P = sum_i w_i |v_i| in index
+// order (the terms formed in parallel, the additions one after another, as
+// the sequential sum rounds them), then the map.
 // With an error word given and set, the batch's values and scores are NaN.
 // ---------------------------------------------------------------------------
 
@@ -975,7 +977,7 @@ __global__ void __launch_bounds__(128)
     k_finalize(Geom g, const float2 *__restrict__ part, const double *__restrict__ params,
                double *__restrict__ values, double *__restrict__ scores,
                const int *__restrict__ err) {
-  __shared__ double v[kNValues];
+  __shared__ double wv[kNValues];  // the pooling terms w_j |v_j|
   const int frame = blockIdx.x;
   const int j = threadIdx.x;
   if (err && *err != 0) {
@@ -999,16 +1001,13 @@ __global__ void __launch_bounds__(128)
       const double N = (double)g.ws[s] * (double)g.hs[s];
       out = n == 0 ? S / N : sqrt(sqrt(S / N));
     }
-    v[j] = out;
     values[(long long)frame * kNValues + j] = out;
+    wv[j] = params[kPWeights + j] * fabs(out);
   }
   __syncthreads();
   if (j == 0) {
     double P = 0.0;
-    for (int i = 0; i < kNValues; ++i) {
-      const double t = params[kPWeights + i] * fabs(v[i]);
-      P = P + t;
-    }
+    for (int i = 0; i < kNValues; ++i) P = P + wv[i];
     const double *pc = params + kPPoly;
     double sc = pc[3] * P;
     sc = sc + pc[2];
