@@ -96,6 +96,30 @@ def test_planes_bitwise(cuda, geom):
                 f"horizontal blur differs at scale {s}"
 
 
+@pytest.mark.parametrize("geom", [(853, 481, 8, 444), (17, 13, 10, 444), (131, 67, 9, 444),
+                                  (201, 99, 8, 444)],
+                         ids=lambda g: "x".join(map(str, g)))
+def test_planes_bitwise_from_unaligned_frame(cuda, geom):
+    """Frame 1 of a batch whose frame size is not a multiple of 4 bytes,
+    handed over as a view that starts at that odd offset: the pyramid
+    kernel's word staging then meets every byte alignment and its
+    sample-by-sample reads at the frame's first and last bytes."""
+    w, h, d, c = geom
+    wl = synth.custom(w, h, d, c, 2, seed=17)
+    ref, dis = _to_dev(wl.ref), _to_dev(wl.dis)
+    r1, d1 = ref[1:], dis[1:]
+    assert r1.data_ptr() % 4 != 0, "the case must start off a word boundary"
+    dims = oracle.scale_dims(w, h)
+    with _scorer(wl.spec) as sc:
+        for s in range(len(dims)):
+            xyb, hb = sc.debug_planes(r1, d1, s)
+            _, _, dump = oracle.score(wl.ref[1], wl.dis[1], w, h, d, c, dump_scale=s)
+            assert np.array_equal(xyb.view(np.uint32), dump["xyb"].view(np.uint32)), \
+                f"XYB differs at scale {s}"
+            assert np.array_equal(hb.view(np.uint32), dump["hblur"].view(np.uint32)), \
+                f"horizontal blur differs at scale {s}"
+
+
 @pytest.mark.parametrize("geom", GEOMS, ids=lambda g: "x".join(map(str, g)))
 def test_linear_pyramid_bitwise(cuda, geom):
     """Linear RGB at scale 0 and the 2x2-downsampled linear RGB of scales 1-5
