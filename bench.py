@@ -5,11 +5,13 @@ synthetic stand-in for the pages' Big Buck Bunny 4K fixture) through the
 C ABI.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline]
+                  [--workload NAME] [--no-cpu-baseline] [--graphs]
                   [--feature ssimulacra2|fssim|msssim|cambi] [--frames N] [--batch B]
 
 --feature fssim times float_ssim with device decimation instead (frames/s on
-the same workload; the oracle's float_ssim as the CPU baseline); --feature
+the same workload; the oracle's float_ssim as the CPU baseline); --graphs
+replays each device-input call of the timed steps from a captured CUDA graph
+(off by default; it measured no faster); --feature
 msssim times MS-SSIM of the luma and both chroma planes the same way; --feature cambi times
 CAMBI c-values and top-K pooling of the distorted luma as 10-bit levels.
 
@@ -393,8 +395,16 @@ def time_pipeline(spec, wl, args, ws, dev, steps: int, clocks=None) -> dict:
     batch = args.batch or (min(n, 1024) if args.frames else None)
     sc = Scorer(spec.width, spec.height, spec.depth, spec.chroma, batch=batch)
     stream = torch.cuda.current_stream()
+    if args.graphs:
+        # replay each call from a CUDA graph; the warm-up runs under
+        # per-kernel timing too, so the timed call's graph (its timing
+        # events included) is captured there and the timed steps only replay
+        sc.set_graphs(True)
+        sc.profile_begin()
     for _ in range(args.warmup):
         sc.score(ref, dis, stream)
+    if args.graphs:
+        sc.profile_end()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
@@ -550,6 +560,7 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": spec.name, "frames_per_step": n, "batch": batch,
+                   "launches": "cuda graph replays" if args.graphs else "one by one",
                    "l2": m["l2"]},
         "roofline": m["roofline"],
         "pipeline": m["pipeline"],
@@ -1024,6 +1035,8 @@ def main(argv=None) -> int:
                     help="all (default): after the headline workload, time the other four "
                          "workloads too and report each under 'workloads'; one: only "
                          "--workload")
+    ap.add_argument("--graphs", action="store_true",
+                    help="replay the scoring calls from captured CUDA graphs (ss2_set_graphs)")
     ap.add_argument("--batch", type=int, default=0,
                     help="frames per pass (default: the library's choice for the geometry)")
     ap.add_argument("--frames", type=int, default=0,
